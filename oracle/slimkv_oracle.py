@@ -1,0 +1,158 @@
+"""Oracle for SlimKV decode-step attention: plain, slow, float64, CPU.
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this module. The library's CUDA path
+never calls it and shares no code with it.
+
+Source: "Can SlimKV compress KV cache jointly across tokens and features"
+(wispaper.ai), section "Latent-space attention removes the rebuild step", which
+states the decode rule: RoPE stays on all queries and on raw-window keys; beacon
+keys carry no key-side RoPE and are cached only as latent rows C_K, C_V; scores
+against beacons are (Q' U_K) C_K^T with the query projection taken after
+grouped-query grouping; values aggregate as (A C_V) U_V^T, i.e. in latent form
+before the up-projection. The SlimKV abstract (omanscience.com citation record)
+restates the same: a K-RoPE-free constraint enables latent-space attention in
+decoding without full-dimensional reconstruction.
+
+Readings where the pages are silent (each also listed in the design notes):
+* RoPE pairs element i with element i + d/2 ("rotate-half"), with
+  theta_i = base^(-2i/d); no frequency remapping.
+* One softmax spans the beacon scores and the window scores of a query head.
+* The score scale is the same for both sets (1/sqrt(d) in every workload).
+* Query head h belongs to KV group g = h // (Hq / Hkv); U^(g) is the block of
+  rows g*d .. (g+1)*d of U, i.e. the part of the up-projection that produces
+  KV head g.
+* No masking: a decode query sees every beacon and every window token.
+
+Every function takes and returns float64 numpy arrays.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def rope_angles(d: int, pos: float, base: float) -> np.ndarray:
+    """Angles p * theta_i for i < d/2, theta_i = base^(-2i/d) (float64)."""
+    i = np.arange(d // 2, dtype=np.float64)
+    theta = np.power(float(base), -2.0 * i / d)
+    return float(pos) * theta
+
+
+def rope(x: np.ndarray, pos: float, base: float) -> np.ndarray:
+    """Rotate-half RoPE of the last axis of ``x`` at position ``pos``.
+
+    For i < d/2: x'_i = x_i cos(p th_i) - x_{i+d/2} sin(p th_i) and
+    x'_{i+d/2} = x_{i+d/2} cos(p th_i) + x_i sin(p th_i).
+    """
+    d = x.shape[-1]
+    h = d // 2
+    ang = rope_angles(d, pos, base)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :h], x[..., h:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def softmax_weights(scores: np.ndarray):
+    """Unnormalised weights w = exp(s - max s), their sum l and the max m."""
+    m = np.max(scores)
+    w = np.exp(scores - m)
+    return w, np.sum(w), m
+
+
+def _groups(Hq: int, Hkv: int) -> int:
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    return Hq // Hkv
+
+
+def _pairs(B, Hq, pairs):
+    return [(b, h) for b in range(B) for h in range(Hq)] if pairs is None else list(pairs)
+
+
+def decode_attn(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, scale, rope_base,
+                pairs=None, return_weights=False):
+    """Reconstruction-free decode attention for one layer.
+
+    q [B,Hq,d]; C_K [B,N_b,r_k]; C_V [B,N_b,r_v]; K_raw, V_raw [B,W,Hkv,d]
+    (keys stored after RoPE); U_K [Hkv*d,r_k]; U_V [Hkv*d,r_v]; q_pos [B].
+    Returns out [B,Hq,d] (rows not in ``pairs`` stay zero) and, with
+    ``return_weights``, the normalised weights of each computed (b, h).
+    For every (b, h), with g its KV group and p its position:
+      qr = RoPE(q[b,h], p)                 (query RoPE)
+      qt = qr . U_K^(g)                    (query projected into latent space)
+      s  = [scale * C_K[b] qt ; scale * K_raw[b,:,g] qr]   (one score vector)
+      A  = softmax(s)
+      out = (A_beacon . C_V[b]) . U_V^(g)T + A_window . V_raw[b,:,g]
+    """
+    B, Hq, d = q.shape
+    Hkv = U_K.shape[0] // d if U_K is not None else K_raw.shape[2]
+    G = _groups(Hq, Hkv)
+    N_b = 0 if C_K is None else C_K.shape[1]
+    out = np.zeros((B, Hq, d))
+    weights = {}
+    for b, h in _pairs(B, Hq, pairs):
+        g = h // G
+        qr = rope(q[b, h], q_pos[b], rope_base)
+        parts = []
+        if N_b:
+            UKg = U_K[g * d:(g + 1) * d, :]          # [d, r_k]
+            qt = qr @ UKg                            # (Q' U_K)
+            parts.append(scale * (C_K[b] @ qt))      # (Q' U_K) C_K^T
+        if K_raw is not None and K_raw.shape[1]:
+            parts.append(scale * (K_raw[b, :, g, :] @ qr))
+        s = np.concatenate(parts)
+        w, l, _ = softmax_weights(s)
+        o = np.zeros(d)
+        if N_b:
+            UVg = U_V[g * d:(g + 1) * d, :]          # [d, r_v]
+            z = w[:N_b] @ C_V[b]                     # (A C_V): latent aggregate
+            o = o + z @ UVg.T                        # ... then (.) U_V^T
+        if K_raw is not None and K_raw.shape[1]:
+            o = o + w[N_b:] @ V_raw[b, :, g, :]
+        out[b, h] = o / l
+        if return_weights:
+            weights[(b, h)] = w / l
+    return (out, weights) if return_weights else out
+
+
+def reconstruct_kv(C, U, Hkv: int, d: int):
+    """Explicit reconstruction C . U^T reshaped to [B, N_b, Hkv, d] (no RoPE)."""
+    B, N_b, _ = C.shape
+    return (C @ U.T).reshape(B, N_b, Hkv, d)
+
+
+def gqa_attn(q, K, V, q_pos, scale, rope_base, pairs=None):
+    """Standard RoPE GQA decode attention over a cache of RoPE'd keys.
+
+    q [B,Hq,d]; K, V [B,T,Hkv,d]. out[b,h] = softmax(scale * K[b,:,g] qr) V[b,:,g].
+    """
+    B, Hq, d = q.shape
+    Hkv = K.shape[2]
+    G = _groups(Hq, Hkv)
+    out = np.zeros((B, Hq, d))
+    for b, h in _pairs(B, Hq, pairs):
+        g = h // G
+        qr = rope(q[b, h], q_pos[b], rope_base)
+        s = scale * (K[b, :, g, :] @ qr)
+        w, l, _ = softmax_weights(s)
+        out[b, h] = (w @ V[b, :, g, :]) / l
+    return out
+
+
+def decode_attn_reconstruct(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, scale,
+                            rope_base, pairs=None):
+    """The feature-wise baseline: materialise K_b = C_K U_K^T and V_b = C_V U_V^T
+    at full dimension (beacon keys get no RoPE), then attend over beacons and the
+    raw window with standard GQA attention."""
+    d = q.shape[2]
+    Hkv = U_K.shape[0] // d
+    K_b = reconstruct_kv(C_K, U_K, Hkv, d)
+    V_b = reconstruct_kv(C_V, U_V, Hkv, d)
+    K = np.concatenate([K_b, K_raw], axis=1)
+    V = np.concatenate([V_b, V_raw], axis=1)
+    return gqa_attn(q, K, V, q_pos, scale, rope_base, pairs=pairs)
+
+
+def decode_attn_full_kv(q, K, V, q_pos, scale, rope_base, pairs=None):
+    """Uncompressed GQA decode over a full RoPE'd cache (the speed baseline)."""
+    return gqa_attn(q, K, V, q_pos, scale, rope_base, pairs=pairs)

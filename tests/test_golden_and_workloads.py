@@ -1,0 +1,58 @@
+"""Stored oracle outputs and the seeded workload recipes (CPU only)."""
+import os
+
+import numpy as np
+
+from latent_kv_cache_decode_b300 import workloads as wl
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def test_golden_config0_matches_oracle():
+    from tests.golden.make_golden import config0_arrays
+    lat, rec = config0_arrays()
+    g_lat = np.loadtxt(os.path.join(HERE, "golden", "config0_latent_out.txt"))
+    g_rec = np.loadtxt(os.path.join(HERE, "golden", "config0_reconstruct_out.txt"))
+    np.testing.assert_allclose(lat.reshape(g_lat.shape), g_lat, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(rec.reshape(g_rec.shape), g_rec, rtol=1e-14, atol=1e-15)
+    # the two formulations agree to float64 rounding
+    np.testing.assert_allclose(lat, rec, rtol=1e-11, atol=1e-12)
+
+
+def test_config_shapes_and_positions():
+    c1, c2, c3 = wl.config(1), wl.config(2), wl.config(3)
+    assert (c1.B, c1.Hq, c1.Hkv, c1.d, c1.N_b, c1.rank, c1.W, c1.layers) == (1, 32, 8, 128, 4096, 256, 1024, 32)
+    assert (c2.B, c2.N_b, c2.W, c2.q_pos) == (8, 8192, 2048, 8192 * 16 + 2048)
+    assert wl.config(0).q_pos == 2080
+    # 4 GiB of cache per 32-layer step at 128K / 16x
+    assert sum(wl.cache_bytes(c2, l) for l in range(c2.layers)) == 4 << 30
+    assert (c3.Hq, c3.Hkv, c3.layers) == (40, 8, 48)
+
+
+def test_qwen_ranks_recipe():
+    r = wl.config(3).ranks
+    assert len(r) == 48
+    assert all(x % 32 == 0 and 128 <= x <= 512 for x in r)
+    assert sum(r) == 48 * 256
+    assert r == wl._qwen_ranks(3, 48)          # deterministic
+
+
+def test_layer_tensors_deterministic_and_sliceable():
+    w = wl.custom(B=3, N_b=40, W=24, rank=32, Hq=4, Hkv=2, d=64)
+    a = wl.layer_tensors(w, 0)
+    b = wl.layer_tensors(w, 0, batch=[2])
+    for k in ("C_K", "C_V", "K_raw", "V_raw", "q"):
+        assert a[k].shape[0] == 3
+        assert bool((a[k][2:3] == b[k]).all())
+    assert bool((a["U_K"] == b["U_K"]).all())
+    u = wl.as_f64(a["U_K"])
+    # bf16-rounded orthonormal columns stay orthonormal to bf16 accuracy
+    assert np.abs(u.T @ u - np.eye(u.shape[1])).max() < 2e-2
+
+
+def test_peaked_keys_fraction():
+    w = wl.custom(B=1, W=2000, N_b=0, rank=32, peak_frac=0.01, peak_scale=8.0, dtype="f32")
+    k = wl.as_f64(wl.layer_tensors(w, 0)["K_raw"])[0]
+    norms = np.linalg.norm(k.reshape(2000, -1), axis=1)
+    big = norms > 4 * np.median(norms)
+    assert big.sum() == 20

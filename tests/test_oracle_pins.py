@@ -1,0 +1,322 @@
+"""Pins for the float64 oracle, each independent of the oracle's own code.
+
+The SlimKV pages print no worked example, so the oracle is pinned by what the
+mathematics fixes: closed forms, a second formulation of RoPE (complex
+multiplication), the relative-position identity RoPE is built for, reductions to
+torch's scaled_dot_product_attention (a library routine the oracle never calls),
+brute-force scalar loops written straight from the decode rule, and identities
+that the reconstruction-free rewrite must satisfy ((Q'U_K)C_K^T = Q'(C_K U_K^T)^T
+and (A C_V)U_V^T = A (C_V U_V^T), "Latent-space attention removes the rebuild
+step"). The mutation tests at the end plant typical mistakes in a copy of the
+oracle and check that some pin catches each of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import slimkv_oracle as O
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+def _ortho(rng, n, r):
+    qm, _ = np.linalg.qr(rng.standard_normal((n, r)))
+    return qm
+
+
+def _rope_complex(x, pos, base):
+    """RoPE as complex multiplication: z_i = x_i + 1j x_{i+d/2} times e^{i p th_i}."""
+    d = x.shape[-1]
+    h = d // 2
+    th = np.array([base ** (-(2.0 * i) / d) for i in range(h)])
+    z = (x[..., :h] + 1j * x[..., h:]) * np.exp(1j * pos * th)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def _sdpa(q, K, V, scale):
+    """torch fp64 SDPA for one decode query per (b, h); q [B,Hq,d], K/V [B,T,Hq,d]."""
+    qt = torch.from_numpy(q)[:, :, None, :]                  # [B,Hq,1,d]
+    kt = torch.from_numpy(K).permute(0, 2, 1, 3)             # [B,Hq,T,d]
+    vt = torch.from_numpy(V).permute(0, 2, 1, 3)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+    return o[:, :, 0, :].numpy()
+
+
+def _expand_heads(K, G):
+    return np.repeat(K, G, axis=2)       # contiguous grouping: head h -> g = h // G
+
+
+# ---------------------------------------------------------------- RoPE pins
+
+def test_rope_closed_form_d2():
+    # d = 2: one pair, theta_0 = 1, so position p rotates (x0, x1) by p radians
+    for p in (0.0, 1.0, 2.5, -3.0):
+        out = oracle.rope(np.array([1.0, 0.0]), p, 10000.0)
+        np.testing.assert_allclose(out, [math.cos(p), math.sin(p)], rtol=0, atol=1e-15)
+        out = oracle.rope(np.array([0.0, 1.0]), p, 10000.0)
+        np.testing.assert_allclose(out, [-math.sin(p), math.cos(p)], rtol=0, atol=1e-15)
+
+
+def test_rope_closed_form_frequencies():
+    # d = 4, base 100: theta = (1, 100^(-1/2)) = (1, 0.1)
+    x = np.array([1.0, 1.0, 0.0, 0.0])
+    out = oracle.rope(x, 2.0, 100.0)
+    np.testing.assert_allclose(out, [math.cos(2.0), math.cos(0.2), math.sin(2.0), math.sin(0.2)],
+                               atol=1e-15)
+
+
+def test_rope_matches_complex_multiplication():
+    rng = np.random.default_rng(1)
+    for d in (8, 64, 128):
+        x = _rand(rng, 5, d)
+        for pos in (0, 7, 2080, 133120):
+            # angles reach ~1.3e5 rad, whose float64 ulp is ~1.5e-11
+            np.testing.assert_allclose(oracle.rope(x, pos, 500000.0), _rope_complex(x, pos, 500000.0),
+                                       rtol=0, atol=1e-9)
+
+
+def test_rope_relative_position_and_norm():
+    rng = np.random.default_rng(2)
+    q, k = _rand(rng, 128), _rand(rng, 128)
+    for p, pp in ((2080, 2048), (133120, 131073), (5, 9)):
+        lhs = oracle.rope(q, p, 10000.0) @ oracle.rope(k, pp, 10000.0)
+        rhs = oracle.rope(q, p - pp, 10000.0) @ k
+        assert abs(lhs - rhs) < 1e-9 * (1 + abs(lhs))
+        assert abs(np.linalg.norm(oracle.rope(q, p, 10000.0)) - np.linalg.norm(q)) < 1e-12
+
+
+def test_rope_position_zero_is_identity():
+    x = np.random.default_rng(3).standard_normal((3, 64))
+    np.testing.assert_array_equal(oracle.rope(x, 0, 10000.0), x)
+
+
+# ------------------------------------------------------- attention-level pins
+
+def _case(seed, B=2, Hq=6, Hkv=2, d=16, N_b=20, W=11, r_k=8, r_v=12):
+    rng = np.random.default_rng(seed)
+    return dict(q=_rand(rng, B, Hq, d), C_K=_rand(rng, B, N_b, r_k), C_V=_rand(rng, B, N_b, r_v),
+                K_raw=_rand(rng, B, W, Hkv, d), V_raw=_rand(rng, B, W, Hkv, d),
+                U_K=_ortho(rng, Hkv * d, r_k), U_V=_ortho(rng, Hkv * d, r_v),
+                q_pos=np.array([37 + 5 * b for b in range(B)]), scale=1 / math.sqrt(d),
+                rope_base=10000.0)
+
+
+def test_latent_equals_explicit_reconstruction():
+    # associativity: (qU)c = q(cU^T) and (A C)U^T = A(C U^T); exact up to rounding
+    for seed in range(3):
+        c = _case(seed)
+        a = oracle.decode_attn(**c)
+        b = oracle.decode_attn_reconstruct(**c)
+        np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
+
+
+def test_empty_beacon_set_is_rope_gqa_attention():
+    c = _case(4, N_b=0)
+    out = oracle.decode_attn(**c)
+    G = c["q"].shape[1] // c["K_raw"].shape[2]
+    qr = np.stack([_rope_complex(c["q"][b], c["q_pos"][b], c["rope_base"]) for b in range(2)])
+    ref = _sdpa(qr, _expand_heads(c["K_raw"], G), _expand_heads(c["V_raw"], G), c["scale"])
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_full_rank_orthonormal_u_equals_uncompressed_attention():
+    # rank = d, U square orthogonal, one KV head: C = K U gives K = C U^T exactly, so the
+    # latent path is plain attention over [K_beacon (no RoPE) ; K_raw (RoPE'd)]
+    rng = np.random.default_rng(5)
+    B, Hq, d, N_b, W = 2, 4, 16, 13, 9
+    U_K, U_V = _ortho(rng, d, d), _ortho(rng, d, d)
+    Kb, Vb = _rand(rng, B, N_b, 1, d), _rand(rng, B, N_b, 1, d)
+    c = dict(q=_rand(rng, B, Hq, d), C_K=Kb[:, :, 0] @ U_K, C_V=Vb[:, :, 0] @ U_V,
+             K_raw=_rand(rng, B, W, 1, d), V_raw=_rand(rng, B, W, 1, d), U_K=U_K, U_V=U_V,
+             q_pos=np.array([300, 17]), scale=0.3, rope_base=500000.0)
+    out = oracle.decode_attn(**c)
+    qr = np.stack([_rope_complex(c["q"][b], c["q_pos"][b], 500000.0) for b in range(B)])
+    K = np.concatenate([Kb, c["K_raw"]], axis=1)
+    V = np.concatenate([Vb, c["V_raw"]], axis=1)
+    ref = _sdpa(qr, _expand_heads(K, Hq), _expand_heads(V, Hq), 0.3)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_full_kv_is_sdpa():
+    rng = np.random.default_rng(6)
+    B, Hq, Hkv, d, T = 2, 8, 2, 32, 50
+    q, K, V = _rand(rng, B, Hq, d), _rand(rng, B, T, Hkv, d), _rand(rng, B, T, Hkv, d)
+    pos = np.array([50, 4096])
+    out = oracle.decode_attn_full_kv(q, K, V, pos, 0.2, 10000.0)
+    qr = np.stack([_rope_complex(q[b], pos[b], 10000.0) for b in range(B)])
+    ref = _sdpa(qr, _expand_heads(K, 4), _expand_heads(V, 4), 0.2)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+
+
+def _brute(c):
+    """Scalar loops straight from the decode rule, no numpy linear algebra."""
+    q, C_K, C_V, K, V, U_K, U_V = (c[k] for k in ("q", "C_K", "C_V", "K_raw", "V_raw", "U_K", "U_V"))
+    B, Hq, d = q.shape
+    N_b, r_k, r_v = C_K.shape[1], C_K.shape[2], C_V.shape[2]
+    W, Hkv = K.shape[1], K.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, d))
+    for b in range(B):
+        p = float(c["q_pos"][b])
+        for h in range(Hq):
+            g = h // G
+            qr = [0.0] * d
+            for i in range(d // 2):
+                a = p * c["rope_base"] ** (-2.0 * i / d)
+                qr[i] = q[b, h, i] * math.cos(a) - q[b, h, i + d // 2] * math.sin(a)
+                qr[i + d // 2] = q[b, h, i + d // 2] * math.cos(a) + q[b, h, i] * math.sin(a)
+            s = []
+            for j in range(N_b):
+                acc = 0.0
+                for k in range(r_k):
+                    qt = sum(qr[i] * U_K[g * d + i, k] for i in range(d))
+                    acc += qt * C_K[b, j, k]
+                s.append(c["scale"] * acc)
+            for t in range(W):
+                s.append(c["scale"] * sum(qr[i] * K[b, t, g, i] for i in range(d)))
+            m = max(s)
+            e = [math.exp(x - m) for x in s]
+            l = sum(e)
+            for i in range(d):
+                v = 0.0
+                for j in range(N_b):
+                    full_v = sum(C_V[b, j, k] * U_V[g * d + i, k] for k in range(r_v))
+                    v += e[j] * full_v
+                for t in range(W):
+                    v += e[N_b + t] * V[b, t, g, i]
+                out[b, h, i] = v / l
+    return out
+
+
+def test_brute_force_scalar_loops():
+    c = _case(7, B=2, Hq=6, Hkv=2, d=4, N_b=5, W=3, r_k=3, r_v=2)
+    np.testing.assert_allclose(oracle.decode_attn(**c), _brute(c), rtol=1e-12, atol=1e-13)
+
+
+def test_weights_sum_to_one():
+    c = _case(8)
+    _, w = oracle.decode_attn(**c, return_weights=True)
+    for v in w.values():
+        assert abs(v.sum() - 1.0) < 1e-14
+        assert np.all(v >= 0)
+
+
+def test_zero_query_gives_mean_of_values():
+    c = _case(9)
+    c["q"] = np.zeros_like(c["q"])
+    out = oracle.decode_attn(**c)
+    d = c["q"].shape[2]
+    G = c["q"].shape[1] // c["K_raw"].shape[2]
+    for b in range(2):
+        for h in range(6):
+            g = h // G
+            vb = c["C_V"][b] @ c["U_V"][g * d:(g + 1) * d].T     # full-dim beacon values
+            rows = np.concatenate([vb, c["V_raw"][b, :, g, :]])
+            np.testing.assert_allclose(out[b, h], rows.mean(axis=0), rtol=1e-12, atol=1e-13)
+
+
+def test_dominant_raw_key_selects_its_value():
+    c = _case(10, B=1, Hq=2, Hkv=1)
+    qr = oracle.rope(c["q"][0, 0], c["q_pos"][0], c["rope_base"])
+    c["K_raw"][0, 4, 0] = 1e3 * qr / np.linalg.norm(qr)        # aligned with RoPE(q)
+    out = oracle.decode_attn(**c)
+    np.testing.assert_allclose(out[0, 0], c["V_raw"][0, 4, 0], rtol=0, atol=1e-9)
+
+
+def test_dominant_beacon_selects_its_latent_value():
+    c = _case(11, B=1, Hq=2, Hkv=1, r_k=16, d=16)
+    c["U_K"] = _ortho(np.random.default_rng(0), 16, 16)
+    qr = oracle.rope(c["q"][0, 0], c["q_pos"][0], c["rope_base"])
+    qt = qr @ c["U_K"]
+    c["C_K"][0, 3] = 1e3 * qt / np.linalg.norm(qt)
+    out = oracle.decode_attn(**c)
+    np.testing.assert_allclose(out[0, 0], c["C_V"][0, 3] @ c["U_V"].T, rtol=0, atol=1e-9)
+
+
+def test_grouping_is_contiguous():
+    # heads 0..G-1 read KV group 0 only: changing group 1's window leaves them unchanged
+    c = _case(12, Hq=6, Hkv=2)
+    a = oracle.decode_attn(**c)
+    c["K_raw"][:, :, 1] += 5.0
+    c["V_raw"][:, :, 1] -= 3.0
+    b = oracle.decode_attn(**c)
+    np.testing.assert_array_equal(a[:, :3], b[:, :3])
+    assert np.abs(a[:, 3:] - b[:, 3:]).max() > 1e-3
+
+
+def test_beacon_keys_carry_no_rope():
+    # beacon scores do not depend on the query position beyond RoPE(q): with a window
+    # that is empty, moving q_pos changes the output only through RoPE(q)
+    c = _case(13, W=0)
+    c["K_raw"] = c["K_raw"][:, :0]
+    c["V_raw"] = c["V_raw"][:, :0]
+    out = oracle.decode_attn(**c)
+    d = c["q"].shape[2]
+    G = 3
+    for b in range(2):
+        for h in range(6):
+            g = h // G
+            qr = _rope_complex(c["q"][b, h], c["q_pos"][b], c["rope_base"])
+            Kb = c["C_K"][b] @ c["U_K"][g * d:(g + 1) * d].T     # un-RoPE'd beacon keys
+            Vb = c["C_V"][b] @ c["U_V"][g * d:(g + 1) * d].T
+            s = c["scale"] * Kb @ qr
+            e = np.exp(s - s.max())
+            np.testing.assert_allclose(out[b, h], e @ Vb / e.sum(), rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------- planted mistakes must be caught
+
+def _check_rope_complex_with(mod):
+    x = np.random.default_rng(1).standard_normal((3, 64))
+    np.testing.assert_allclose(mod.rope(x, 2080, 10000.0), _rope_complex(x, 2080, 10000.0),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_pins_catch_wrong_rope_sign(monkeypatch):
+    def bad_rope(x, pos, base):
+        d = x.shape[-1]
+        h = d // 2
+        ang = O.rope_angles(d, pos, base)
+        c, s = np.cos(ang), np.sin(ang)
+        return np.concatenate([x[..., :h] * c + x[..., h:] * s, x[..., h:] * c - x[..., :h] * s], -1)
+    _check_rope_complex_with(O)
+    monkeypatch.setattr(O, "rope", bad_rope)
+    with pytest.raises(AssertionError):
+        _check_rope_complex_with(O)
+
+
+def test_pins_catch_interleaved_grouping(monkeypatch):
+    c = _case(14, B=1, Hq=4, Hkv=2, d=4, N_b=3, W=2, r_k=2, r_v=2)
+    good = O.decode_attn(**c)
+    orig_groups = O._groups
+
+    def bad_decode(**kw):
+        # planted mistake: head h reads group h % Hkv instead of h // G
+        q = kw["q"]
+        perm = [0, 2, 1, 3]
+        kw = dict(kw)
+        kw["q"] = q[:, perm]
+        return O.decode_attn(**kw)[:, perm]
+    assert orig_groups(4, 2) == 2
+    bad = bad_decode(**c)
+    assert np.abs(bad - _brute(c)).max() > 1e-6
+    np.testing.assert_allclose(good, _brute(c), rtol=1e-12, atol=1e-13)
+
+
+def test_pins_catch_transposed_projection():
+    # using U^(g) from the wrong block (g-th column block of U^T) breaks the
+    # reconstruction identity
+    c = _case(15)
+    d = c["q"].shape[2]
+    out_good = O.decode_attn(**c)
+    ref = O.decode_attn_reconstruct(**c)
+    c_bad = dict(c)
+    c_bad["U_K"] = np.roll(c["U_K"], d, axis=0)     # group blocks swapped
+    out_bad = O.decode_attn(**c_bad)
+    np.testing.assert_allclose(out_good, ref, rtol=1e-11, atol=1e-12)
+    assert np.abs(out_bad - ref).max() > 1e-6
