@@ -1,0 +1,163 @@
+/*
+ * slimkv.h - C ABI of libslimkv: SlimKV reconstruction-free decode attention
+ * for one transformer layer and one decode step, on an NVIDIA B300 (sm_103a).
+ *
+ * The method. "Can SlimKV compress KV cache jointly across tokens and features"
+ * (wispaper.ai), section "Latent-space attention removes the rebuild step": the
+ * history of a sequence is folded into beacon states whose keys and values are
+ * cached only as low-rank latent rows C_K, C_V, with no key-side RoPE; recent
+ * raw tokens keep full-dimension keys with RoPE. RoPE is applied to every query.
+ * A query head h of KV group g is scored against the beacons in latent space,
+ * (RoPE(q_h) . U_K^(g)) . C_K^T, and against the raw window as
+ * RoPE(q_h) . K_raw[:, g]^T; one softmax spans both score sets, and the values
+ * are aggregated as (A_beacon . C_V) . U_V^(g)T + A_window . V_raw[:, g]. Beacon
+ * keys are never materialised at full dimension. The SlimKV abstract
+ * (omanscience.com citation record) states the same K-RoPE-free latent decode.
+ *
+ * Conventions used by every call:
+ *  - Query head h belongs to KV group g = h / (Hq / Hkv) (contiguous groups).
+ *  - U_K, U_V are row-major [Hkv*d, r]; U^(g) is the row block g*d .. g*d+d-1,
+ *    the part of the up-projection that yields KV head g.
+ *  - RoPE pairs element i with element i + d/2 ("rotate-half") at angle
+ *    q_pos[b] * rope_base^(-2i/d); the angle is formed in double precision.
+ *  - Raw-window keys (and full-KV keys) are stored after RoPE.
+ *  - The same scale multiplies beacon and window scores (typically 1/sqrt(d)).
+ *  - No masking: the decode query attends to every beacon and window row.
+ *
+ * Memory and ordering:
+ *  - Every pointer is device memory owned by the caller; the library allocates
+ *    and frees nothing. Each call only enqueues kernels on `stream` (a
+ *    cudaStream_t passed as void*; NULL is the legacy default stream) and
+ *    returns; buffers must stay valid until the stream has passed the call.
+ *  - Every tensor pointer must be 16-byte aligned, and the workspace 256-byte
+ *    aligned.
+ *  - Kernels of a call may be launched before the previous call on the same
+ *    stream has finished (programmatic dependent launch); each kernel waits for
+ *    its predecessor before it reads the workspace or writes anything, but may
+ *    read its cache operands (C_K, C_V, K_raw, V_raw, K, V, U_K, U_V) early.
+ *    So the cache operands of a call must not alias the `out` or `workspace`
+ *    of the slimkv call issued just before it on the same stream.
+ *  - One workspace may be reused by consecutive calls on one stream; calls on
+ *    different streams that may overlap need separate workspaces.
+ *
+ * Errors: every argument is checked on the host before any launch; a failed
+ * check returns a status and launches nothing. SLIMKV_ERR_CUDA means a launch
+ * or a driver call failed (the CUDA error is left for cudaGetLastError).
+ */
+#ifndef SLIMKV_H
+#define SLIMKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SLIMKV_ABI_VERSION 1
+
+typedef enum {
+    SLIMKV_OK = 0,
+    SLIMKV_ERR_NULL = 1,      /* a required pointer is NULL                       */
+    SLIMKV_ERR_SHAPE = 2,     /* a size is out of range or inconsistent           */
+    SLIMKV_ERR_DTYPE = 3,     /* unknown storage dtype                            */
+    SLIMKV_ERR_ALIGN = 4,     /* a pointer breaks the alignment rule              */
+    SLIMKV_ERR_WORKSPACE = 5, /* workspace missing or smaller than required       */
+    SLIMKV_ERR_CUDA = 6       /* a CUDA launch or driver call failed              */
+} slimkv_status;
+
+/* Storage type of q, C_K, C_V, K_raw, V_raw, K, V, U_K and U_V. Arithmetic is
+ * float32 (tensor-core products take bf16 operands with float32 accumulation;
+ * the query operand is split into a bf16 high and low part). `out` is float32. */
+typedef enum { SLIMKV_F32 = 0, SLIMKV_BF16 = 1 } slimkv_dtype;
+
+/* Problem sizes of one layer.
+ *  B      batch elements (1..256)            Hq, Hkv  query / KV heads, Hq % Hkv == 0, Hq <= 128
+ *  d      head dimension (64 or 128)          N_b      beacon states per batch element (>= 0)
+ *  r_k    latent key rank, r_v latent value rank: multiples of 32 in [32, 512] when N_b > 0
+ *  W      raw-window tokens per element (>= 0); N_b + W >= 1
+ *  scale  score scale (finite)                rope_base RoPE base (> 0)
+ *  N_b <= 2^24 and W <= 2^24. For slimkv_decode_attn_full_kv, N_b must be 0 and W is the
+ *  cache length T. */
+typedef struct {
+    int B, Hq, Hkv, d, N_b, r_k, r_v, W;
+    float scale;
+    double rope_base;
+    slimkv_dtype dtype;
+} slimkv_shape;
+
+/* which: SLIMKV_LATENT for slimkv_decode_attn, SLIMKV_RECONSTRUCT for
+ * slimkv_decode_attn_reconstruct, SLIMKV_FULL_KV for slimkv_decode_attn_full_kv. */
+enum { SLIMKV_LATENT = 0, SLIMKV_RECONSTRUCT = 1, SLIMKV_FULL_KV = 2 };
+
+/* Bytes of device workspace the call `which` needs for `shape` (0 if the shape
+ * is invalid). The workspace holds the rotated and latent queries, per-split
+ * softmax partials and, for SLIMKV_RECONSTRUCT, the materialised K_b and V_b. */
+size_t slimkv_workspace_bytes(const slimkv_shape* shape, int which);
+
+/* SlimKV decode attention, "Latent-space attention removes the rebuild step":
+ * out[b,h,:] = ( (A_b . C_V[b]) . U_V^(g)T + A_w . V_raw[b,:,g,:] ) / l, where the
+ * scores are scale*(RoPE(q[b,h]) . U_K^(g)) . C_K[b]^T over the beacons and
+ * scale*RoPE(q[b,h]) . K_raw[b,:,g,:]^T over the window, A = exp(s - max s) over
+ * both sets and l = sum(A).
+ *   q      [B, Hq, d]        queries before RoPE, position q_pos[b]
+ *   C_K    [B, N_b, r_k]     latent beacon keys (no RoPE)           (unused if N_b == 0)
+ *   C_V    [B, N_b, r_v]     latent beacon values                   (unused if N_b == 0)
+ *   K_raw  [B, W, Hkv, d]    raw-window keys, RoPE already applied  (unused if W == 0)
+ *   V_raw  [B, W, Hkv, d]    raw-window values                      (unused if W == 0)
+ *   U_K    [Hkv*d, r_k]      key up-projection                      (unused if N_b == 0)
+ *   U_V    [Hkv*d, r_v]      value up-projection                    (unused if N_b == 0)
+ *   q_pos  [B] int32         query positions (device)
+ *   out    [B, Hq, d] f32    result
+ *   workspace, ws_bytes      device scratch, >= slimkv_workspace_bytes(shape, SLIMKV_LATENT)
+ * Beacon keys and values are never expanded to full dimension. */
+slimkv_status slimkv_decode_attn(const slimkv_shape* shape, const void* q, const void* C_K,
+                                 const void* C_V, const void* K_raw, const void* V_raw,
+                                 const void* U_K, const void* U_V, const int32_t* q_pos,
+                                 float* out, void* workspace, size_t ws_bytes, void* stream);
+
+/* The feature-wise baseline the SlimKV pages compare against ("Speedups are
+ * real, but memory is set by the ratio": a reconstruction-based variant that
+ * materialises full-dimensional K/V before attention): K_b = C_K . U_K^T and
+ * V_b = C_V . U_V^T are written to the workspace as [B, N_b, Hkv, d] in the
+ * storage dtype, then standard GQA attention runs over [K_b ; K_raw] with RoPE on
+ * the query only (beacon keys get none, so the result equals slimkv_decode_attn
+ * up to rounding). Same arguments as slimkv_decode_attn; workspace >=
+ * slimkv_workspace_bytes(shape, SLIMKV_RECONSTRUCT). Requires N_b > 0. */
+slimkv_status slimkv_decode_attn_reconstruct(const slimkv_shape* shape, const void* q,
+                                             const void* C_K, const void* C_V,
+                                             const void* K_raw, const void* V_raw,
+                                             const void* U_K, const void* U_V,
+                                             const int32_t* q_pos, float* out,
+                                             void* workspace, size_t ws_bytes, void* stream);
+
+/* Uncompressed GQA decode attention ("Full KV" in the same section):
+ * out[b,h,:] = softmax(scale * RoPE(q[b,h]) . K[b,:,g,:]^T) . V[b,:,g,:].
+ *   K, V [B, T, Hkv, d] with T = shape->W (keys stored after RoPE); shape->N_b == 0.
+ * workspace >= slimkv_workspace_bytes(shape, SLIMKV_FULL_KV). */
+slimkv_status slimkv_decode_attn_full_kv(const slimkv_shape* shape, const void* q,
+                                         const void* K, const void* V,
+                                         const int32_t* q_pos, float* out,
+                                         void* workspace, size_t ws_bytes, void* stream);
+
+/* Human-readable name of a status. Never NULL. */
+const char* slimkv_status_str(slimkv_status status);
+
+/* SLIMKV_ABI_VERSION of the loaded library. */
+int slimkv_abi_version(void);
+
+/* Kernel path a call `which` with `shape` takes on the current device:
+ * 1 = tcgen05/TMA path (bf16 storage, d == 128, sm_100-family device),
+ * 0 = SIMT float32 path (float32 storage, d == 64, or forced), -1 = invalid shape. */
+int slimkv_kernel_path(const slimkv_shape* shape, int which);
+
+/* Process-wide switch: force the SIMT path for every later call (on != 0), or
+ * restore automatic selection (on == 0). Returns the previous setting. Meant for
+ * cross-checking the two paths; not thread-safe against concurrent calls. */
+int slimkv_force_simt(int on);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SLIMKV_H */

@@ -1,0 +1,204 @@
+"""Thin Python binding of libslimkv (ctypes): argument marshalling only.
+
+Every step of the decode path runs in the library's CUDA kernels; torch is used
+for device memory and streams. The names follow ``include/slimkv.h``.
+There is no CPU fallback: without the built library on a CUDA device every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libslimkv.so")
+
+SLIMKV_F32, SLIMKV_BF16 = 0, 1
+SLIMKV_LATENT, SLIMKV_RECONSTRUCT, SLIMKV_FULL_KV = 0, 1, 2
+STATUS = {0: "SLIMKV_OK", 1: "SLIMKV_ERR_NULL", 2: "SLIMKV_ERR_SHAPE", 3: "SLIMKV_ERR_DTYPE",
+          4: "SLIMKV_ERR_ALIGN", 5: "SLIMKV_ERR_WORKSPACE", 6: "SLIMKV_ERR_CUDA"}
+
+# every symbol include/slimkv.h declares
+EXPORTS = ("slimkv_workspace_bytes", "slimkv_decode_attn", "slimkv_decode_attn_reconstruct",
+           "slimkv_decode_attn_full_kv", "slimkv_status_str", "slimkv_abi_version",
+           "slimkv_kernel_path", "slimkv_force_simt")
+
+
+class SlimkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+                ("d", ctypes.c_int), ("N_b", ctypes.c_int), ("r_k", ctypes.c_int),
+                ("r_v", ctypes.c_int), ("W", ctypes.c_int), ("scale", ctypes.c_float),
+                ("rope_base", ctypes.c_double), ("dtype", ctypes.c_int)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libslimkv.so (built in-tree by ``latent_kv_cache_decode_b300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libslimkv.so not built ({path}); run "
+                           "`python -m latent_kv_cache_decode_b300.build`")
+    lib = ctypes.CDLL(path)
+    vp, sz, i32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
+    sp = ctypes.POINTER(Shape)
+    lib.slimkv_workspace_bytes.argtypes = [sp, ctypes.c_int]
+    lib.slimkv_workspace_bytes.restype = sz
+    lib.slimkv_decode_attn.argtypes = [sp] + [vp] * 7 + [i32p, vp, vp, sz, vp]
+    lib.slimkv_decode_attn.restype = ctypes.c_int
+    lib.slimkv_decode_attn_reconstruct.argtypes = [sp] + [vp] * 7 + [i32p, vp, vp, sz, vp]
+    lib.slimkv_decode_attn_reconstruct.restype = ctypes.c_int
+    lib.slimkv_decode_attn_full_kv.argtypes = [sp, vp, vp, vp, i32p, vp, vp, sz, vp]
+    lib.slimkv_decode_attn_full_kv.restype = ctypes.c_int
+    lib.slimkv_status_str.argtypes = [ctypes.c_int]
+    lib.slimkv_status_str.restype = ctypes.c_char_p
+    lib.slimkv_abi_version.argtypes = []
+    lib.slimkv_abi_version.restype = ctypes.c_int
+    lib.slimkv_kernel_path.argtypes = [sp, ctypes.c_int]
+    lib.slimkv_kernel_path.restype = ctypes.c_int
+    lib.slimkv_force_simt.argtypes = [ctypes.c_int]
+    lib.slimkv_force_simt.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return SLIMKV_F32
+    if t == torch.bfloat16:
+        return SLIMKV_BF16
+    raise TypeError(f"unsupported storage dtype {t}")
+
+
+def make_shape(B, Hq, Hkv, d, N_b, r_k, r_v, W, dtype, scale=None, rope_base=10000.0) -> Shape:
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    return Shape(B, Hq, Hkv, d, N_b, r_k, r_v, W, scale, rope_base, code)
+
+
+def workspace_bytes(shape: Shape, which: int) -> int:
+    return int(load().slimkv_workspace_bytes(ctypes.byref(shape), which))
+
+
+def kernel_path(shape: Shape, which: int) -> int:
+    return int(load().slimkv_kernel_path(ctypes.byref(shape), which))
+
+
+def force_simt(on: bool) -> bool:
+    return bool(load().slimkv_force_simt(1 if on else 0))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on the CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise SlimkvError(status, what)
+
+
+class Workspace:
+    """A reusable device workspace (grows on demand)."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf: Optional[torch.Tensor] = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device or "cuda")
+        return self.buf
+
+
+def decode_attn(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, *, scale=None, rope_base=10000.0,
+                out=None, workspace: Optional[Workspace] = None, stream=None, shape=None):
+    """slimkv_decode_attn on torch CUDA tensors; returns out [B,Hq,d] float32."""
+    lib = load()
+    B, Hq, d = q.shape
+    N_b = C_K.shape[1] if C_K is not None else 0
+    W = K_raw.shape[1] if K_raw is not None else 0
+    Hkv = U_K.shape[0] // d if U_K is not None else K_raw.shape[2]
+    r_k = C_K.shape[2] if C_K is not None else 0
+    r_v = C_V.shape[2] if C_V is not None else 0
+    sh = shape or make_shape(B, Hq, Hkv, d, N_b, r_k, r_v, W, q.dtype, scale, rope_base)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    nb = lib.slimkv_workspace_bytes(ctypes.byref(sh), SLIMKV_LATENT)
+    if nb == 0:
+        _check(2, "slimkv_decode_attn")
+    ws = (workspace or Workspace(q.device)).get(nb)
+    st = lib.slimkv_decode_attn(ctypes.byref(sh), _ptr(q), _ptr(C_K), _ptr(C_V), _ptr(K_raw),
+                                _ptr(V_raw), _ptr(U_K), _ptr(U_V), _ptr(q_pos), _ptr(out),
+                                _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "slimkv_decode_attn")
+    return out
+
+
+def decode_attn_reconstruct(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, *, scale=None,
+                            rope_base=10000.0, out=None, workspace: Optional[Workspace] = None,
+                            stream=None):
+    """slimkv_decode_attn_reconstruct on torch CUDA tensors."""
+    lib = load()
+    B, Hq, d = q.shape
+    W = K_raw.shape[1] if K_raw is not None else 0
+    sh = make_shape(B, Hq, U_K.shape[0] // d, d, C_K.shape[1], C_K.shape[2], C_V.shape[2], W,
+                    q.dtype, scale, rope_base)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    nb = lib.slimkv_workspace_bytes(ctypes.byref(sh), SLIMKV_RECONSTRUCT)
+    if nb == 0:
+        _check(2, "slimkv_decode_attn_reconstruct")
+    ws = (workspace or Workspace(q.device)).get(nb)
+    st = lib.slimkv_decode_attn_reconstruct(ctypes.byref(sh), _ptr(q), _ptr(C_K), _ptr(C_V),
+                                            _ptr(K_raw), _ptr(V_raw), _ptr(U_K), _ptr(U_V),
+                                            _ptr(q_pos), _ptr(out), _ptr(ws), ws.numel(),
+                                            _stream(stream))
+    _check(st, "slimkv_decode_attn_reconstruct")
+    return out
+
+
+def decode_attn_full_kv(q, K, V, q_pos, *, scale=None, rope_base=10000.0, out=None,
+                        workspace: Optional[Workspace] = None, stream=None):
+    """slimkv_decode_attn_full_kv on torch CUDA tensors."""
+    lib = load()
+    B, Hq, d = q.shape
+    sh = make_shape(B, Hq, K.shape[2], d, 0, 0, 0, K.shape[1], q.dtype, scale, rope_base)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    nb = lib.slimkv_workspace_bytes(ctypes.byref(sh), SLIMKV_FULL_KV)
+    if nb == 0:
+        _check(2, "slimkv_decode_attn_full_kv")
+    ws = (workspace or Workspace(q.device)).get(nb)
+    st = lib.slimkv_decode_attn_full_kv(ctypes.byref(sh), _ptr(q), _ptr(K), _ptr(V), _ptr(q_pos),
+                                        _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "slimkv_decode_attn_full_kv")
+    return out
+
+
+def status_str(status: int) -> str:
+    return load().slimkv_status_str(status).decode()

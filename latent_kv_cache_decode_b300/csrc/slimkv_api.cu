@@ -1,0 +1,315 @@
+// C-ABI layer of libslimkv: argument checks, workspace partition, the host-side
+// work planner, and kernel dispatch (tensor-core path or SIMT path).
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "slimkv_internal.cuh"
+#include "tc_decode.cuh"
+
+using namespace slimkv;
+
+namespace {
+
+int g_force_simt = 0;
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+size_t elem_size(slimkv_dtype t) { return t == SLIMKV_F32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+slimkv_status check_shape(const slimkv_shape* s, int which) {
+    if (s == nullptr) return SLIMKV_ERR_NULL;
+    if (s->dtype != SLIMKV_F32 && s->dtype != SLIMKV_BF16) return SLIMKV_ERR_DTYPE;
+    if (which < SLIMKV_LATENT || which > SLIMKV_FULL_KV) return SLIMKV_ERR_SHAPE;
+    if (s->B < 1 || s->B > kMaxB) return SLIMKV_ERR_SHAPE;
+    if (s->Hq < 1 || s->Hq > kMaxHq || s->Hkv < 1 || s->Hq % s->Hkv != 0) return SLIMKV_ERR_SHAPE;
+    if (s->d != 64 && s->d != 128) return SLIMKV_ERR_SHAPE;
+    if (s->N_b < 0 || s->W < 0 || s->N_b > (1 << 24) || s->W > (1 << 24)) return SLIMKV_ERR_SHAPE;
+    if ((int64_t)s->W * s->Hkv > (int64_t(1) << 28)) return SLIMKV_ERR_SHAPE;
+    if ((int64_t)s->N_b * s->Hkv > (int64_t(1) << 28)) return SLIMKV_ERR_SHAPE;
+    if (s->N_b + s->W < 1) return SLIMKV_ERR_SHAPE;
+    if (s->N_b > 0) {
+        if (s->r_k < 32 || s->r_k > kMaxRank || s->r_k % 32) return SLIMKV_ERR_SHAPE;
+        if (s->r_v < 32 || s->r_v > kMaxRank || s->r_v % 32) return SLIMKV_ERR_SHAPE;
+    }
+    if (!isfinite(s->scale)) return SLIMKV_ERR_SHAPE;
+    if (!(s->rope_base > 0.0) || !isfinite(s->rope_base)) return SLIMKV_ERR_SHAPE;
+    if (which == SLIMKV_FULL_KV && (s->N_b != 0 || s->W < 1)) return SLIMKV_ERR_SHAPE;
+    if (which == SLIMKV_RECONSTRUCT && s->N_b < 1) return SLIMKV_ERR_SHAPE;
+    return SLIMKV_OK;
+}
+
+// Number of segments (runs of rows of one kind for one batch element).
+int n_segments(const slimkv_shape* s, int which) {
+    int per_b = 0;
+    if (which == SLIMKV_LATENT) per_b = (s->N_b > 0) + (s->W > 0);
+    if (which == SLIMKV_RECONSTRUCT) per_b = 1 + (s->W > 0);
+    if (which == SLIMKV_FULL_KV) per_b = 1;
+    return per_b * s->B;
+}
+
+WsLayout layout(const slimkv_shape* s, int which) {
+    WsLayout L;
+    const bool lat = which == SLIMKV_LATENT && s->N_b > 0;
+    L.Dmax = std::max(lat ? s->r_v : 0, s->d);
+    L.slots = kSlotCap + n_segments(s, which);
+    size_t off = 0;
+    L.q_rot = off;
+    off = align_up(off + sizeof(float) * s->B * s->Hq * s->d);
+    L.q_lat = off;
+    if (lat) off = align_up(off + sizeof(float) * s->B * s->Hq * s->r_k);
+    L.acc = off;
+    off = align_up(off + sizeof(float) * (size_t)L.slots * s->Hq * L.Dmax);
+    L.ml = off;
+    off = align_up(off + sizeof(float) * (size_t)L.slots * 2 * s->Hq);
+    L.kind = off;
+    off = align_up(off + sizeof(int) * (size_t)L.slots);
+    if (which == SLIMKV_RECONSTRUCT) {
+        const size_t kv = (size_t)s->B * s->N_b * s->Hkv * s->d * elem_size(s->dtype);
+        L.kb = off;
+        off = align_up(off + kv);
+        L.vb = off;
+        off = align_up(off + kv);
+    }
+    L.total = off;
+    return L;
+}
+
+int device_cc_major() {
+    int dev = 0, major = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return 0;
+    return major;
+}
+
+int select_path(const slimkv_shape* s, int which) {
+    if (check_shape(s, which) != SLIMKV_OK) return -1;
+    if (g_force_simt) return 0;
+    if (s->dtype != SLIMKV_BF16 || s->d != 128) return 0;
+    if (!tc_supported(s->Hq, s->Hkv, s->d, which == SLIMKV_LATENT ? s->N_b : 0, s->r_k, s->r_v))
+        return 0;
+    return device_cc_major() == 10 ? 1 : 0;
+}
+
+struct Ptrs {
+    const void* q;
+    const void* C_K;
+    const void* C_V;
+    const void* K_raw;
+    const void* V_raw;
+    const void* U_K;
+    const void* U_V;
+    const int32_t* q_pos;
+    float* out;
+    void* ws;
+    size_t ws_bytes;
+};
+
+slimkv_status check_ptrs(const slimkv_shape* s, int which, const Ptrs& p) {
+    const bool beacons = s->N_b > 0 && which != SLIMKV_FULL_KV;
+    if (!p.q || !p.q_pos || !p.out || !p.ws) return SLIMKV_ERR_NULL;
+    if (beacons && (!p.C_K || !p.C_V || !p.U_K || !p.U_V)) return SLIMKV_ERR_NULL;
+    if (s->W > 0 && (!p.K_raw || !p.V_raw)) return SLIMKV_ERR_NULL;
+    if (!aligned16(p.q) || !aligned16(p.out)) return SLIMKV_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(p.q_pos) & 3u) != 0) return SLIMKV_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(p.ws) & (kAlign - 1)) != 0) return SLIMKV_ERR_ALIGN;
+    if (beacons && (!aligned16(p.C_K) || !aligned16(p.C_V) || !aligned16(p.U_K) || !aligned16(p.U_V)))
+        return SLIMKV_ERR_ALIGN;
+    if (s->W > 0 && (!aligned16(p.K_raw) || !aligned16(p.V_raw))) return SLIMKV_ERR_ALIGN;
+    if (p.ws_bytes < layout(s, which).total) return SLIMKV_ERR_WORKSPACE;
+    return SLIMKV_OK;
+}
+
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// SIMT path: qproj -> split decode (one CTA per item and head) -> combine.
+template <typename T>
+slimkv_status run_simt(const slimkv_shape* s, int which, const Ptrs& p, cudaStream_t st) {
+    const WsLayout L = layout(s, which);
+    char* ws = static_cast<char*>(p.ws);
+    float* q_rot = reinterpret_cast<float*>(ws + L.q_rot);
+    float* q_lat = reinterpret_cast<float*>(ws + L.q_lat);
+    const bool lat = which == SLIMKV_LATENT && s->N_b > 0;
+    cudaError_t e = launch_qproj<T>((const T*)p.q, lat ? (const T*)p.U_K : nullptr, p.q_pos, q_rot,
+                                    lat ? q_lat : nullptr, s->B, s->Hq, s->Hkv, s->d, s->r_k,
+                                    s->rope_base, st, false);
+    if (e != cudaSuccess) return SLIMKV_ERR_CUDA;
+
+    SimtDecodeArgs a = {};
+    a.B = s->B;
+    a.Hq = s->Hq;
+    a.Hkv = s->Hkv;
+    a.d = s->d;
+    a.N_b = lat ? s->N_b : 0;
+    a.r_k = s->r_k;
+    a.r_v = s->r_v;
+    a.scale_log2 = s->scale * kLog2e;
+    a.C_K = p.C_K;
+    a.C_V = p.C_V;
+    a.q_rot = q_rot;
+    a.q_lat = q_lat;
+    a.acc = reinterpret_cast<float*>(ws + L.acc);
+    a.ml = reinterpret_cast<float*>(ws + L.ml);
+    a.kind = reinterpret_cast<int*>(ws + L.kind);
+    a.Dmax = L.Dmax;
+    if (which == SLIMKV_RECONSTRUCT) {
+        T* kb = reinterpret_cast<T*>(ws + L.kb);
+        T* vb = reinterpret_cast<T*>(ws + L.vb);
+        const int rows = s->B * s->N_b, n = s->Hkv * s->d;
+        if (launch_simt_reconstruct<T>((const T*)p.C_K, (const T*)p.U_K, kb, rows, n, s->r_k, st) !=
+            cudaSuccess)
+            return SLIMKV_ERR_CUDA;
+        if (launch_simt_reconstruct<T>((const T*)p.C_V, (const T*)p.U_V, vb, rows, n, s->r_v, st) !=
+            cudaSuccess)
+            return SLIMKV_ERR_CUDA;
+        a.K0 = kb;
+        a.V0 = vb;
+        a.W0 = s->N_b;
+        a.K1 = p.K_raw;
+        a.V1 = p.V_raw;
+        a.W1 = s->W;
+    } else {
+        a.K0 = p.K_raw;
+        a.V0 = p.V_raw;
+        a.W0 = s->W;
+        a.W1 = 0;
+    }
+    // rows per item: grow until the item count fits the slot capacity
+    int rpi = 256;
+    for (;;) {
+        const int per_b = (a.N_b ? cdiv(a.N_b, rpi) : 0) + (a.W0 ? cdiv(a.W0, rpi) : 0) +
+                          (a.W1 ? cdiv(a.W1, rpi) : 0);
+        if ((int64_t)per_b * s->B <= L.slots) break;
+        rpi *= 2;
+    }
+    a.rpi_L = a.rpi_R = rpi;
+    a.nit_L = a.N_b ? cdiv(a.N_b, rpi) : 0;
+    a.nit_R0 = a.W0 ? cdiv(a.W0, rpi) : 0;
+    a.nit_R1 = a.W1 ? cdiv(a.W1, rpi) : 0;
+    if (launch_simt_decode<T>(a, st) != cudaSuccess) return SLIMKV_ERR_CUDA;
+
+    CombineArgs c;
+    c.B = s->B;
+    c.Hq = s->Hq;
+    c.Hkv = s->Hkv;
+    c.d = s->d;
+    c.r_v = s->r_v;
+    c.Dmax = L.Dmax;
+    c.U_V = lat ? p.U_V : nullptr;
+    c.acc = a.acc;
+    c.ml = a.ml;
+    c.kind = a.kind;
+    c.out = p.out;
+    const int per_b = a.nit_L + a.nit_R0 + a.nit_R1;
+    for (int b = 0; b <= s->B; ++b) c.slot_begin[b] = b * per_b;
+    if (launch_combine<T>(c, st, false) != cudaSuccess) return SLIMKV_ERR_CUDA;
+    return SLIMKV_OK;
+}
+
+slimkv_status run(const slimkv_shape* s, int which, const Ptrs& p, void* stream) {
+    slimkv_status st = check_shape(s, which);
+    if (st != SLIMKV_OK) return st;
+    st = check_ptrs(s, which, p);
+    if (st != SLIMKV_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (select_path(s, which) == 1) {
+        TcCall c;
+        c.which = which;
+        c.B = s->B;
+        c.Hq = s->Hq;
+        c.Hkv = s->Hkv;
+        c.d = s->d;
+        c.N_b = s->N_b;
+        c.r_k = s->r_k;
+        c.r_v = s->r_v;
+        c.W = s->W;
+        c.scale_log2 = s->scale * kLog2e;
+        c.rope_base = s->rope_base;
+        c.q = p.q;
+        c.C_K = p.C_K;
+        c.C_V = p.C_V;
+        c.K_raw = p.K_raw;
+        c.V_raw = p.V_raw;
+        c.U_K = p.U_K;
+        c.U_V = p.U_V;
+        c.q_pos = p.q_pos;
+        c.out = p.out;
+        const WsLayout L = layout(s, which);
+        char* ws = static_cast<char*>(p.ws);
+        c.q_rot = reinterpret_cast<float*>(ws + L.q_rot);
+        c.q_lat = reinterpret_cast<float*>(ws + L.q_lat);
+        c.acc = reinterpret_cast<float*>(ws + L.acc);
+        c.ml = reinterpret_cast<float*>(ws + L.ml);
+        c.kind = reinterpret_cast<int*>(ws + L.kind);
+        c.kb = ws + L.kb;
+        c.vb = ws + L.vb;
+        c.slots = L.slots;
+        c.Dmax = L.Dmax;
+        return tc_run(c, cs) == cudaSuccess ? SLIMKV_OK : SLIMKV_ERR_CUDA;
+    }
+    if (s->dtype == SLIMKV_F32) return run_simt<float>(s, which, p, cs);
+    return run_simt<__nv_bfloat16>(s, which, p, cs);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t slimkv_workspace_bytes(const slimkv_shape* shape, int which) {
+    if (check_shape(shape, which) != SLIMKV_OK) return 0;
+    return layout(shape, which).total;
+}
+
+slimkv_status slimkv_decode_attn(const slimkv_shape* shape, const void* q, const void* C_K,
+                                 const void* C_V, const void* K_raw, const void* V_raw,
+                                 const void* U_K, const void* U_V, const int32_t* q_pos,
+                                 float* out, void* workspace, size_t ws_bytes, void* stream) {
+    Ptrs p{q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, out, workspace, ws_bytes};
+    return run(shape, SLIMKV_LATENT, p, stream);
+}
+
+slimkv_status slimkv_decode_attn_reconstruct(const slimkv_shape* shape, const void* q,
+                                             const void* C_K, const void* C_V,
+                                             const void* K_raw, const void* V_raw,
+                                             const void* U_K, const void* U_V,
+                                             const int32_t* q_pos, float* out,
+                                             void* workspace, size_t ws_bytes, void* stream) {
+    Ptrs p{q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, out, workspace, ws_bytes};
+    return run(shape, SLIMKV_RECONSTRUCT, p, stream);
+}
+
+slimkv_status slimkv_decode_attn_full_kv(const slimkv_shape* shape, const void* q, const void* K,
+                                         const void* V, const int32_t* q_pos, float* out,
+                                         void* workspace, size_t ws_bytes, void* stream) {
+    Ptrs p{q, nullptr, nullptr, K, V, nullptr, nullptr, q_pos, out, workspace, ws_bytes};
+    return run(shape, SLIMKV_FULL_KV, p, stream);
+}
+
+const char* slimkv_status_str(slimkv_status status) {
+    switch (status) {
+        case SLIMKV_OK: return "ok";
+        case SLIMKV_ERR_NULL: return "required pointer is NULL";
+        case SLIMKV_ERR_SHAPE: return "invalid or unsupported shape";
+        case SLIMKV_ERR_DTYPE: return "unknown dtype";
+        case SLIMKV_ERR_ALIGN: return "pointer breaks the alignment rule";
+        case SLIMKV_ERR_WORKSPACE: return "workspace too small";
+        case SLIMKV_ERR_CUDA: return "CUDA launch or driver call failed";
+    }
+    return "unknown status";
+}
+
+int slimkv_abi_version(void) { return SLIMKV_ABI_VERSION; }
+
+int slimkv_kernel_path(const slimkv_shape* shape, int which) { return select_path(shape, which); }
+
+int slimkv_force_simt(int on) {
+    const int prev = g_force_simt;
+    g_force_simt = on ? 1 : 0;
+    return prev;
+}
+
+}  // extern "C"

@@ -1,0 +1,98 @@
+// Internal declarations shared by the kernels and the C-ABI layer of libslimkv.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/slimkv.h"
+
+namespace slimkv {
+
+constexpr int kMaxB = 256;      // batch elements per call
+constexpr int kMaxHq = 128;     // query heads
+constexpr int kMaxCtas = 296;   // CTAs of one tensor-core decode launch (2 per SM on 148 SMs)
+constexpr int kSlotCap = 512;   // partial slots beyond one per segment
+constexpr int kMaxRank = 512;
+
+// Scores are kept in the log2 domain: s2 = scale * log2(e) * (q . k).
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Programmatic dependent launch: wait for the preceding grid (and everything it
+// waited on) to finish and flush, and allow the next grid to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// Workspace partition (byte offsets from the workspace base, 256-byte aligned).
+struct WsLayout {
+    size_t q_rot = 0;    // float [B, Hq, d]          rotated queries
+    size_t q_lat = 0;    // float [B, Hq, r_k]        latent queries q . U_K^(g)
+    size_t acc = 0;      // float [slots, Hq, Dmax]   per-split value accumulators
+    size_t ml = 0;       // float [slots, 2, Hq]      per-split running max (log2) and sum
+    size_t kind = 0;     // int   [slots]             0 latent accumulator, 1 raw accumulator
+    size_t kb = 0;       // T     [B, N_b, Hkv, d]    materialised beacon keys (reconstruct)
+    size_t vb = 0;       // T     [B, N_b, Hkv, d]    materialised beacon values (reconstruct)
+    size_t total = 0;
+    int slots = 0;       // capacity in slots
+    int Dmax = 0;        // accumulator width
+};
+
+// One "segment" is a run of key rows of one kind for one batch element. Rows of
+// a latent segment are beacons; rows of a raw segment are (token, KV head) pairs
+// flattened as token * Hkv + g, so one row is one d-vector of the cache.
+enum SegKind { kSegLatent = 0, kSegRaw0 = 1, kSegRaw1 = 2 };
+
+// Arguments of the SIMT split-decode kernel.
+struct SimtDecodeArgs {
+    int B, Hq, Hkv, d, N_b, r_k, r_v;
+    int W0, W1;                 // tokens of raw sources 0 and 1 (0 = absent)
+    float scale_log2;
+    const void* C_K;
+    const void* C_V;
+    const void* K0;
+    const void* V0;
+    const void* K1;
+    const void* V1;
+    const float* q_rot;
+    const float* q_lat;
+    float* acc;
+    float* ml;
+    int* kind;
+    int Dmax;
+    int rpi_L, rpi_R;            // rows (beacons / tokens) per item
+    int nit_L, nit_R0, nit_R1;   // items per batch element
+};
+
+// Arguments of the split-combine kernel (merges partials, applies U_V^(g)T).
+struct CombineArgs {
+    int B, Hq, Hkv, d, r_v, Dmax;
+    const void* U_V;             // NULL when no latent partials exist
+    const float* acc;
+    const float* ml;
+    const int* kind;
+    float* out;
+    int slot_begin[kMaxB + 1];   // partial slots of batch element b: [slot_begin[b], slot_begin[b+1])
+};
+
+// ---- kernels (simt_kernels.cu) ----
+template <typename T>
+cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* q_rot,
+                         float* q_lat, int B, int Hq, int Hkv, int d, int r_k, double base,
+                         cudaStream_t st, bool pdl);
+template <typename T>
+cudaError_t launch_simt_decode(const SimtDecodeArgs& a, cudaStream_t st);
+template <typename T>
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl);
+template <typename T>
+cudaError_t launch_simt_reconstruct(const T* C, const T* U, T* out, int rows, int n, int r,
+                                    cudaStream_t st);
+
+}  // namespace slimkv

@@ -1,0 +1,124 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, sizes workspaces, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from latent_kv_cache_decode_b300 import binding as bd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(slimkv_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from latent_kv_cache_decode_b300 import build
+    build.build()
+    return bd.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _header_functions()
+    assert set(bd.EXPORTS) == set(declared), declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.slimkv_abi_version() == 1
+    for code, name in bd.STATUS.items():
+        s = lib.slimkv_status_str(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert lib.slimkv_status_str(99) == b"unknown status"
+
+
+def _shape(**kw):
+    base = dict(B=8, Hq=32, Hkv=8, d=128, N_b=8192, r_k=256, r_v=256, W=2048, dtype=bd.SLIMKV_BF16,
+                scale=0.08838834764831845, rope_base=500000.0)
+    base.update(kw)
+    return bd.make_shape(**base)
+
+
+def test_workspace_sizes(lib):
+    s = _shape()
+    lat = bd.workspace_bytes(s, bd.SLIMKV_LATENT)
+    rec = bd.workspace_bytes(s, bd.SLIMKV_RECONSTRUCT)
+    assert lat > 0 and lat % 256 == 0
+    # reconstruct also holds K_b and V_b: 2 * B * N_b * Hkv * d bf16
+    assert rec >= 2 * 8 * 8192 * 8 * 128 * 2
+    full = bd.workspace_bytes(_shape(N_b=0, W=131072), bd.SLIMKV_FULL_KV)
+    assert full > 0
+    assert bd.workspace_bytes(_shape(N_b=5), bd.SLIMKV_FULL_KV) == 0       # full-KV needs N_b == 0
+
+
+@pytest.mark.parametrize("bad", [dict(Hq=30), dict(d=96), dict(r_k=48), dict(r_v=544), dict(B=0),
+                                 dict(B=257), dict(N_b=0, W=0), dict(N_b=-1), dict(Hq=256, Hkv=8),
+                                 dict(scale=float("inf")), dict(rope_base=0.0), dict(r_k=0)])
+def test_invalid_shapes_rejected(lib, bad):
+    s = _shape(**bad)
+    assert bd.workspace_bytes(s, bd.SLIMKV_LATENT) == 0
+    assert bd.kernel_path(s, bd.SLIMKV_LATENT) == -1
+    st = lib.slimkv_decode_attn(ctypes.byref(s), *([256] * 7), 256, 256, 256, 1 << 40, None)
+    assert st == 2
+
+
+def test_bad_dtype(lib):
+    s = _shape(dtype=7)
+    st = lib.slimkv_decode_attn(ctypes.byref(s), *([256] * 7), 256, 256, 256, 1 << 40, None)
+    assert st == 3
+
+
+def _call(lib, s, ptrs, ws_bytes, fn="slimkv_decode_attn"):
+    return getattr(lib, fn)(ctypes.byref(s), *ptrs, ws_bytes, None)
+
+
+def test_null_misaligned_and_small_workspace_rejected(lib):
+    s = _shape()
+    good = [256 * (i + 1) for i in range(7)] + [4096, 8192, 1 << 20]   # 7 tensors, q_pos, out, ws
+    need = bd.workspace_bytes(s, bd.SLIMKV_LATENT)
+    for i in range(10):                                   # each required pointer NULL in turn
+        p = list(good)
+        p[i] = None
+        assert _call(lib, s, p, need) == 1
+    for i in range(7):                                    # each tensor 8-byte aligned only
+        p = list(good)
+        p[i] += 8
+        assert _call(lib, s, p, need) == 4
+    p = list(good)
+    p[9] += 16                                            # workspace not 256-byte aligned
+    assert _call(lib, s, p, need) == 4
+    assert _call(lib, s, good, need - 1) == 5             # workspace one byte short
+    # full-KV: 7 pointer arguments (q, K, V, q_pos, out, ws)
+    sf = _shape(N_b=0, W=4096)
+    needf = bd.workspace_bytes(sf, bd.SLIMKV_FULL_KV)
+    st = lib.slimkv_decode_attn_full_kv(ctypes.byref(sf), 256, 512, None, 4096, 8192, 1 << 20,
+                                        needf, None)
+    assert st == 1
+    st = lib.slimkv_decode_attn_full_kv(ctypes.byref(sf), 256, 512, 768, 4096, 8192, 1 << 20,
+                                        needf - 256, None)
+    assert st == 5
+    # reconstruct requires beacons
+    sr = _shape(N_b=0)
+    assert _call(lib, sr, good, 1 << 40, "slimkv_decode_attn_reconstruct") == 2
+
+
+def test_unused_operands_may_be_null(lib):
+    # W == 0: K_raw/V_raw may be NULL; N_b == 0: C_K, C_V, U_K, U_V may be NULL.
+    # A too-small workspace is then the first error reported (nothing launches).
+    s = _shape(W=0)
+    p = [256, 512, 768, None, None, 1024, 1280, 4096, 8192, 1 << 20]
+    assert _call(lib, s, p, 256) == 5
+    s = _shape(N_b=0)
+    p = [256, None, None, 768, 1024, None, None, 4096, 8192, 1 << 20]
+    assert _call(lib, s, p, 256) == 5
