@@ -156,6 +156,14 @@ int slimkv_kernel_path(const slimkv_shape* shape, int which);
  * cross-checking the two paths; not thread-safe against concurrent calls. */
 int slimkv_force_simt(int on);
 
+/* Measurement hook: the next call made by this host thread records `start_event`
+ * on its stream right before launching its split-decode kernel and `stop_event`
+ * right after it (both cudaEvent_t passed as void*, created by the caller), so
+ * cudaEventElapsedTime gives that kernel's duration. One-shot; NULL events
+ * cancel a pending request. The events also stop the decode kernel from
+ * overlapping the kernel before it, so the time measured is the kernel alone. */
+void slimkv_time_next_decode(void* start_event, void* stop_event);
+
 #ifdef __cplusplus
 }
 #endif

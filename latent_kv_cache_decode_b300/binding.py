@@ -25,7 +25,7 @@ STATUS = {0: "SLIMKV_OK", 1: "SLIMKV_ERR_NULL", 2: "SLIMKV_ERR_SHAPE", 3: "SLIMK
 # every symbol include/slimkv.h declares
 EXPORTS = ("slimkv_workspace_bytes", "slimkv_decode_attn", "slimkv_decode_attn_reconstruct",
            "slimkv_decode_attn_full_kv", "slimkv_status_str", "slimkv_abi_version",
-           "slimkv_kernel_path", "slimkv_force_simt")
+           "slimkv_kernel_path", "slimkv_force_simt", "slimkv_time_next_decode")
 
 
 class SlimkvError(RuntimeError):
@@ -71,6 +71,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.slimkv_kernel_path.restype = ctypes.c_int
     lib.slimkv_force_simt.argtypes = [ctypes.c_int]
     lib.slimkv_force_simt.restype = ctypes.c_int
+    lib.slimkv_time_next_decode.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.slimkv_time_next_decode.restype = None
     _lib = lib
     return lib
 

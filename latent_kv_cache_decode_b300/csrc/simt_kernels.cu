@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
             for (int s = s0 + lane; s < s1; s += 32) {
                 const float ms = a.ml[((size_t)s * 2) * a.Hq + h];
                 const float ls = a.ml[((size_t)s * 2 + 1) * a.Hq + h];
-                L += (ls > 0.f) ? exp2f(ms - M) * ls : 0.f;
+                L += (ls != 0.f) ? exp2f(ms - M) * ls : 0.f;   // a NaN partial poisons L
             }
             L = warp_sum(L);
             if (lane == 0) {
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
                     for (int s = s0; s < s1; ++s) {
                         if (a.kind[s] != 0) continue;
                         const float ls = a.ml[((size_t)s * 2 + 1) * a.Hq + h];
-                        if (!(ls > 0.f)) continue;
+                        if (ls == 0.f) continue;
                         const float w = exp2f(a.ml[((size_t)s * 2) * a.Hq + h] - M);
                         z = fmaf(w, a.acc[((size_t)s * a.Hq + h) * a.Dmax + j], z);
                     }
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
                 for (int s = s0; s < s1; ++s) {
                     if (a.kind[s] != 1) continue;
                     const float ls = a.ml[((size_t)s * 2 + 1) * a.Hq + h];
-                    if (!(ls > 0.f)) continue;
+                    if (ls == 0.f) continue;
                     const float w = exp2f(a.ml[((size_t)s * 2) * a.Hq + h] - M);
                     y = fmaf(w, a.acc[((size_t)s * a.Hq + h) * a.Dmax + i], y);
                 }

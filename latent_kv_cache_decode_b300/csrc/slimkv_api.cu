@@ -10,6 +10,13 @@
 
 using namespace slimkv;
 
+namespace slimkv {
+DecodeTimer& decode_timer() {
+    static thread_local DecodeTimer t;
+    return t;
+}
+}  // namespace slimkv
+
 namespace {
 
 int g_force_simt = 0;
@@ -190,7 +197,10 @@ slimkv_status run_simt(const slimkv_shape* s, int which, const Ptrs& p, cudaStre
     a.nit_L = a.N_b ? cdiv(a.N_b, rpi) : 0;
     a.nit_R0 = a.W0 ? cdiv(a.W0, rpi) : 0;
     a.nit_R1 = a.W1 ? cdiv(a.W1, rpi) : 0;
-    if (launch_simt_decode<T>(a, st) != cudaSuccess) return SLIMKV_ERR_CUDA;
+    timer_before(st);
+    const cudaError_t de = launch_simt_decode<T>(a, st);
+    timer_after(st);
+    if (de != cudaSuccess) return SLIMKV_ERR_CUDA;
 
     CombineArgs c;
     c.B = s->B;
@@ -305,6 +315,13 @@ const char* slimkv_status_str(slimkv_status status) {
 int slimkv_abi_version(void) { return SLIMKV_ABI_VERSION; }
 
 int slimkv_kernel_path(const slimkv_shape* shape, int which) { return select_path(shape, which); }
+
+void slimkv_time_next_decode(void* start_event, void* stop_event) {
+    DecodeTimer& t = decode_timer();
+    t.start = static_cast<cudaEvent_t>(start_event);
+    t.stop = static_cast<cudaEvent_t>(stop_event);
+    if (!t.start || !t.stop) t.start = t.stop = nullptr;
+}
 
 int slimkv_force_simt(int on) {
     const int prev = g_force_simt;

@@ -82,6 +82,22 @@ struct CombineArgs {
     int slot_begin[kMaxB + 1];   // partial slots of batch element b: [slot_begin[b], slot_begin[b+1])
 };
 
+// Events requested by slimkv_time_next_decode for the next call of this thread.
+struct DecodeTimer {
+    cudaEvent_t start = nullptr, stop = nullptr;
+};
+DecodeTimer& decode_timer();
+// Record the pending start event on `st` (before the decode launch).
+inline void timer_before(cudaStream_t st) {
+    if (decode_timer().start) cudaEventRecord(decode_timer().start, st);
+}
+// Record the pending stop event on `st` (after the decode launch) and clear the request.
+inline void timer_after(cudaStream_t st) {
+    DecodeTimer& t = decode_timer();
+    if (t.stop) cudaEventRecord(t.stop, st);
+    t.start = t.stop = nullptr;
+}
+
 // ---- kernels (simt_kernels.cu) ----
 template <typename T>
 cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* q_rot,
@@ -94,5 +110,9 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl);
 template <typename T>
 cudaError_t launch_simt_reconstruct(const T* C, const T* U, T* out, int rows, int n, int r,
                                     cudaStream_t st);
+
+// Materialise out[rows, n] = C[rows, r] . U[n, r]^T in bf16 (reconstruction baseline).
+cudaError_t launch_reconstruct_gemm(const __nv_bfloat16* C, const __nv_bfloat16* U, __nv_bfloat16* out,
+                                    int rows, int n, int r, cudaStream_t st);
 
 }  // namespace slimkv

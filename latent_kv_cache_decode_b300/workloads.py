@@ -138,6 +138,8 @@ def _normal(rng: np.random.Generator, shape) -> np.ndarray:
 def orthonormal_columns(rng: np.random.Generator, rows: int, cols: int) -> np.ndarray:
     """rows x cols matrix with orthonormal columns (QR of a float64 Gaussian,
     column signs fixed so that diag(R) > 0)."""
+    if cols > rows:
+        raise ValueError(f"{rows}x{cols} cannot have orthonormal columns")
     a = rng.standard_normal((rows, cols))
     qm, rm = np.linalg.qr(a)
     sgn = np.sign(np.diag(rm))

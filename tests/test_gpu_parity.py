@@ -101,7 +101,7 @@ EDGE = [
     dict(name="one-window-token", N_b=128, W=1),
     dict(name="ragged", N_b=333, W=77, B=3),
     dict(name="rank32", N_b=256, W=64, rank=32),
-    dict(name="rank512", N_b=200, W=50, rank=512),
+    dict(name="rank512", Hq=16, Hkv=4, N_b=200, W=50, rank=512),
     dict(name="mha", Hq=8, Hkv=8, N_b=150, W=40),
     dict(name="group5", Hq=40, Hkv=8, N_b=256, W=128),
     dict(name="mqa", Hq=16, Hkv=1, N_b=256, W=128),
