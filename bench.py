@@ -1,0 +1,355 @@
+#!/usr/bin/env python
+"""SlimKV decode-attention benchmark: prints ONE JSON line.
+
+The headline workload is 128K context at 16x compression on the Llama-3.1-8B
+attention shape (batch 8, 32 query / 8 KV heads, d = 128, 8192 beacon states at
+latent rank 256 plus a 2048-token raw window, 32 layers). One "step" is one
+decode step: the slimkv_decode_attn call of each of the 32 layers, each layer
+with its own cache buffers in HBM (4 GiB of cache per step, far larger than L2,
+so no flush is needed between steps).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl slimkv|reference]
+                  [--config 2] [--mode latent|reconstruct|full]
+
+--impl reference times the float64 CPU oracle on the host cores on a bounded
+sample of the same workload (the pages describe a method, not a program).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step & HBM GB/s (frac of 8 TB/s), 128K ctx @16x, 1 B300"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def _workload(cfg: int):
+    from latent_kv_cache_decode_b300 import workloads as wl
+    return wl.config(cfg)
+
+
+def build_layers(w, device, unique: int = 4):
+    """Device buffers for every layer. Values come from the seeded generator for
+    `unique` distinct layers (every distinct rank for variable-rank workloads);
+    every layer still gets buffers of its own, so each step streams the whole
+    cache from HBM."""
+    from latent_kv_cache_decode_b300 import workloads as wl
+    src = {}
+    layers = []
+    for l in range(w.layers):
+        key = w.r(l) if w.ranks is not None else l % unique
+        if key not in src:
+            src[key] = wl.layer_tensors(w, l)
+        layers.append({k: v.to(device).clone() for k, v in src[key].items()})
+    return layers
+
+
+def _cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else os.cpu_count()
+    except Exception:
+        return os.cpu_count()
+
+
+def oracle_layer_seconds(w, layers_sample):
+    """Wall time of the float64 oracle on the given layers (host cores)."""
+    import oracle
+    from latent_kv_cache_decode_b300 import workloads as wl
+    secs = []
+    for l in layers_sample:
+        t = wl.layer_tensors(w, l)
+        f = {k: (wl.as_f64(v) if k != "q_pos" else v.numpy()) for k, v in t.items()}
+        t0 = time.perf_counter()
+        oracle.decode_attn(f["q"], f["C_K"], f["C_V"], f["K_raw"], f["V_raw"], f["U_K"], f["U_V"],
+                           f["q_pos"], w.scale, w.rope_base)
+        secs.append(time.perf_counter() - t0)
+    return secs
+
+
+def run_reference(args):
+    """CPU oracle arm: each step is one sampled layer, reported per full step."""
+    w = _workload(args.config)
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    n = args.warmup + args.steps
+    layers = [(i * 7) % w.layers for i in range(n)]
+    secs = oracle_layer_seconds(w, layers)
+    timed = secs[args.warmup:]
+    us_step = statistics.mean(timed) * w.layers * 1e6
+    sample = (f"{len(timed)} sampled layers of {w.layers} (one per step, after {args.warmup} "
+              f"warm-up layers), float64 numpy oracle, mean per layer x{w.layers}")
+    return {"impl": "reference", "metric": METRIC, "value": us_step, "unit": "us/step",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
+            "config": {"workload": w.name, "batch": w.B, "layers": w.layers, "N_b": w.N_b,
+                       "W": w.W, "rank": w.rank or "per-layer", "mode": "latent"},
+            "cpu_baseline": {"value": us_step, "unit": "us/step", "cores": _cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": us_step, "unit": "us/step", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def run_slimkv(args):
+    import torch
+    import torch.distributed as dist
+    from latent_kv_cache_decode_b300 import binding as bd
+    from latent_kv_cache_decode_b300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = bd.load()
+    w = _workload(args.config)
+    mode = args.mode
+    layers = build_layers(w, dev)
+    full = []
+    n_buf = 0
+    if mode == "full":
+        # uncompressed cache of T_full tokens per layer, drawn on the device from a
+        # seeded generator; cycled over distinct buffers when HBM is short
+        free, _ = torch.cuda.mem_get_info()
+        per_layer = 2 * w.B * w.T_full * w.Hkv * w.d * 2
+        n_buf = max(2, min(w.layers, int(0.8 * free // per_layer)))
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed)
+        for _ in range(n_buf):
+            K = torch.randn((w.B, w.T_full, w.Hkv, w.d), generator=g, device=dev, dtype=torch.bfloat16)
+            V = torch.randn((w.B, w.T_full, w.Hkv, w.d), generator=g, device=dev, dtype=torch.bfloat16)
+            full.append((K, V))
+    stream = torch.cuda.Stream(device=dev)
+    ws = bd.Workspace(dev)
+    outs = [torch.empty((w.B, w.Hq, w.d), dtype=torch.float32, device=dev) for _ in layers]
+
+    def call(l, t):
+        kw = dict(scale=w.scale, rope_base=w.rope_base, out=outs[l], workspace=ws, stream=stream)
+        if mode == "latent":
+            bd.decode_attn(t["q"], t["C_K"], t["C_V"], t["K_raw"], t["V_raw"], t["U_K"], t["U_V"],
+                           t["q_pos"], **kw)
+        elif mode == "reconstruct":
+            bd.decode_attn_reconstruct(t["q"], t["C_K"], t["C_V"], t["K_raw"], t["V_raw"], t["U_K"],
+                                       t["U_V"], t["q_pos"], **kw)
+        else:
+            K, V = full[l % n_buf]
+            bd.decode_attn_full_kv(t["q"], K, V, t["q_pos"], **kw)
+
+    def step():
+        for l, t in enumerate(layers):
+            call(l, t)
+
+    # size the workspace and build the plans outside the capture
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # dominant kernel (split decode) timed alone: events around each launch
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, min(args.steps, 5))):
+            for l, t in enumerate(layers):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                lib.slimkv_time_next_decode(a.cuda_event, b.cuda_event)
+                call(l, t)
+                evs.append((a, b))
+    torch.cuda.synchronize()
+    kern_ms = [a.elapsed_time(b) for a, b in evs]
+    kern_avg_ms = statistics.mean(kern_ms)
+
+    # end to end through the public API with host buffers: each layer's q and
+    # q_pos are copied from pinned host memory and its out read back, inside the
+    # timed region (the cache is device-resident state, like model weights)
+    q_host = [t["q"].cpu().pin_memory() for t in layers]
+    pos_host = [t["q_pos"].cpu().pin_memory() for t in layers]
+    out_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(q.numel() * q.element_size() + p.numel() * p.element_size()
+              for q, p in zip(q_host, pos_host))
+    d2h = sum(o.numel() * o.element_size() for o in out_host)
+    e2e_steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            for l, t in enumerate(layers):
+                t["q"].copy_(q_host[l], non_blocking=True)
+                t["q_pos"].copy_(pos_host[l], non_blocking=True)
+                call(l, t)
+                out_host[l].copy_(outs[l], non_blocking=True)
+        stream.synchronize()
+    e2e_us = (time.perf_counter() - t0) / e2e_steps * 1e6
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+    peak, peak_kind = _peaks()
+    if mode == "full":
+        cache_b = w.layers * 2 * w.B * w.T_full * w.Hkv * w.d * 2
+    else:
+        cache_b = sum(wl.cache_bytes(w, l) for l in range(w.layers))
+    us = ms * 1e3
+    layer_bytes = cache_b / w.layers
+    achieved = layer_bytes / (kern_avg_ms * 1e-3) / 1e9
+    launches_per_call = {"latent": 3, "reconstruct": 5, "full": 3}[mode]
+    res = {
+        "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator)",
+        "config": {"workload": w.name, "batch": w.B, "layers": w.layers, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "d": w.d, "N_b": w.N_b, "rank": w.rank or "per-layer", "W": w.W, "mode": mode,
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": "no flush: each step streams the whole per-layer cache (>> 126 MB L2)"},
+        "tokens_per_s": world * w.B / (ms * 1e-3),
+        "cache_bytes_per_step": cache_b,
+        "hbm_gbs": cache_b / (ms * 1e-3) / 1e9,
+        "frac_of_8tbs": cache_b / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
+        "frac_of_measured_copy": cache_b / (ms * 1e-3) / 1e9 / peak,
+        "roofline": {"bound": "hbm", "kernel": "tc_decode_kernel", "achieved": achieved,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "launch_us": kern_avg_ms * 1e3, "bytes_per_launch": layer_bytes},
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * w.layers * launches_per_call,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        sample_layers = [0, w.layers // 2]
+        secs = oracle_layer_seconds(w, sample_layers)
+        v = statistics.mean(secs) * w.layers * 1e6
+        res["cpu_baseline"] = {"value": v, "unit": "us/step", "cores": _cpu_cores(), "kind": "oracle",
+                               "sample": f"layers {sample_layers} of {w.layers}, float64 numpy "
+                                         f"oracle, mean per layer x{w.layers}"}
+    if world > 1:
+        dist.destroy_process_group()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="slimkv", choices=["slimkv", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--mode", default="latent", choices=["latent", "reconstruct", "full"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    res = run_reference(args) if args.impl == "reference" else run_slimkv(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()
