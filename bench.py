@@ -101,9 +101,14 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
-def _workload(cfg: int):
+def _workload(cfg: int, layers: int = 0):
+    import dataclasses
     from latent_kv_cache_decode_b300 import workloads as wl
-    return wl.config(cfg)
+    w = wl.config(cfg)
+    if layers and layers < w.layers:
+        w = dataclasses.replace(w, layers=layers,
+                                ranks=w.ranks[:layers] if w.ranks is not None else None)
+    return w
 
 
 def build_layers(w, device, unique: int = 4):
@@ -148,7 +153,7 @@ def oracle_layer_seconds(w, layers_sample):
 
 def run_reference(args):
     """CPU oracle arm: each step is one sampled layer, reported per full step."""
-    w = _workload(args.config)
+    w = _workload(args.config, args.layers)
     if int(os.environ.get("RANK", "0")) != 0:
         return None
     n = args.warmup + args.steps
@@ -184,7 +189,7 @@ def run_slimkv(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     lib = bd.load()
-    w = _workload(args.config)
+    w = _workload(args.config, args.layers)
     mode = args.mode
     layers = build_layers(w, dev)
     full = []
@@ -253,17 +258,25 @@ def run_slimkv(args):
         ms = float(tt.item())
 
     # dominant kernel (split decode) timed alone: events around each launch
+    # (raw CUDA events: the library records them on the launching stream itself)
+    from cuda.bindings import runtime as rt
     evs = []
     with torch.cuda.stream(stream):
         for _ in range(max(1, min(args.steps, 5))):
             for l, t in enumerate(layers):
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                lib.slimkv_time_next_decode(a.cuda_event, b.cuda_event)
+                a, b = rt.cudaEventCreate()[1], rt.cudaEventCreate()[1]
+                lib.slimkv_time_next_decode(int(a), int(b))
                 call(l, t)
                 evs.append((a, b))
     torch.cuda.synchronize()
-    kern_ms = [a.elapsed_time(b) for a, b in evs]
+    kern_ms = []
+    for a, b in evs:
+        err, t_ms = rt.cudaEventElapsedTime(a, b)
+        if err != rt.cudaError_t.cudaSuccess:
+            raise RuntimeError(f"cudaEventElapsedTime: {err}")
+        kern_ms.append(t_ms)
+        rt.cudaEventDestroy(a)
+        rt.cudaEventDestroy(b)
     kern_avg_ms = statistics.mean(kern_ms)
 
     # end to end through the public API with host buffers: each layer's q and
@@ -344,6 +357,8 @@ def main():
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--mode", default="latent", choices=["latent", "reconstruct", "full"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers (small profiling captures; 0 = all)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     res = run_reference(args) if args.impl == "reference" else run_slimkv(args)
