@@ -111,18 +111,18 @@ def _workload(cfg: int, layers: int = 0):
     return w
 
 
-def build_layers(w, device, unique: int = 4):
+def build_layers(w, device, unique: int = 4, batch=None):
     """Device buffers for every layer. Values come from the seeded generator for
     `unique` distinct layers (every distinct rank for variable-rank workloads);
     every layer still gets buffers of its own, so each step streams the whole
-    cache from HBM."""
+    cache from HBM. `batch` lists the global batch elements this rank owns."""
     from latent_kv_cache_decode_b300 import workloads as wl
     src = {}
     layers = []
     for l in range(w.layers):
         key = w.r(l) if w.ranks is not None else l % unique
         if key not in src:
-            src[key] = wl.layer_tensors(w, l)
+            src[key] = wl.layer_tensors(w, l, batch=batch)
         layers.append({k: v.to(device).clone() for k, v in src[key].items()})
     return layers
 
@@ -191,7 +191,8 @@ def run_slimkv(args):
     lib = bd.load()
     w = _workload(args.config, args.layers)
     mode = args.mode
-    layers = build_layers(w, dev)
+    from latent_kv_cache_decode_b300.sharding import batch_shard, max_over_ranks
+    layers = build_layers(w, dev, batch=batch_shard(w.B, world, rank))
     full = []
     n_buf = 0
     if mode == "full":
@@ -251,11 +252,7 @@ def run_slimkv(args):
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dist if world > 1 else None, dev)
 
     # dominant kernel (split decode) timed alone: events around each launch
     # (raw CUDA events: the library records them on the launching stream itself)
@@ -320,7 +317,8 @@ def run_slimkv(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator)",
         "config": {"workload": w.name, "batch": w.B, "layers": w.layers, "Hq": w.Hq, "Hkv": w.Hkv,
                    "d": w.d, "N_b": w.N_b, "rank": w.rank or "per-layer", "W": w.W, "mode": mode,
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "parallelism": f"batch-sharded dp{world}" if world > 1 else "1 GPU",
+                   "global_batch": world * w.B,
                    "l2": "no flush: each step streams the whole per-layer cache (>> 126 MB L2)"},
         "tokens_per_s": world * w.B / (ms * 1e-3),
         "cache_bytes_per_step": cache_b,
