@@ -63,7 +63,9 @@ typedef enum {
     SLIMKV_ERR_DTYPE = 3,     /* unknown storage dtype                            */
     SLIMKV_ERR_ALIGN = 4,     /* a pointer breaks the alignment rule              */
     SLIMKV_ERR_WORKSPACE = 5, /* workspace missing or smaller than required       */
-    SLIMKV_ERR_CUDA = 6       /* a CUDA launch or driver call failed              */
+    SLIMKV_ERR_CUDA = 6,      /* a CUDA launch or driver call failed              */
+    SLIMKV_ERR_TOO_LARGE = 7  /* the shape needs more scratch than the fixed array
+                                 of slimkv_decode_attn_noalloc holds              */
 } slimkv_status;
 
 /* Storage type of q, C_K, C_V, K_raw, V_raw, K, V, U_K and U_V. Arithmetic is
@@ -139,6 +141,38 @@ slimkv_status slimkv_decode_attn_full_kv(const slimkv_shape* shape, const void* 
                                          const void* K, const void* V,
                                          const int32_t* q_pos, float* out,
                                          void* workspace, size_t ws_bytes, void* stream);
+
+/* Size of the fixed device scratch array behind slimkv_decode_attn_noalloc. */
+#define SLIMKV_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* slimkv_decode_attn for callers that cannot allocate device memory. The SlimKV
+ * pages have no counterpart to this call; it exists for host programs that have no
+ * way to hand the library a workspace: an inference engine that reserves nearly all
+ * of HBM in its own pool and forbids other allocations, a plain C caller that links
+ * no device allocator, or a latency-critical decode loop in which a cudaMalloc
+ * (which may synchronise the device and can fail once memory is fragmented) is not
+ * allowed.
+ *
+ * Arguments and result are those of slimkv_decode_attn without the workspace. The
+ * scratch is one file-scope device array of SLIMKV_NOALLOC_SCRATCH_BYTES (64 MiB)
+ * that every GPU which loads the library's device code holds until the process
+ * exits; this call itself allocates and frees nothing.
+ *  - A shape whose workspace (slimkv_workspace_bytes(shape, SLIMKV_LATENT)) exceeds
+ *    SLIMKV_NOALLOC_SCRATCH_BYTES is rejected with SLIMKV_ERR_TOO_LARGE before any
+ *    launch; other argument errors are reported as by slimkv_decode_attn.
+ *  - The first call on a device looks up the array's device address on that device
+ *    (cudaGetSymbolAddress, with that device current); make that first call before
+ *    any stream capture. A failed lookup returns SLIMKV_ERR_CUDA.
+ *  - All calls on a device share the one array, and it keeps the previous call's
+ *    contents; no call depends on them (each writes every scratch word before
+ *    reading it). Calls that may overlap on the GPU (different streams, or
+ *    different host threads without ordering) race on the array: serialise them,
+ *    e.g. on one stream. */
+slimkv_status slimkv_decode_attn_noalloc(const slimkv_shape* shape, const void* q,
+                                         const void* C_K, const void* C_V,
+                                         const void* K_raw, const void* V_raw,
+                                         const void* U_K, const void* U_V,
+                                         const int32_t* q_pos, float* out, void* stream);
 
 /* Human-readable name of a status. Never NULL. */
 const char* slimkv_status_str(slimkv_status status);

@@ -20,12 +20,15 @@ LIB_PATH = os.path.join(_PKG, "libslimkv.so")
 SLIMKV_F32, SLIMKV_BF16 = 0, 1
 SLIMKV_LATENT, SLIMKV_RECONSTRUCT, SLIMKV_FULL_KV = 0, 1, 2
 STATUS = {0: "SLIMKV_OK", 1: "SLIMKV_ERR_NULL", 2: "SLIMKV_ERR_SHAPE", 3: "SLIMKV_ERR_DTYPE",
-          4: "SLIMKV_ERR_ALIGN", 5: "SLIMKV_ERR_WORKSPACE", 6: "SLIMKV_ERR_CUDA"}
+          4: "SLIMKV_ERR_ALIGN", 5: "SLIMKV_ERR_WORKSPACE", 6: "SLIMKV_ERR_CUDA",
+          7: "SLIMKV_ERR_TOO_LARGE"}
+NOALLOC_SCRATCH_BYTES = 64 << 20   # SLIMKV_NOALLOC_SCRATCH_BYTES
 
 # every symbol include/slimkv.h declares
 EXPORTS = ("slimkv_workspace_bytes", "slimkv_decode_attn", "slimkv_decode_attn_reconstruct",
            "slimkv_decode_attn_full_kv", "slimkv_status_str", "slimkv_abi_version",
-           "slimkv_kernel_path", "slimkv_force_simt", "slimkv_time_next_decode")
+           "slimkv_kernel_path", "slimkv_force_simt", "slimkv_time_next_decode",
+           "slimkv_decode_attn_noalloc")
 
 
 class SlimkvError(RuntimeError):
@@ -63,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.slimkv_decode_attn_reconstruct.restype = ctypes.c_int
     lib.slimkv_decode_attn_full_kv.argtypes = [sp, vp, vp, vp, i32p, vp, vp, sz, vp]
     lib.slimkv_decode_attn_full_kv.restype = ctypes.c_int
+    lib.slimkv_decode_attn_noalloc.argtypes = [sp] + [vp] * 7 + [i32p, vp, vp]
+    lib.slimkv_decode_attn_noalloc.restype = ctypes.c_int
     lib.slimkv_status_str.argtypes = [ctypes.c_int]
     lib.slimkv_status_str.restype = ctypes.c_char_p
     lib.slimkv_abi_version.argtypes = []
@@ -199,6 +204,28 @@ def decode_attn_full_kv(q, K, V, q_pos, *, scale=None, rope_base=10000.0, out=No
     st = lib.slimkv_decode_attn_full_kv(ctypes.byref(sh), _ptr(q), _ptr(K), _ptr(V), _ptr(q_pos),
                                         _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "slimkv_decode_attn_full_kv")
+    return out
+
+
+def decode_attn_noalloc(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, *, scale=None,
+                        rope_base=10000.0, out=None, stream=None):
+    """slimkv_decode_attn_noalloc on torch CUDA tensors: the library uses its own fixed
+    device scratch array instead of a caller workspace (for callers that cannot
+    allocate device memory). ``out`` may be preallocated; nothing else is allocated."""
+    lib = load()
+    B, Hq, d = q.shape
+    N_b = C_K.shape[1] if C_K is not None else 0
+    W = K_raw.shape[1] if K_raw is not None else 0
+    Hkv = U_K.shape[0] // d if U_K is not None else K_raw.shape[2]
+    r_k = C_K.shape[2] if C_K is not None else 0
+    r_v = C_V.shape[2] if C_V is not None else 0
+    sh = make_shape(B, Hq, Hkv, d, N_b, r_k, r_v, W, q.dtype, scale, rope_base)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    st = lib.slimkv_decode_attn_noalloc(ctypes.byref(sh), _ptr(q), _ptr(C_K), _ptr(C_V),
+                                        _ptr(K_raw), _ptr(V_raw), _ptr(U_K), _ptr(U_V),
+                                        _ptr(q_pos), _ptr(out), _stream(stream))
+    _check(st, "slimkv_decode_attn_noalloc")
     return out
 
 

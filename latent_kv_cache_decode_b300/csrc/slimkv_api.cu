@@ -308,6 +308,7 @@ const char* slimkv_status_str(slimkv_status status) {
         case SLIMKV_ERR_ALIGN: return "pointer breaks the alignment rule";
         case SLIMKV_ERR_WORKSPACE: return "workspace too small";
         case SLIMKV_ERR_CUDA: return "CUDA launch or driver call failed";
+        case SLIMKV_ERR_TOO_LARGE: return "shape needs more scratch than the no-allocation entry point holds";
     }
     return "unknown status";
 }

@@ -113,6 +113,17 @@ def test_null_misaligned_and_small_workspace_rejected(lib):
     assert _call(lib, sr, good, 1 << 40, "slimkv_decode_attn_reconstruct") == 2
 
 
+def test_noalloc_host_checks(lib):
+    # oversized shapes and bad shapes are rejected before any device work
+    big = _shape(B=256, Hq=128, r_k=512, r_v=512)
+    assert bd.workspace_bytes(big, bd.SLIMKV_LATENT) > bd.NOALLOC_SCRATCH_BYTES
+    p = [256 * (i + 1) for i in range(7)] + [4096, 8192]
+    assert lib.slimkv_decode_attn_noalloc(ctypes.byref(big), *p, None) == 7
+    assert lib.slimkv_decode_attn_noalloc(ctypes.byref(_shape(Hq=30)), *p, None) == 2
+    assert lib.slimkv_decode_attn_noalloc(None, *p, None) == 1
+    assert lib.slimkv_status_str(7) != b"unknown status"
+
+
 def test_unused_operands_may_be_null(lib):
     # W == 0: K_raw/V_raw may be NULL; N_b == 0: C_K, C_V, U_K, U_V may be NULL.
     # A too-small workspace is then the first error reported (nothing launches).
