@@ -9,6 +9,8 @@
 // grouping, RoPE on all queries and on raw keys only).
 #include <math.h>
 
+#include <algorithm>
+
 #include "slimkv_internal.cuh"
 
 namespace slimkv {
@@ -43,60 +45,158 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------------------
-// Query RoPE and latent projection. One CTA per (KV group g, batch element b):
-// q_rot[b,h] = RoPE(q[b,h], q_pos[b]) for the heads of group g, and, when q_lat
-// is given, q_lat[b,h,:] = q_rot[b,h,:] . U_K^(g) (the projection is taken after
-// grouping, so U_K^(g) is read once for the G heads that share it).
-// The RoPE angle q_pos * base^(-2i/d) is formed and rotated in double precision.
+// Query RoPE and latent projection, "Latent-space attention removes the rebuild
+// step": RoPE stays on every query, and the beacon query is projected into the
+// latent space per GQA group, q_lat[b,h,:] = RoPE(q[b,h]) . U_K^(g) (the
+// projection is taken after grouping, so U_K^(g) serves the G heads of group g).
+//
+// Grid (Hkv, column blocks of 32 latent columns, row blocks). A row is one
+// (batch element, head of group g) pair; a CTA holds at most 32 rows: `nbb`
+// whole batch elements when G <= 32, else one 32-head chunk of one element.
+// The rotation angle p * theta_i is reduced modulo one turn exactly with 64-bit
+// fixed-point arithmetic (turn[i] = theta_i / 2pi), then sin/cos of the reduced
+// angle are taken in float32; both outputs are scaled by scale * log2(e).
 // ---------------------------------------------------------------------------
+constexpr int kQpRows = 32;
+constexpr int kQpCols = 32;
+constexpr int kQpThreads = 128;
+
+// 16-byte vector of storage elements: 8 bf16 or 4 float32.
+template <typename T> struct Vec16;
+template <> struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    static __device__ __forceinline__ void to_f(const uint4& v, float* out) {
+        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(p[i]);
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
+    }
+};
+template <> struct Vec16<float> {
+    static constexpr int N = 4;
+    static __device__ __forceinline__ void to_f(const uint4& v, float* out) {
+        out[0] = __uint_as_float(v.x);
+        out[1] = __uint_as_float(v.y);
+        out[2] = __uint_as_float(v.z);
+        out[3] = __uint_as_float(v.w);
+    }
+};
+
 template <typename T>
-__global__ void __launch_bounds__(256) qproj_kernel(const T* __restrict__ q,
-                                                     const T* __restrict__ U_K,
-                                                     const int32_t* __restrict__ q_pos,
-                                                     float* __restrict__ q_rot,
-                                                     float* __restrict__ q_lat, int Hq, int Hkv,
-                                                     int d, int r_k, double base) {
-    extern __shared__ float qr_s[];  // [G][d]
+__global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant__ QprojArgs a) {
+    __shared__ __align__(16) float qr_s[kQpRows][128];   // query rows, rotated in place (scaled)
+    __shared__ float cs_s[kQpRows][64], sn_s[kQpRows][64];   // per batch element of the block
+    __shared__ __align__(16) float u_s[128][kQpCols];        // U_K^(g) column block
+    constexpr int VN = Vec16<T>::N;
     pdl_trigger();
-    const int g = blockIdx.x, b = blockIdx.y;
-    const int G = Hq / Hkv;
-    const int half = d >> 1;
-    const double pos = (double)q_pos[b];
-    for (int idx = threadIdx.x; idx < G * half; idx += blockDim.x) {
-        const int hl = idx / half, i = idx - hl * half;
-        const int h = g * G + hl;
-        const double theta = pow(base, -2.0 * (double)i / (double)d);
-        double sn, cs;
-        sincos(pos * theta, &sn, &cs);
-        const T* qh = q + ((size_t)b * Hq + h) * d;
-        const double x1 = (double)to_f(qh[i]), x2 = (double)to_f(qh[i + half]);
-        qr_s[hl * d + i] = (float)(x1 * cs - x2 * sn);
-        qr_s[hl * d + i + half] = (float)(x2 * cs + x1 * sn);
+    const int g = blockIdx.x, cb = blockIdx.y, rb = blockIdx.z;
+    const int tid = threadIdx.x;
+    const int G = a.Hq / a.Hkv, d = a.d, half = d >> 1;
+    // rows of this block: batch elements [b0, b0 + nb) x heads-in-group [i0, i1)
+    int b0, nb, i0, i1;
+    if (a.hcn == 1) {
+        b0 = rb * a.nbb;
+        nb = min(a.nbb, a.B - b0);
+        i0 = 0;
+        i1 = G;
+    } else {
+        b0 = rb / a.hcn;
+        nb = 1;
+        i0 = (rb % a.hcn) * 32;
+        i1 = min(G, i0 + 32);
+    }
+    const int ni = i1 - i0, rows = nb * ni;
+
+    // issue every global load of the block before using any of them
+    const int qv = d / VN;                                  // vectors per query row
+    const int nq = rows * qv;                               // <= 32 * 32
+    const int nu = a.U_K ? d * (kQpCols / VN) : 0;          // vectors of the U_K block
+    constexpr int kMaxLd = (32 * 32 + 128 * 8) / kQpThreads;   // 16
+    uint4 buf[kMaxLd];
+#pragma unroll
+    for (int k = 0; k < kMaxLd; ++k) {
+        const int idx = tid + k * kQpThreads;
+        if (idx < nq) {
+            const int r = idx / qv, e = (idx - r * qv) * VN;
+            const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
+            buf[k] = *reinterpret_cast<const uint4*>((const T*)a.q + ((size_t)(b0 + bl) * a.Hq + h) * d + e);
+        } else if (idx - nq < nu) {
+            const int j = idx - nq, i = j / (kQpCols / VN), e = (j - i * (kQpCols / VN)) * VN;
+            buf[k] = *reinterpret_cast<const uint4*>((const T*)a.U_K + ((size_t)g * d + i) * a.r_k +
+                                                     cb * kQpCols + e);
+        }
+    }
+    // cos / sin of p * theta_i per batch element: the angle reduced to a signed
+    // fraction of a turn (exact 64-bit wrap-around), then sin / cos in float32
+    for (int idx = tid; idx < nb * half; idx += kQpThreads) {
+        const int bl = idx / half, i = idx - bl * half;
+        const unsigned long long pos = (unsigned long long)(long long)a.q_pos[b0 + bl];
+        const long long frac = (long long)(pos * a.turn[i]);
+        float sn, cs;
+        sincospif((float)frac * 1.0842021724855044e-19f, &sn, &cs);   // x 2^-63: half-turns
+        cs_s[bl][i] = cs;
+        sn_s[bl][i] = sn;
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxLd; ++k) {
+        const int idx = tid + k * kQpThreads;
+        float f[VN];
+        if (idx < nq) {
+            const int r = idx / qv, e = (idx - r * qv) * VN;
+            Vec16<T>::to_f(buf[k], f);
+#pragma unroll
+            for (int v = 0; v < VN; ++v) qr_s[r][e + v] = f[v];
+        } else if (idx - nq < nu) {
+            const int j = idx - nq, i = j / (kQpCols / VN), e = (j - i * (kQpCols / VN)) * VN;
+            Vec16<T>::to_f(buf[k], f);
+#pragma unroll
+            for (int v = 0; v < VN; ++v) u_s[i][e + v] = f[v];
+        }
     }
     __syncthreads();
-    // the previous call's kernels may still read q_rot / q_lat of this workspace
-    pdl_wait();
-    for (int idx = threadIdx.x; idx < G * d; idx += blockDim.x) {
-        const int hl = idx / d, i = idx - hl * d;
-        q_rot[((size_t)b * Hq + g * G + hl) * d + i] = qr_s[idx];
+    for (int idx = tid; idx < rows * half; idx += kQpThreads) {
+        const int r = idx / half, i = idx - r * half;
+        const int bl = r / ni;
+        const float x1 = qr_s[r][i], x2 = qr_s[r][i + half];
+        const float c = cs_s[bl][i], sn = sn_s[bl][i];
+        qr_s[r][i] = (x1 * c - x2 * sn) * a.scale_log2;
+        qr_s[r][i + half] = (x2 * c + x1 * sn) * a.scale_log2;
     }
-    if (q_lat == nullptr) return;
-    for (int h0 = 0; h0 < G; h0 += 8) {
-        const int nh = min(8, G - h0);
-        for (int j = threadIdx.x; j < r_k; j += blockDim.x) {
-            float acc[8];
+    __syncthreads();
+    // the previous call's kernels may still read this workspace; every CTA waits
+    // (so this grid completes only after its predecessor) before writing it
+    pdl_wait();
+    if (cb == 0) {
+        for (int idx = tid; idx < rows * (d / 4); idx += kQpThreads) {
+            const int r = idx / (d / 4), e = (idx - r * (d / 4)) * 4;
+            const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
+            *reinterpret_cast<float4*>(a.q_rot + ((size_t)(b0 + bl) * a.Hq + h) * d + e) =
+                *reinterpret_cast<const float4*>(&qr_s[r][e]);
+        }
+    }
+    if (a.U_K == nullptr) return;
+    // q_lat block: 32 rows x 32 columns; thread = (column, group of 8 rows)
+    const int c = tid & 31, rg = tid >> 5;
+    float acc[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-            const T* u = U_K + (size_t)g * d * r_k + j;
-            for (int i = 0; i < d; ++i) {
-                const float uv = to_f(u[(size_t)i * r_k]);
+    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+    for (int i = 0; i < d; i += 4) {
+        const float u0 = u_s[i][c], u1 = u_s[i + 1][c], u2 = u_s[i + 2][c], u3 = u_s[i + 3][c];
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    if (k < nh) acc[k] = fmaf(qr_s[(h0 + k) * d + i], uv, acc[k]);
-            }
+        for (int k = 0; k < 8; ++k) {
+            const float4 q4 = *reinterpret_cast<const float4*>(&qr_s[rg * 8 + k][i]);
+            acc[k] = fmaf(q4.x, u0, fmaf(q4.y, u1, fmaf(q4.z, u2, fmaf(q4.w, u3, acc[k]))));
+        }
+    }
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k < nh) q_lat[((size_t)b * Hq + g * G + h0 + k) * r_k + j] = acc[k];
+    for (int k = 0; k < 8; ++k) {
+        const int r = rg * 8 + k;
+        if (r < rows) {
+            const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
+            a.q_lat[((size_t)(b0 + bl) * a.Hq + h) * a.r_k + cb * kQpCols + c] = acc[k];
         }
     }
 }
@@ -172,7 +272,7 @@ __global__ void __launch_bounds__(128) simt_decode_kernel(SimtDecodeArgs a) {
             const T* kr = Kp + (size_t)j * ks;
             float dot = 0.f;
             for (int i = 0; i < Dk; ++i) dot = fmaf(q_s[i], to_f(kr[i]), dot);
-            s = dot * a.scale_log2;
+            s = dot;   // the query carries scale * log2(e)
         }
         float cm = warp_max(s);
         if (lane == 0) red[warp] = cm;
@@ -216,104 +316,149 @@ __global__ void __launch_bounds__(128) simt_decode_kernel(SimtDecodeArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Split combine fused with the value up-projection. One CTA per (KV group g,
-// batch element b), 128 threads. For each head h of the group it merges the
-// partials of batch b by their log2-domain maxima:
+// Split combine fused with the value up-projection ("(A C_V) U_V^T": the latent
+// aggregate is up-projected once, after all beacon splits are merged). One CTA
+// per (query head h, batch element b), g its KV group. The partials of batch b
+// that cover head h (SlotKind) are merged by their log2-domain maxima:
 //   M = max_s m_s, w_s = exp2(m_s - M), L = sum_s w_s l_s,
-//   z = sum_{latent s} w_s acc_s (latent, r_v wide), y = sum_{raw s} w_s acc_s,
+//   z = sum_{latent s} w_s acc_s (r_v wide), y = sum_{raw s} w_s acc_s (d wide),
 //   out[b,h,:] = (z . U_V^(g)T + y) / L.
+// Global loads are issued in independent batches so that the kernel costs a few
+// memory round trips, not one per partial.
 // ---------------------------------------------------------------------------
-constexpr int kCombHeads = 8;
+constexpr int kCombThreads = 256;
+constexpr int kCombBatch = 8;
 
 template <typename T>
-__global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
-    __shared__ float z_s[kCombHeads][kMaxRank];
-    __shared__ float y_s[kCombHeads][128];
-    __shared__ float M_s[kCombHeads], L_s[kCombHeads];
+__global__ void __launch_bounds__(kCombThreads) combine_kernel(const __grid_constant__ CombineArgs a) {
+    extern __shared__ float dyn[];   // lat: slot, weight; raw: slot, weight (each up to ns)
+    __shared__ __align__(16) float z_s[kMaxRank];
+    __shared__ float y_s[128];
+    __shared__ int n_lat_s, n_raw_s;
+    __shared__ float L_s;
     pdl_trigger();
-    const int g = blockIdx.x, b = blockIdx.y;
+    const int h = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int G = a.Hq / a.Hkv;
+    const int G = a.Hq / a.Hkv, g = h / G;
     const bool latent = a.U_V != nullptr;
-    pdl_wait();
-    const int s0 = a.slot_begin[b], s1 = a.slot_begin[b + 1];
-    for (int h0 = 0; h0 < G; h0 += kCombHeads) {
-        const int nh = min(kCombHeads, G - h0);
-        // per-head max and weighted sum, one warp per head
-        for (int k = warp; k < nh; k += 4) {
-            const int h = g * G + h0 + k;
-            float M = -INFINITY;
-            for (int s = s0 + lane; s < s1; s += 32) M = fmaxf(M, a.ml[((size_t)s * 2) * a.Hq + h]);
-            M = warp_max(M);
-            float L = 0.f;
-            for (int s = s0 + lane; s < s1; s += 32) {
-                const float ms = a.ml[((size_t)s * 2) * a.Hq + h];
-                const float ls = a.ml[((size_t)s * 2 + 1) * a.Hq + h];
-                L += (ls != 0.f) ? exp2f(ms - M) * ls : 0.f;   // a NaN partial poisons L
+    pdl_wait();   // partials come from the decode kernel
+    const int s0 = a.slot_begin[b], ns = a.slot_begin[b + 1] - s0;
+    int* lat_slot = reinterpret_cast<int*>(dyn);
+    float* lat_w = dyn + ns;
+    int* raw_slot = reinterpret_cast<int*>(dyn + 2 * ns);
+    float* raw_w = dyn + 3 * ns;
+    if (warp == 0) {
+        // compact the partials that cover head h, then their weights
+        int nl = 0, nr = 0;
+        float M = -INFINITY;
+        for (int base = 0; base < ns; base += 32) {
+            const int s = base + lane;
+            int kd = -1;
+            float m = -INFINITY, l = 0.f;
+            if (s < ns) {
+                kd = a.kind[s0 + s];
+                m = a.ml[((size_t)(s0 + s) * 2) * a.Hq + h];
+                l = a.ml[((size_t)(s0 + s) * 2 + 1) * a.Hq + h];
             }
-            L = warp_sum(L);
-            if (lane == 0) {
-                M_s[k] = M;
-                L_s[k] = L;
+            const bool is_lat = latent && kd == kSlotLatent;
+            const bool is_raw = kd == kSlotRawAll || kd == kSlotRawGroup + g;
+            const bool use = (is_lat || is_raw) && l != 0.f;   // a NaN (poisoned) l is kept
+            if (use) M = fmaxf(M, m);
+            const unsigned bl = __ballot_sync(0xffffffffu, use && is_lat);
+            const unsigned br = __ballot_sync(0xffffffffu, use && is_raw);
+            const unsigned below = (1u << lane) - 1u;
+            if (use && is_lat) {
+                lat_slot[nl + __popc(bl & below)] = s0 + s;
+                lat_w[nl + __popc(bl & below)] = m;    // the max for now; weight below
+            }
+            if (use && is_raw) {
+                raw_slot[nr + __popc(br & below)] = s0 + s;
+                raw_w[nr + __popc(br & below)] = m;
+            }
+            nl += __popc(bl);
+            nr += __popc(br);
+        }
+        M = warp_max(M);
+        __syncwarp();
+        float L = 0.f;
+        for (int i = lane; i < nl; i += 32) {
+            const float w = exp2f(lat_w[i] - M);
+            L = fmaf(w, a.ml[((size_t)lat_slot[i] * 2 + 1) * a.Hq + h], L);
+            lat_w[i] = w;
+        }
+        for (int i = lane; i < nr; i += 32) {
+            const float w = exp2f(raw_w[i] - M);
+            L = fmaf(w, a.ml[((size_t)raw_slot[i] * 2 + 1) * a.Hq + h], L);
+            raw_w[i] = w;
+        }
+        L = warp_sum(L);
+        if (lane == 0) {
+            n_lat_s = nl;
+            n_raw_s = nr;
+            L_s = L;
+        }
+    }
+    __syncthreads();
+    const int nl = n_lat_s, nr = n_raw_s;
+    // z[j] and y[i]: batches of independent loads over the covering partials
+    auto accumulate = [&](const int* slot, const float* w, int n, int col) {
+        float acc = 0.f;
+        for (int i0 = 0; i0 < n; i0 += kCombBatch) {
+            float v[kCombBatch];
+#pragma unroll
+            for (int k = 0; k < kCombBatch; ++k)
+                v[k] = (i0 + k < n) ? a.acc[((size_t)slot[i0 + k] * a.Hq + h) * a.Dmax + col] : 0.f;
+#pragma unroll
+            for (int k = 0; k < kCombBatch; ++k)
+                if (i0 + k < n) acc = fmaf(w[i0 + k], v[k], acc);
+        }
+        return acc;
+    };
+    if (latent)
+        for (int j = tid; j < a.r_v; j += kCombThreads) z_s[j] = accumulate(lat_slot, lat_w, nl, j);
+    for (int i = tid; i < a.d; i += kCombThreads) y_s[i] = accumulate(raw_slot, raw_w, nr, i);
+    __syncthreads();
+    const float invL = 1.f / L_s;
+    if (!latent) {
+        for (int i = tid; i < a.d; i += kCombThreads) a.out[((size_t)b * a.Hq + h) * a.d + i] = y_s[i] * invL;
+        return;
+    }
+    // out[i] = (z . U_V^(g)[i, :] + y[i]) / L; a warp covers rows i = warp, warp + 8, ...
+    // with lane l owning latent columns [8l, 8l + 8) of each 256-column chunk
+    constexpr int VN = Vec16<T>::N;
+    constexpr int kRowsPerWarp = 128 / (kCombThreads / 32);   // 16 (d <= 128)
+    const int nrow = (a.d + (kCombThreads / 32) - 1) / (kCombThreads / 32);
+    for (int c0 = 0; c0 < a.r_v; c0 += 256) {
+        const int j = c0 + lane * 8;
+        float zl[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zl[e] = (j + e < a.r_v) ? z_s[j + e] : 0.f;
+        float part[kRowsPerWarp];
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            part[r] = 0.f;
+            const int i = warp + r * (kCombThreads / 32);
+            if (r < nrow && i < a.d && j < a.r_v) {
+                const T* u = (const T*)a.U_V + ((size_t)g * a.d + i) * a.r_v + j;
+                float f[8];
+#pragma unroll
+                for (int q = 0; q < 8 / VN; ++q)
+                    Vec16<T>::to_f(*reinterpret_cast<const uint4*>(u + q * VN), f + q * VN);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) part[r] = fmaf(zl[e], f[e], part[r]);
             }
         }
-        __syncthreads();
-        // weighted sums of the accumulators
-        for (int k = 0; k < nh; ++k) {
-            const int h = g * G + h0 + k;
-            const float M = M_s[k];
-            if (latent) {
-                for (int j = tid; j < a.r_v; j += 128) {
-                    float z = 0.f;
-                    for (int s = s0; s < s1; ++s) {
-                        if (a.kind[s] != 0) continue;
-                        const float ls = a.ml[((size_t)s * 2 + 1) * a.Hq + h];
-                        if (ls == 0.f) continue;
-                        const float w = exp2f(a.ml[((size_t)s * 2) * a.Hq + h] - M);
-                        z = fmaf(w, a.acc[((size_t)s * a.Hq + h) * a.Dmax + j], z);
-                    }
-                    z_s[k][j] = z;
-                }
-            }
-            for (int i = tid; i < a.d; i += 128) {
-                float y = 0.f;
-                for (int s = s0; s < s1; ++s) {
-                    if (a.kind[s] != 1) continue;
-                    const float ls = a.ml[((size_t)s * 2 + 1) * a.Hq + h];
-                    if (ls == 0.f) continue;
-                    const float w = exp2f(a.ml[((size_t)s * 2) * a.Hq + h] - M);
-                    y = fmaf(w, a.acc[((size_t)s * a.Hq + h) * a.Dmax + i], y);
-                }
-                y_s[k][i] = y;
-            }
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            const float v = warp_sum(part[r]);
+            const int i = warp + r * (kCombThreads / 32);
+            if (lane == 0 && r < nrow && i < a.d) y_s[i] += v;
         }
-        __syncthreads();
-        // out row i of head k: (z_k . U_V^(g)[i,:] + y_k[i]) / L_k; one warp per row
-        for (int i = warp; i < a.d; i += 4) {
-            float part[kCombHeads];
-#pragma unroll
-            for (int k = 0; k < kCombHeads; ++k) part[k] = 0.f;
-            if (latent) {
-                const T* u = (const T*)a.U_V + ((size_t)g * a.d + i) * a.r_v;
-                for (int j = lane; j < a.r_v; j += 32) {
-                    const float uv = to_f(u[j]);
-#pragma unroll
-                    for (int k = 0; k < kCombHeads; ++k)
-                        if (k < nh) part[k] = fmaf(z_s[k][j], uv, part[k]);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < kCombHeads; ++k) {
-                if (k < nh) {
-                    const float v = warp_sum(part[k]);
-                    if (lane == 0) {
-                        const int h = g * G + h0 + k;
-                        a.out[((size_t)b * a.Hq + h) * a.d + i] = (v + y_s[k][i]) / L_s[k];
-                    }
-                }
-            }
-        }
-        __syncthreads();
+    }
+    __syncwarp();
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const int i = warp + r * (kCombThreads / 32);
+        if (lane == 0 && r < nrow && i < a.d) a.out[((size_t)b * a.Hq + h) * a.d + i] = y_s[i] * invL;
     }
 }
 
@@ -358,16 +503,40 @@ __global__ void __launch_bounds__(256) simt_reconstruct_kernel(const T* __restri
 template <typename T>
 cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* q_rot,
                          float* q_lat, int B, int Hq, int Hkv, int d, int r_k, double base,
-                         cudaStream_t st, bool pdl) {
+                         float scale_log2, cudaStream_t st, bool pdl) {
+    QprojArgs a;
+    a.q = q;
+    a.U_K = U_K;
+    a.q_pos = q_pos;
+    a.q_rot = q_rot;
+    a.q_lat = q_lat;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.r_k = r_k;
+    a.scale_log2 = scale_log2;
     const int G = Hq / Hkv;
-    const size_t smem = (size_t)G * d * sizeof(float);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(qproj_kernel<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
+    if (G <= kQpRows) {
+        a.nbb = kQpRows / G;
+        a.hcn = 1;
+    } else {
+        a.nbb = 1;
+        a.hcn = (G + kQpRows - 1) / kQpRows;
     }
-    return launch_ex(qproj_kernel<T>, dim3(Hkv, B), dim3(256), smem, st, pdl, q, U_K, q_pos, q_rot,
-                     q_lat, Hq, Hkv, d, r_k, base);
+    // theta_i / (2 pi) as a fraction of a turn in 64-bit fixed point
+    const long double two_pi = 6.283185307179586476925286766559L;
+    for (int i = 0; i < 64; ++i) {
+        a.turn[i] = 0;
+        if (i < d / 2) {
+            long double t = powl((long double)base, -2.0L * i / d) / two_pi;
+            t -= floorl(t);
+            a.turn[i] = (unsigned long long)(t * 18446744073709551616.0L + 0.5L);
+        }
+    }
+    const int row_blocks = (G <= kQpRows) ? (B + a.nbb - 1) / a.nbb : B * a.hcn;
+    const int col_blocks = U_K ? r_k / kQpCols : 1;
+    return launch_ex(qproj_kernel<T>, dim3(Hkv, col_blocks, row_blocks), dim3(kQpThreads), 0, st, pdl, a);
 }
 
 template <typename T>
@@ -379,7 +548,11 @@ cudaError_t launch_simt_decode(const SimtDecodeArgs& a, cudaStream_t st) {
 
 template <typename T>
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl) {
-    return launch_ex(combine_kernel<T>, dim3(a.Hkv, a.B), dim3(128), 0, st, pdl, a);
+    int ns_max = 0;
+    for (int b = 0; b < a.B; ++b) ns_max = std::max(ns_max, a.slot_begin[b + 1] - a.slot_begin[b]);
+    if (ns_max > kMaxSlotsPerB) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)ns_max * 4 * sizeof(float);
+    return launch_ex(combine_kernel<T>, dim3(a.Hq, a.B), dim3(kCombThreads), smem, st, pdl, a);
 }
 
 template <typename T>
@@ -392,7 +565,7 @@ cudaError_t launch_simt_reconstruct(const T* C, const T* U, T* out, int rows, in
 
 #define SLIMKV_INST(T)                                                                           \
     template cudaError_t launch_qproj<T>(const T*, const T*, const int32_t*, float*, float*, int, \
-                                         int, int, int, int, double, cudaStream_t, bool);         \
+                                         int, int, int, int, double, float, cudaStream_t, bool);  \
     template cudaError_t launch_simt_decode<T>(const SimtDecodeArgs&, cudaStream_t);              \
     template cudaError_t launch_combine<T>(const CombineArgs&, cudaStream_t, bool);               \
     template cudaError_t launch_simt_reconstruct<T>(const T*, const T*, T*, int, int, int,        \

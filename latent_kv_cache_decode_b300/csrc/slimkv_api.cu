@@ -143,7 +143,7 @@ slimkv_status run_simt(const slimkv_shape* s, int which, const Ptrs& p, cudaStre
     const bool lat = which == SLIMKV_LATENT && s->N_b > 0;
     cudaError_t e = launch_qproj<T>((const T*)p.q, lat ? (const T*)p.U_K : nullptr, p.q_pos, q_rot,
                                     lat ? q_lat : nullptr, s->B, s->Hq, s->Hkv, s->d, s->r_k,
-                                    s->rope_base, st, false);
+                                    s->rope_base, s->scale * kLog2e, st, false);
     if (e != cudaSuccess) return SLIMKV_ERR_CUDA;
 
     SimtDecodeArgs a = {};
@@ -154,7 +154,6 @@ slimkv_status run_simt(const slimkv_shape* s, int which, const Ptrs& p, cudaStre
     a.N_b = lat ? s->N_b : 0;
     a.r_k = s->r_k;
     a.r_v = s->r_v;
-    a.scale_log2 = s->scale * kLog2e;
     a.C_K = p.C_K;
     a.C_V = p.C_V;
     a.q_rot = q_rot;

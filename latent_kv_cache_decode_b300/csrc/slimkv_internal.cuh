@@ -14,6 +14,7 @@ constexpr int kMaxHq = 128;     // query heads
 constexpr int kMaxCtas = 296;   // CTAs of one tensor-core decode launch (2 per SM on 148 SMs)
 constexpr int kSlotCap = 512;   // partial slots beyond one per segment
 constexpr int kMaxRank = 512;
+constexpr int kMaxSlotsPerB = 1024;   // partial slots of one batch element (combine limit)
 
 // Scores are kept in the log2 domain: s2 = scale * log2(e) * (q . k).
 constexpr float kLog2e = 1.4426950408889634f;
@@ -37,7 +38,7 @@ struct WsLayout {
     size_t q_lat = 0;    // float [B, Hq, r_k]        latent queries q . U_K^(g)
     size_t acc = 0;      // float [slots, Hq, Dmax]   per-split value accumulators
     size_t ml = 0;       // float [slots, 2, Hq]      per-split running max (log2) and sum
-    size_t kind = 0;     // int   [slots]             0 latent accumulator, 1 raw accumulator
+    size_t kind = 0;     // int   [slots]             what a partial covers (SlotKind)
     size_t kb = 0;       // T     [B, N_b, Hkv, d]    materialised beacon keys (reconstruct)
     size_t vb = 0;       // T     [B, N_b, Hkv, d]    materialised beacon values (reconstruct)
     size_t total = 0;
@@ -50,11 +51,14 @@ struct WsLayout {
 // flattened as token * Hkv + g, so one row is one d-vector of the cache.
 enum SegKind { kSegLatent = 0, kSegRaw0 = 1, kSegRaw1 = 2 };
 
+// What one partial slot holds: a latent accumulator (r_v wide) for every head, a
+// raw accumulator (d wide) for every head, or a raw accumulator for the heads of
+// one KV group g only (kSlotRawGroup + g; the other heads' rows are not written).
+enum SlotKind { kSlotLatent = 0, kSlotRawAll = 1, kSlotRawGroup = 2 };
 // Arguments of the SIMT split-decode kernel.
 struct SimtDecodeArgs {
     int B, Hq, Hkv, d, N_b, r_k, r_v;
     int W0, W1;                 // tokens of raw sources 0 and 1 (0 = absent)
-    float scale_log2;
     const void* C_K;
     const void* C_V;
     const void* K0;
@@ -82,6 +86,22 @@ struct CombineArgs {
     int slot_begin[kMaxB + 1];   // partial slots of batch element b: [slot_begin[b], slot_begin[b+1])
 };
 
+// Arguments of the query kernel (RoPE + latent projection). The RoPE angle of pair
+// i at integer position p is p * theta_i; turn[i] holds theta_i / (2 pi) as a
+// 64-bit fixed-point fraction of a turn, so p * turn[i] (mod 2^64) is the angle's
+// fraction of a full turn, exact up to the rounding of turn[i].
+struct QprojArgs {
+    const void* q;
+    const void* U_K;             // NULL: rotate only
+    const int32_t* q_pos;
+    float* q_rot;                // [B, Hq, d]   RoPE(q) * scale_log2
+    float* q_lat;                // [B, Hq, r_k] RoPE(q) . U_K^(g) * scale_log2
+    int B, Hq, Hkv, d, r_k;
+    int nbb, hcn;                // batch elements and 32-head chunks per CTA row block
+    float scale_log2;            // score scale * log2(e), folded into both outputs
+    unsigned long long turn[64];
+};
+
 // Events requested by slimkv_time_next_decode for the next call of this thread.
 struct DecodeTimer {
     cudaEvent_t start = nullptr, stop = nullptr;
@@ -99,10 +119,12 @@ inline void timer_after(cudaStream_t st) {
 }
 
 // ---- kernels (simt_kernels.cu) ----
+// Query RoPE and latent projection; outputs carry the factor scale*log2(e) so the
+// decode kernels read scores directly in the log2 domain.
 template <typename T>
 cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* q_rot,
                          float* q_lat, int B, int Hq, int Hkv, int d, int r_k, double base,
-                         cudaStream_t st, bool pdl);
+                         float scale_log2, cudaStream_t st, bool pdl);
 template <typename T>
 cudaError_t launch_simt_decode(const SimtDecodeArgs& a, cudaStream_t st);
 template <typename T>

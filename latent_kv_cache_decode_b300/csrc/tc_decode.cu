@@ -6,25 +6,34 @@
 // RoPE(q) K_raw^T against the raw window, in one softmax; values aggregate as
 // (A C_V) U_V^(g)T + A V_raw, the latent aggregate taken before the up-projection.
 //
-// Layout of the work. A "tile" is 128 key rows of one segment; a segment is all
-// rows of one kind for one batch element:
-//   latent: rows are beacons j of C_K[b] / C_V[b] (widths r_k / r_v);
-//   raw:    rows are the flattened (token, KV head) pairs t*Hkv + g of K[b] / V[b]
-//           (width d), so a 128-row tile is one contiguous 32 KB block of the cache.
-// Every query head of batch element b shares a latent tile, so one tcgen05.mma
-// with M = 128 tile rows and N = all heads (a bf16 high and low part of the query,
-// N = 2*NP) gives the tile's scores S^T in TMEM. Raw tiles use the same MMA; a
-// row of KV head g only counts for the heads of group g (block-diagonal mask,
-// applied to the scores). The softmax warps turn S^T into P (bf16 high + low
-// parts, zero outside the group) in shared memory, and a second MMA with M = 128
-// rows of the value width accumulates acc^T[value dim, head] += V_tile^T P^T in
-// TMEM, i.e. the latent aggregate A.C_V (or A.V_raw) per head.
+// Work layout. A "segment" is all key rows of one kind for one batch element:
+//   latent: the N_b beacons of C_K[b] / C_V[b] (widths r_k / r_v), shared by
+//           every query head (one latent cache per layer for all KV heads);
+//   raw:    the tokens of KV head g in K[b] / V[b] (width d), read by the G
+//           query heads of group g only; there is one raw segment per group.
+// A "tile" (unit of work) is 128 rows of a segment. A host planner gives every
+// CTA a contiguous, byte-balanced run of tiles (flash-decoding split of the
+// context); a run's part inside one segment is a "piece", which produces one
+// partial (m, l, acc) in the workspace, merged later by the combine kernel.
+//
+// Per tile, with the query operand Q = [q_hi ; q_lo] (bf16 high and low parts of
+// the float32 query, which already carries scale * log2(e)), stacked along N:
+//   scores  S^T[row, (part, head)] = tile[row, :] . Q[(part, head), :]
+//           (one tcgen05.mma per 16-wide k-step, M = 128 rows, N = 2 x heads); the
+//           softmax adds the two parts;
+//   softmax P[row, head] = exp2(S^T - m_ref[head]), split into bf16 high + low parts,
+//           again stacked along N;
+//   values  acc^T[value dim, (part, head)] += tile_V[:, value dim]^T . P (M = 128
+//           value dims); the two parts are added when the partial is written.
+// Issuing few, wide MMAs matters: the issuing thread, not the tensor core, is the
+// limit for narrow ones.
+// m_ref is a lazy running maximum: it moves (and the TMEM accumulator is rescaled)
+// only when some score exceeds it by more than 2^8, which one warp vote per tile
+// detects; so most tiles need no cross-row reduction at all.
 //
 // Roles (192 threads): warp 0 issues TMA loads into a ring of 32 KB slots, warp 1
-// issues the MMAs and owns TMEM, warps 2-5 run the online softmax (running max in
-// the log2 domain, rescaling the TMEM accumulator only when a head's max grows by
-// more than 2^8) and write one partial (m, l, acc) per (CTA, segment) to the
-// workspace. A separate kernel merges the partials and applies U_V^(g)T.
+// issues the MMAs and owns TMEM, warps 2-5 (one per TMEM lane quadrant; thread =
+// tile row) run the softmax and write the partials.
 #include <cuda.h>
 #include <string.h>
 
@@ -49,84 +58,274 @@ constexpr int kSlot = 2 * kBox;       // ring slot: 128 rows x 128 columns
 constexpr int kThreads = 192;
 constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory we may use per CTA
 constexpr int kNumKinds = 3;          // latent, raw source 0, raw source 1
+constexpr int kNG = 16;               // MMA N of a raw tile: the group's heads, padded
+constexpr float kLazy = 8.f;          // m_ref moves only when a score exceeds it by this (log2)
+constexpr int kPAtom = 128 * 32;      // bytes of one 16-head column block of P (128 rows x 32 B)
 
 struct TcParams {
-    CUtensorMap tm[2 * kNumKinds];    // per kind: keys, values
+    CUtensorMap tm[2 * kNumKinds];    // per kind: keys, values (latent 3-D, raw 4-D)
     int B, Hq, Hkv, G;
-    int rows[kNumKinds];              // key rows per batch element (0 = kind absent)
-    int tiles[kNumKinds];             // tiles per batch element
+    int rows[kNumKinds];              // rows of one segment (0 = kind absent)
+    int tiles[kNumKinds];             // tiles of one segment
+    int ngroups[kNumKinds];           // segments of this kind per batch element
     int dk[kNumKinds], dv[kNumKinds]; // key / value width
     int tiles_per_b;
-    float scale_log2;
-    const float* q_lat;               // [B, Hq, r_k]
-    const float* q_rot;               // [B, Hq, d]
+    const float* q_lat;               // [B, Hq, r_k]  (scaled)
+    const float* q_rot;               // [B, Hq, d]    (scaled)
     float* acc;                       // [slots, Hq, Dmax]
     float* ml;                        // [slots, 2, Hq]
     int* kind;                        // [slots]
     int Dmax;
     int nslot, npbuf, lookahead;
-    int q_cols;                       // columns of the query operand buffer (multiple of 64)
+    int q_cols;                       // columns of each query operand part (multiple of 64)
     uint32_t off_q, off_p, off_bar, off_red;
     uint32_t tmem_cols;
+    int vstack;                       // value accumulator keeps hi / lo parts side by side
     int u_begin[kMaxCtas + 1];        // CTA i owns units (tiles) [u_begin[i], u_begin[i+1])
     int slot_base[kMaxCtas];          // first partial slot of CTA i
 };
 
-// Position of unit u: batch element, kind and tile index inside its segment.
-struct UnitPos {
-    int b, k, t;
-};
-__device__ __forceinline__ UnitPos unit_pos(const TcParams& p, int u) {
-    UnitPos r;
-    r.b = u / p.tiles_per_b;
-    int t = u - r.b * p.tiles_per_b;
-    r.k = 0;
-    while (r.k < kNumKinds - 1 && t >= p.tiles[r.k]) {
-        t -= p.tiles[r.k];
-        ++r.k;
-    }
-    r.t = t;
-    return r;
-}
-
-// The run of this CTA's units that starts at u and stays inside one segment.
+// The run of a CTA's units that starts at u and stays inside one segment.
 struct Piece {
-    int b, k, t0, n;
+    int b, k, g, t0, n;
 };
 __device__ __forceinline__ Piece piece_at(const TcParams& p, int u, int u1) {
-    const UnitPos q = unit_pos(p, u);
     Piece r;
-    r.b = q.b;
-    r.k = q.k;
-    r.t0 = q.t;
-    r.n = min(u1 - u, p.tiles[q.k] - q.t);
+    r.b = u / p.tiles_per_b;
+    int t = u - r.b * p.tiles_per_b;
+    int k = 0;
+    for (; k < kNumKinds - 1; ++k) {
+        const int span = p.ngroups[k] * p.tiles[k];
+        if (t < span) break;
+        t -= span;
+    }
+    r.k = k;
+    r.g = t / p.tiles[k];
+    r.t0 = t - r.g * p.tiles[k];
+    r.n = min(u1 - u, p.tiles[k] - r.t0);
     return r;
 }
 
 struct TileInfo {
     int k, nK, nV;
-    uint32_t ld0;   // index of the tile's first ring load
     bool first, last;
     int seg;
 };
+
+// A tile's coordinates for the producer.
+struct TileRef {
+    int b, k, g, t;
+};
+
+// Shared state of the softmax warps.
+struct SoftCtx {
+    uint64_t* s_full;
+    uint64_t* s_empty;
+    uint64_t* p_full;
+    uint64_t* p_empty;
+    uint8_t* pbuf;
+    float* red;         // [4][NP] per-warp reductions
+    float* m_ref_s;     // [NP] reference max (log2 domain) of the current piece
+    float* alpha_s;     // [NP] rescale factors
+    volatile int* flags;  // [2][4] per-tile "needs a new reference max" votes
+    volatile int* abort;
+    uint32_t t_S, t_acc, lane_off;
+    int tid, wq, lane, myrow, npbuf, nMB;
+    int aw;             // TMEM columns per 128 value rows of the accumulator
+    bool vstack;        // accumulator holds hi and lo parts side by side
+};
+
+__device__ __forceinline__ int pbuf_index(int j, int npbuf) { return npbuf == 2 ? (j & 1) : 0; }
+__device__ __forceinline__ uint32_t pbuf_parity(int j, int npbuf) {
+    return (uint32_t)(npbuf == 2 ? (j >> 1) : j) & 1u;
+}
+
+// bf16 high part of x and the bf16 rounding of the remainder, packed in pairs.
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Softmax of tile j (rows t*128 ..) of the current piece, NS heads wide, `nvalid`
+// of them real. Reads S^T from TMEM, writes P (hi, lo) as the MN-major B operand
+// of the value MMA: 16-head column blocks of 128 rows x 32 bytes, 32-byte swizzle.
+template <int NS, int NP>
+__device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, bool valid, bool has_prev,
+                                             int nvalid, float (&l_part)[NP], float (&mref)[NP]) {
+    const int sb = j & 1;
+    ptx::mbar_wait(&c.s_full[sb], (j >> 1) & 1, c.abort);
+    ptx::tc_fence_after();
+    const uint32_t tS = c.t_S + c.lane_off + sb * (2 * NP);   // hi scores, then lo scores at +NS
+
+    // pass 1: does a score of this row exceed its head's reference by more than kLazy?
+    float dmax = -INFINITY;
+#pragma unroll
+    for (int hc = 0; hc < NS / 16; ++hc) {
+        float hi[16], lo[16];
+        ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi, lo);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (hc * 16 + i < nvalid) dmax = fmaxf(dmax, (hi[i] + lo[i]) - mref[hc * 16 + i]);
+    }
+    if (!valid) dmax = -INFINITY;
+    const bool any = __any_sync(0xffffffffu, dmax > kLazy);
+    volatile int* fl = c.flags + (j & 1) * 4;
+    if (c.lane == 0) fl[c.wq] = any ? 1 : 0;
+    ptx::named_bar(1, 128);
+    if (fl[0] | fl[1] | fl[2] | fl[3]) {
+        // new reference: the exact per-head maximum over this tile's valid rows
+#pragma unroll
+        for (int hc = 0; hc < NS / 16; ++hc) {
+            float hi[16], lo[16];
+            ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi, lo);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float x = (valid && hc * 16 + i < nvalid) ? hi[i] + lo[i] : -INFINITY;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+                if (c.lane == 0) c.red[c.wq * NP + hc * 16 + i] = x;
+            }
+        }
+        ptx::named_bar(1, 128);
+        if (c.tid < NS) {
+            const float M = fmaxf(fmaxf(c.red[c.tid], c.red[NP + c.tid]),
+                                  fmaxf(c.red[2 * NP + c.tid], c.red[3 * NP + c.tid]));
+            const float mo = c.m_ref_s[c.tid];
+            float a = 1.f;
+            if (M > mo) {
+                a = (mo == -INFINITY) ? 0.f : exp2f(mo - M);
+                c.m_ref_s[c.tid] = M;
+            }
+            c.alpha_s[c.tid] = a;
+        }
+        ptx::named_bar(1, 128);
+#pragma unroll
+        for (int h = 0; h < NS; ++h) {
+            mref[h] = c.m_ref_s[h];
+            l_part[h] *= c.alpha_s[h];
+        }
+        if (has_prev) {
+            // the accumulator holds earlier tiles of this piece: wait until their
+            // value MMAs are done, then scale each head's column(s)
+            const int jp = j - 1;
+            ptx::mbar_wait(&c.p_empty[pbuf_index(jp, c.npbuf)], pbuf_parity(jp, c.npbuf), c.abort);
+            ptx::tc_fence_after();
+            for (int cc = 0; cc < c.nMB; ++cc) {
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    if (part == 1 && !c.vstack) break;
+#pragma unroll
+                    for (int hc = 0; hc < NS / 16; ++hc) {
+                        float v[16];
+                        const uint32_t ta = c.t_acc + c.lane_off + cc * c.aw + part * NS + hc * 16;
+                        ptx::tmem_ld16(ta, v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= c.alpha_s[hc * 16 + i];
+                        ptx::tmem_st16(ta, v);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+        }
+    }
+
+    // pass 2: probabilities against the reference, as bf16 high + low parts
+    const int pb = pbuf_index(j, c.npbuf);
+    if (j >= c.npbuf) ptx::mbar_wait(&c.p_empty[pb], pbuf_parity(j, c.npbuf) ^ 1u, c.abort);
+    uint8_t* phi = c.pbuf + pb * (2 * NP * 256);
+    uint8_t* plo = phi + NS * 256;
+    const uint32_t row_off = c.myrow * 32;
+    const uint32_t sw = ((c.myrow >> 2) & 1) << 4;
+#pragma unroll
+    for (int hc = 0; hc < NS / 16; ++hc) {
+        float hi_s[16], lo_s[16];
+        ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi_s, lo_s);
+        float pr[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int h = hc * 16 + i;
+            pr[i] = (valid && h < nvalid) ? exp2f((hi_s[i] + lo_s[i]) - mref[h]) : 0.f;
+            l_part[h] += pr[i];
+        }
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) split_pair(pr[2 * i], pr[2 * i + 1], hi[i], lo[i]);
+        const uint32_t o0 = hc * kPAtom + row_off + (0u ^ sw);
+        const uint32_t o1 = hc * kPAtom + row_off + (16u ^ sw);
+        *reinterpret_cast<uint4*>(phi + o0) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(phi + o1) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+        *reinterpret_cast<uint4*>(plo + o0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(plo + o1) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(&c.s_empty[sb]);
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive(&c.p_full[pb]);
+}
+
+// End of a piece: reduce the row sums, write (m, l) and the accumulator columns of
+// the piece's real heads to partial slot `slot`.
+template <int NS, int NP>
+__device__ __forceinline__ void write_partial(const TcParams& p, const SoftCtx& c, int slot, int kind,
+                                              int h0, int nvalid, int dv, const float (&l_part)[NP]) {
+#pragma unroll
+    for (int h = 0; h < NS; ++h) {
+        float v = l_part[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (c.lane == 0) c.red[c.wq * NP + h] = v;
+    }
+    ptx::named_bar(1, 128);
+    if (c.tid < nvalid) {
+        const float L = c.red[c.tid] + c.red[NP + c.tid] + c.red[2 * NP + c.tid] + c.red[3 * NP + c.tid];
+        p.ml[((size_t)slot * 2) * p.Hq + h0 + c.tid] = c.m_ref_s[c.tid];
+        p.ml[((size_t)slot * 2 + 1) * p.Hq + h0 + c.tid] = L;
+    }
+    if (c.tid == 0) p.kind[slot] = kind;
+    for (int cc = 0; cc < c.nMB; ++cc) {
+        const int r = cc * 128 + c.myrow;
+#pragma unroll
+        for (int hc = 0; hc < NS / 16; ++hc) {
+            float v[16];
+            const uint32_t ta = c.t_acc + c.lane_off + cc * c.aw + hc * 16;
+            if (c.vstack) {
+                float w[16];
+                ptx::tmem_ld16x2(ta, ta + NS, v, w);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] += w[i];
+            } else {
+                ptx::tmem_ld16(ta, v);
+            }
+            if (r < dv) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int h = hc * 16 + i;
+                    if (h < nvalid) p.acc[((size_t)slot * p.Hq + h0 + h) * p.Dmax + r] = v[i];
+                }
+            }
+        }
+    }
+}
 
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int NQ = 2 * NP;
     uint8_t* ring = smem;
-    uint8_t* qbuf = smem + p.off_q;          // [NQ rows x q_cols] query operand (hi rows, lo rows)
-    uint8_t* pbuf = smem + p.off_p;          // [npbuf][hi, lo][NP x 128] probabilities
+    uint8_t* qbuf = smem + p.off_q;          // query operand: 2 NS rows (hi parts, lo parts)
+    uint8_t* pbuf = smem + p.off_p;          // [npbuf][hi, lo][NP/16 blocks][128 rows x 32 B]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     float* red = reinterpret_cast<float*>(smem + p.off_red);   // [4][NP]
-    float* m_run = red + 4 * NP;                               // [NP] running max (log2 domain)
-    float* alpha_s = m_run + NP;                               // [NP] rescale factors
-    // [0] abort; [1], [2] "some head rescales" for even / odd tiles (double-buffered
-    // so a slow warp still reading one tile's flag never sees the next tile's reset)
+    float* m_ref_s = red + 4 * NP;                             // [NP]
+    float* alpha_s = m_ref_s + NP;                             // [NP]
+    // [0] abort; [1..8] per-tile votes, two tiles deep (a slow warp still reading
+    // one tile's votes never sees the next tile's)
     volatile int* flag = reinterpret_cast<volatile int*>(alpha_s + NP);
-    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(alpha_s + NP) + 4;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(alpha_s + NP) + 12;
 
     uint64_t* full = bars;
     uint64_t* empty = bars + p.nslot;
@@ -160,9 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         ptx::mbar_init(acc_full, 1);
         ptx::mbar_init(acc_empty, 128);
         ptx::mbar_init(drain, 1);
-        flag[0] = 0;
-        flag[1] = 0;
-        flag[2] = 0;
+        for (int i = 0; i < 9; ++i) flag[i] = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 1) ptx::tmem_alloc(tmem_base_s, p.tmem_cols);
@@ -170,8 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_base_s;
-    const uint32_t t_S = tmem;             // 2 score buffers, NQ columns each
-    const uint32_t t_acc = tmem + 2 * NQ;  // value accumulators, NP columns per 128 value rows
+    const uint32_t t_S = tmem;             // 2 score buffers, 2*NP columns each (hi, lo)
+    const uint32_t t_acc = tmem + 4 * NP;  // value accumulators, aw columns per 128 value rows
+    const int aw = p.vstack ? 2 * NP : NP;
     volatile int* abort_flag = &flag[0];
     pdl_trigger();
 
@@ -180,31 +378,55 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         if (lane == 0) {
             for (int i = 0; i < 2 * kNumKinds; ++i)
                 if (p.rows[i >> 1] > 0) ptx::tma_prefetch_desc(&p.tm[i]);
+            // Ring loads follow the MMA issue order exactly: with lookahead that is
+            // K(0), K(1), V(0), K(2), V(1), ..., V(n-1), so a value tile arrives about
+            // when its probabilities are ready instead of idling in the ring.
             uint32_t ld = 0;
+            int slot = 0;
+            uint32_t ph = 0;
             bool ok = true;
+            auto load = [&](const TileRef& r, int part) {
+                const CUtensorMap* tm = &p.tm[2 * r.k + part];
+                const int nc = ((part ? p.dv[r.k] : p.dk[r.k]) + 127) >> 7;
+                for (int c = 0; ok && c < nc; ++c) {
+                    if (!ptx::mbar_wait(&empty[slot], ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = ring + (size_t)slot * kSlot;
+                    ptx::mbar_expect_tx(&full[slot], kSlot);
+                    if (r.k == 0) {
+                        ptx::tma_load_3d(dst, tm, c * 128, r.t * kTile, r.b, &full[slot]);
+                        ptx::tma_load_3d(dst + kBox, tm, c * 128 + 64, r.t * kTile, r.b, &full[slot]);
+                    } else {
+                        ptx::tma_load_4d(dst, tm, c * 128, r.g, r.t * kTile, r.b, &full[slot]);
+                        ptx::tma_load_4d(dst + kBox, tm, c * 128 + 64, r.g, r.t * kTile, r.b, &full[slot]);
+                    }
+                    ++ld;
+                    if (++slot == p.nslot) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
+                }
+            };
+            TileRef prev{0, 0, 0, 0};
+            bool has_prev = false;
             for (int u = u0; ok && u < u1;) {
                 const Piece pc = piece_at(p, u, u1);
-                const int nK = (p.dk[pc.k] + 127) >> 7, nV = (p.dv[pc.k] + 127) >> 7;
                 for (int t = pc.t0; ok && t < pc.t0 + pc.n; ++t) {
-                    for (int part = 0; ok && part < 2; ++part) {
-                        const CUtensorMap* tm = &p.tm[2 * pc.k + part];
-                        const int nc = part ? nV : nK;
-                        for (int c = 0; c < nc; ++c) {
-                            const int slot = ld % p.nslot;
-                            if (!ptx::mbar_wait(&empty[slot], ((ld / p.nslot) & 1) ^ 1, abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            uint8_t* dst = ring + (size_t)slot * kSlot;
-                            ptx::mbar_expect_tx(&full[slot], kSlot);
-                            ptx::tma_load_3d(dst, tm, c * 128, t * kTile, pc.b, &full[slot]);
-                            ptx::tma_load_3d(dst + kBox, tm, c * 128 + 64, t * kTile, pc.b, &full[slot]);
-                            ++ld;
-                        }
+                    const TileRef cur{pc.b, pc.k, pc.g, t};
+                    load(cur, 0);
+                    if (p.lookahead) {
+                        if (has_prev) load(prev, 1);
+                        prev = cur;
+                        has_prev = true;
+                    } else {
+                        load(cur, 1);
                     }
                 }
                 u += pc.n;
             }
+            if (ok && has_prev) load(prev, 1);
             if (!ok) {
                 // let the copies already in flight land before the CTA winds down
                 const uint32_t first = ld > (uint32_t)p.nslot ? ld - p.nslot : 0u;
@@ -217,60 +439,83 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
     } else if (warp == 1) {
         // --------------------------------------------------------------------- MMA
         if (lane == 0) {
-            const uint32_t idS = ptx::idesc_bf16(128, NQ, false, false);
-            const uint32_t idV = ptx::idesc_bf16(128, NP, true, false);
-            const uint32_t ring_a = ptx::smem_u32(ring);
-            const uint32_t q_a = ptx::smem_u32(qbuf);
-            const uint32_t p_a = ptx::smem_u32(pbuf);
+            const uint32_t idS_lat = ptx::idesc_bf16(128, 2 * NP, false, false);
+            const uint32_t idS_raw = ptx::idesc_bf16(128, 2 * kNG, false, false);
+            const int vs = p.vstack;
+            const uint32_t idV_lat = ptx::idesc_bf16(128, vs ? 2 * NP : NP, true, true);
+            const uint32_t idV_raw = ptx::idesc_bf16(128, vs ? 2 * kNG : kNG, true, true);
+            // base descriptors; a k-step or ring slot only adds (byte offset >> 4) to
+            // the start-address field, which stays below 2^14 for shared memory
+            const uint64_t dA_S = ptx::sdesc_sw128(ptx::smem_u32(ring), 16, 1024);      // K tile, K-major
+            const uint64_t dA_V = ptx::sdesc_sw128(ptx::smem_u32(ring), kBox, 1024);    // V tile, MN-major
+            const uint64_t dB_Q = ptx::sdesc_sw128(ptx::smem_u32(qbuf), 16, 1024);      // Q, K-major
+            const uint64_t dB_P = ptx::sdesc_sw32(ptx::smem_u32(pbuf), kPAtom, 256);    // P, MN-major
+            // ring cursor: the MMAs consume the ring strictly in load order
+            int sl = 0;
+            uint32_t phs = 0;
+            auto advance = [&]() {
+                if (++sl == p.nslot) {
+                    sl = 0;
+                    phs ^= 1u;
+                }
+            };
 
-            // scores: S^T[tile row, n] = sum_k K_tile[row, k] * Q[n, k]
+            // scores: S^T[tile row, (part, head)] = K_tile[row, :] . Q[(part, head), :]
             auto issue_S = [&](const TileInfo& ti, int jj) -> bool {
                 if (ti.first && !ptx::mbar_wait(q_full, ti.seg & 1, abort_flag)) return false;
                 const int sb = jj & 1;
                 if (!ptx::mbar_wait(&s_empty[sb], ((jj >> 1) & 1) ^ 1, abort_flag)) return false;
                 ptx::tc_fence_after();
+                const bool lat = ti.k == 0;
+                const uint32_t idS = lat ? idS_lat : idS_raw;
+                const uint32_t qstride = (lat ? 2 * NP : 2 * kNG) * 128 >> 4;   // 64-column chunk of Q
                 const int ksteps = p.dk[ti.k] >> 4;
+                const uint32_t dS = t_S + sb * (2 * NP);
                 for (int c = 0; c < ti.nK; ++c) {
-                    const uint32_t li = ti.ld0 + c;
-                    const int slot = li % p.nslot;
-                    if (!ptx::mbar_wait(&full[slot], (li / p.nslot) & 1, abort_flag)) return false;
+                    if (!ptx::mbar_wait(&full[sl], phs, abort_flag)) return false;
                     ptx::tc_fence_after();
-                    const int kn = min(8, ksteps - c * 8);
-                    for (int kk = 0; kk < kn; ++kk) {
-                        const uint32_t a = ring_a + slot * kSlot + (kk >> 2) * kBox + (kk & 3) * 32;
-                        const int kg = c * 8 + kk;
-                        const uint32_t bq = q_a + (kg >> 2) * (NQ * 128) + (kg & 3) * 32;
-                        ptx::mma_bf16(t_S + sb * NQ, ptx::sdesc_sw128(a, 16, 1024),
-                                      ptx::sdesc_sw128(bq, 16, 1024), idS, (c | kk) != 0 ? 1u : 0u);
+                    const uint64_t a0 = dA_S + (uint64_t)((sl * kSlot) >> 4);
+                    const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        if (c * 8 + kk < ksteps)
+                            ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
+                                          b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS,
+                                          (c | kk) != 0 ? 1u : 0u);
                     }
-                    ptx::mma_commit(&empty[slot]);
+                    ptx::mma_commit(&empty[sl]);
+                    advance();
                 }
                 ptx::mma_commit(&s_full[sb]);
                 if (ti.last) ptx::mma_commit(q_empty);
                 return true;
             };
-            // values: acc^T[value row, n] += V_tile[:, value row]^T . P^T  (hi and lo parts of P)
+            // values: acc^T[value row, (part, head)] += V_tile[:, value row]^T . P
             auto issue_V = [&](const TileInfo& ti, int jj) -> bool {
-                const int pb = jj % p.npbuf;
-                if (!ptx::mbar_wait(&p_full[pb], (jj / p.npbuf) & 1, abort_flag)) return false;
+                const int pb = pbuf_index(jj, p.npbuf);
+                if (!ptx::mbar_wait(&p_full[pb], pbuf_parity(jj, p.npbuf), abort_flag)) return false;
                 if (ti.first && ti.seg > 0 && !ptx::mbar_wait(acc_empty, (ti.seg - 1) & 1, abort_flag))
                     return false;
                 ptx::tc_fence_after();
-                const uint32_t phi = p_a + pb * (2 * NP * 256);
-                const uint32_t plo = phi + NP * 256;
+                const bool lat = ti.k == 0;
+                const uint32_t idV = lat ? idV_lat : idV_raw;
+                const uint32_t lo_off = (lat ? NP : kNG) * 256 >> 4;   // lo part of P
+                const uint64_t pd = dB_P + (uint64_t)((pb * (2 * NP * 256)) >> 4);
                 for (int c = 0; c < ti.nV; ++c) {
-                    const uint32_t li = ti.ld0 + ti.nK + c;
-                    const int slot = li % p.nslot;
-                    if (!ptx::mbar_wait(&full[slot], (li / p.nslot) & 1, abort_flag)) return false;
+                    if (!ptx::mbar_wait(&full[sl], phs, abort_flag)) return false;
                     ptx::tc_fence_after();
+                    const uint64_t vd = dA_V + (uint64_t)((sl * kSlot) >> 4);
+                    const uint32_t dacc = t_acc + c * aw;
+#pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ad = ptx::sdesc_sw128(ring_a + slot * kSlot + kk * 2048, kBox, 1024);
-                        const uint32_t boff = (kk >> 2) * (NP * 128) + (kk & 3) * 32;
                         const uint32_t accum = (ti.first && kk == 0) ? 0u : 1u;
-                        ptx::mma_bf16(t_acc + c * NP, ad, ptx::sdesc_sw128(phi + boff, 16, 1024), idV, accum);
-                        ptx::mma_bf16(t_acc + c * NP, ad, ptx::sdesc_sw128(plo + boff, 16, 1024), idV, 1u);
+                        const uint64_t a = vd + (uint64_t)(kk * (2048 >> 4));
+                        const uint64_t b = pd + (uint64_t)(kk * (512 >> 4));
+                        ptx::mma_bf16(dacc, a, b, idV, accum);
+                        if (!vs) ptx::mma_bf16(dacc, a, b + lo_off, idV, 1u);
                     }
-                    ptx::mma_commit(&empty[slot]);
+                    ptx::mma_commit(&empty[sl]);
+                    advance();
                 }
                 ptx::mma_commit(&p_empty[pb]);
                 if (ti.last) ptx::mma_commit(acc_full);
@@ -279,7 +524,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
 
             bool ok = true;
             int jS = 0, jV = 0, seg = 0;
-            uint32_t ld = 0;
             TileInfo pend;
             bool has_pend = false;
             for (int u = u0; ok && u < u1; ++seg) {
@@ -289,11 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                     ti.k = pc.k;
                     ti.nK = (p.dk[pc.k] + 127) >> 7;
                     ti.nV = (p.dv[pc.k] + 127) >> 7;
-                    ti.ld0 = ld;
                     ti.first = (t == pc.t0);
                     ti.last = (t == pc.t0 + pc.n - 1);
                     ti.seg = seg;
-                    ld += ti.nK + ti.nV;
                     ok = issue_S(ti, jS++);
                     if (ok && has_pend) {
                         ok = issue_V(pend, jV++);
@@ -315,50 +557,74 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         }
     } else {
         // ----------------------------------------------------------------- softmax
-        const int tid = threadIdx.x - 64;   // 0..127
-        const int q4 = warp & 3;            // TMEM lane quadrant this warp may access
-        const int myrow = q4 * 32 + lane;   // tile row (S) / value row (acc) of this thread
-        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        SoftCtx c;
+        c.s_full = s_full;
+        c.s_empty = s_empty;
+        c.p_full = p_full;
+        c.p_empty = p_empty;
+        c.pbuf = pbuf;
+        c.red = red;
+        c.m_ref_s = m_ref_s;
+        c.alpha_s = alpha_s;
+        c.flags = flag + 1;
+        c.abort = abort_flag;
+        c.tid = threadIdx.x - 64;            // 0..127
+        c.wq = c.tid >> 5;                   // softmax warp 0..3
+        c.lane = lane;
+        const int q4 = warp & 3;             // TMEM lane quadrant this warp may access
+        c.myrow = q4 * 32 + lane;            // tile row (S) / value row (acc) of this thread
+        c.lane_off = (uint32_t)(q4 * 32) << 16;
+        c.t_S = t_S;
+        c.t_acc = t_acc;
+        c.npbuf = p.npbuf;
+        c.aw = aw;
+        c.vstack = p.vstack != 0;
         const int G = p.G;
-        float l_part[NP];
+        float l_part[NP], mref[NP];
 
-        pdl_wait();   // q_lat / q_rot are written by the preceding kernel
+        pdl_wait();   // q_lat / q_rot come from the preceding kernel
 
-        // bf16 high / low parts of the query operand of segment (b, k)
-        auto write_q = [&](int b, int k) {
+        // bf16 high / low parts of the query operand of segment (b, k, g): NS rows
+        auto write_q = [&](int b, int k, int g) {
             const int dk = p.dk[k];
-            const float* src = (k == 0 ? p.q_lat : p.q_rot) + (size_t)b * p.Hq * dk;
-            const int units = dk >> 3;
-            for (int task = tid; task < NP * units; task += 128) {
-                const int h = task / units, u = task - h * units;
-                float v[8];
-                if (h < p.Hq) {
-                    const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)h * dk + u * 8);
-                    const float4 a = s4[0], c = s4[1];
-                    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-                    v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
-                } else {
+            const int NS = k == 0 ? NP : kNG;   // rows [0, NS) hi parts, [NS, 2 NS) lo parts
+            const int nvalid = k == 0 ? p.Hq : G;
+            const float* src = k == 0 ? p.q_lat + (size_t)b * p.Hq * dk
+                                      : p.q_rot + ((size_t)b * p.Hq + (size_t)g * G) * dk;
+            const int units = dk >> 3, total = NS * units;
+            // batches of 8 units per thread: all loads of a batch are in flight together
+            for (int base = c.tid; base < total; base += 128 * 8) {
+                float4 va[8], vb[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+                for (int q = 0; q < 8; ++q) {
+                    const int task = base + q * 128;
+                    const int h = task / units, u = task - h * units;
+                    va[q] = vb[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (task < total && h < nvalid) {
+                        const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)h * dk + u * 8);
+                        va[q] = s4[0];
+                        vb[q] = s4[1];
+                    }
                 }
-                uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]);
-                    const __nv_bfloat16 h1 = __float2bfloat16_rn(v[2 * i + 1]);
-                    const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * i] - __bfloat162float(h0));
-                    const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * i + 1] - __bfloat162float(h1));
-                    hi[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-                    lo[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                for (int q = 0; q < 8; ++q) {
+                    const int task = base + q * 128;
+                    if (task >= total) break;
+                    const int h = task / units, u = task - h * units;
+                    uint32_t hi[4], lo[4];
+                    split_pair(va[q].x, va[q].y, hi[0], lo[0]);
+                    split_pair(va[q].z, va[q].w, hi[1], lo[1]);
+                    split_pair(vb[q].x, vb[q].y, hi[2], lo[2]);
+                    split_pair(vb[q].z, vb[q].w, hi[3], lo[3]);
+                    *reinterpret_cast<uint4*>(qbuf + ptx::sw128_offset(h, u * 8, 2 * NS)) =
+                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(qbuf + ptx::sw128_offset(NS + h, u * 8, 2 * NS)) =
+                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
-                *reinterpret_cast<uint4*>(qbuf + ptx::sw128_offset(h, u * 8, NQ)) =
-                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(qbuf + ptx::sw128_offset(NP + h, u * 8, NQ)) =
-                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
             ptx::fence_proxy_async_smem();
             ptx::named_bar(1, 128);
-            if (tid == 0) ptx::mbar_arrive(q_full);
+            if (c.tid == 0) ptx::mbar_arrive(q_full);
         };
 
         // A failed wait (abort) does not leave the loop: every softmax thread keeps
@@ -366,149 +632,40 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         // poisoned at the end instead.
         if (u0 < u1) {
             const Piece p0 = piece_at(p, u0, u1);
-            write_q(p0.b, p0.k);
+            write_q(p0.b, p0.k, p0.g);
         }
         int j = 0, seg = 0;
         for (int u = u0; u < u1; ++seg) {
             const Piece pc = piece_at(p, u, u1);
             const int k = pc.k;
-            const int nMB = (p.dv[k] + 127) >> 7;
-            if (tid < NP) m_run[tid] = -INFINITY;
+            const bool lat = (k == 0);
+            const int nvalid = lat ? p.Hq : G;
+            c.nMB = (p.dv[k] + 127) >> 7;
+            if (c.tid < NP) m_ref_s[c.tid] = -INFINITY;
 #pragma unroll
-            for (int h = 0; h < NP; ++h) l_part[h] = 0.f;
+            for (int h = 0; h < NP; ++h) {
+                l_part[h] = 0.f;
+                mref[h] = -INFINITY;
+            }
             ptx::named_bar(1, 128);
             for (int t = pc.t0; t < pc.t0 + pc.n; ++t, ++j) {
-                const int sb = j & 1;
-                ptx::mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag);
-                ptx::tc_fence_after();
-                float s[NP];
-#pragma unroll
-                for (int hc = 0; hc < NP / 16; ++hc) {
-                    float hi[16], lo[16];
-                    ptx::tmem_ld16x2(t_S + lane_off + sb * NQ + hc * 16,
-                                     t_S + lane_off + sb * NQ + NP + hc * 16, hi, lo);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) s[hc * 16 + i] = (hi[i] + lo[i]) * p.scale_log2;
-                }
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(&s_empty[sb]);
-                // mask rows past the segment end, padding heads and, for raw rows,
-                // the heads of other KV groups
-                const int row = t * kTile + myrow;
-                const bool valid = row < p.rows[k];
-                const int g = (k == 0) ? -1 : row % p.Hkv;
-#pragma unroll
-                for (int h = 0; h < NP; ++h) {
-                    const bool keep = valid && h < p.Hq && (g < 0 || h / G == g);
-                    if (!keep) s[h] = -INFINITY;
-                }
-                // per-head maximum over the tile's 128 rows
-#pragma unroll
-                for (int h = 0; h < NP; ++h) {
-                    float v = s[h];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                    if (lane == 0) red[q4 * NP + h] = v;
-                }
-                volatile int* resc = &flag[1 + (j & 1)];
-                if (tid == 0) *resc = 0;
-                ptx::named_bar(1, 128);
-                if (tid < NP) {
-                    const float M = fmaxf(fmaxf(red[tid], red[NP + tid]), fmaxf(red[2 * NP + tid], red[3 * NP + tid]));
-                    const float mo = m_run[tid];
-                    float a = 1.f;
-                    // lazy rescale: keep the reference max unless it grew by more than 8 (x256)
-                    if (M > mo + 8.f) {
-                        a = (mo == -INFINITY) ? 0.f : exp2f(mo - M);
-                        m_run[tid] = M;
-                        *resc = 1;
-                    }
-                    alpha_s[tid] = a;
-                }
-                ptx::named_bar(1, 128);
-                if (*resc) {
-#pragma unroll
-                    for (int h = 0; h < NP; ++h) l_part[h] *= alpha_s[h];
-                    if (t > pc.t0) {
-                        // the accumulator holds earlier tiles of this piece: wait for
-                        // their value MMAs, then scale each head's column
-                        const int jp = j - 1;
-                        ptx::mbar_wait(&p_empty[jp % p.npbuf], (jp / p.npbuf) & 1, abort_flag);
-                        ptx::tc_fence_after();
-                        for (int c = 0; c < nMB; ++c) {
-#pragma unroll
-                            for (int hc = 0; hc < NP / 16; ++hc) {
-                                float v[16];
-                                const uint32_t ta = t_acc + lane_off + c * NP + hc * 16;
-                                ptx::tmem_ld16(ta, v);
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) v[i] *= alpha_s[hc * 16 + i];
-                                ptx::tmem_st16(ta, v);
-                            }
-                        }
-                        ptx::tc_fence_before();
-                    }
-                }
-                // probabilities against the reference max, as bf16 high + low parts
-                const int pb = j % p.npbuf;
-                if (j >= p.npbuf) ptx::mbar_wait(&p_empty[pb], ((j / p.npbuf) - 1) & 1, abort_flag);
-                uint8_t* phi = pbuf + pb * (2 * NP * 256);
-                uint8_t* plo = phi + NP * 256;
-#pragma unroll
-                for (int h = 0; h < NP; ++h) {
-                    const float pr = (s[h] == -INFINITY) ? 0.f : exp2f(s[h] - m_run[h]);
-                    l_part[h] += pr;
-                    const __nv_bfloat16 ph = __float2bfloat16_rn(pr);
-                    const __nv_bfloat16 pl = __float2bfloat16_rn(pr - __bfloat162float(ph));
-                    const uint32_t off = ptx::sw128_offset(h, myrow, NP);
-                    *reinterpret_cast<__nv_bfloat16*>(phi + off) = ph;
-                    *reinterpret_cast<__nv_bfloat16*>(plo + off) = pl;
-                }
-                ptx::fence_proxy_async_smem();
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(&p_full[pb]);
+                const bool valid = t * kTile + c.myrow < p.rows[k];
+                if (lat) softmax_tile<NP, NP>(c, j, valid, t > pc.t0, nvalid, l_part, mref);
+                else softmax_tile<kNG, NP>(c, j, valid, t > pc.t0, nvalid, l_part, mref);
             }
             // the next piece's query operand goes in before this piece's partial is
             // written, so its score MMAs overlap the write-out
             if (u + pc.n < u1) {
                 ptx::mbar_wait(q_empty, seg & 1, abort_flag);
                 const Piece nx = piece_at(p, u + pc.n, u1);
-                write_q(nx.b, nx.k);
+                write_q(nx.b, nx.k, nx.g);
             }
-            // ---- partial of (CTA, piece): running max, sum and accumulator
+            // ---- partial of (CTA, piece): reference max, row sum and accumulator
             ptx::mbar_wait(acc_full, seg & 1, abort_flag);
             ptx::tc_fence_after();
-#pragma unroll
-            for (int h = 0; h < NP; ++h) {
-                float v = l_part[h];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) red[q4 * NP + h] = v;
-            }
-            ptx::named_bar(1, 128);
             const int slot = p.slot_base[cta] + seg;
-            if (tid < p.Hq) {
-                const float L = red[tid] + red[NP + tid] + red[2 * NP + tid] + red[3 * NP + tid];
-                p.ml[((size_t)slot * 2) * p.Hq + tid] = m_run[tid];
-                p.ml[((size_t)slot * 2 + 1) * p.Hq + tid] = L;
-            }
-            if (tid == 0) p.kind[slot] = (k == 0) ? 0 : 1;
-            const int dv = p.dv[k];
-            for (int c = 0; c < nMB; ++c) {
-                const int r = c * 128 + myrow;
-#pragma unroll
-                for (int hc = 0; hc < NP / 16; ++hc) {
-                    float v[16];
-                    ptx::tmem_ld16(t_acc + lane_off + c * NP + hc * 16, v);
-                    if (r < dv) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int h = hc * 16 + i;
-                            if (h < p.Hq) p.acc[((size_t)slot * p.Hq + h) * p.Dmax + r] = v[i];
-                        }
-                    }
-                }
-            }
+            if (lat) write_partial<NP, NP>(p, c, slot, kSlotLatent, 0, nvalid, p.dv[k], l_part);
+            else write_partial<kNG, NP>(p, c, slot, kSlotRawGroup + pc.g, pc.g * G, nvalid, p.dv[k], l_part);
             ptx::tc_fence_before();
             ptx::mbar_arrive(acc_empty);
             ptx::named_bar(1, 128);
@@ -548,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
 
 // Shared-memory plan of one launch.
 struct SmemPlan {
-    int NP, nslot, npbuf, lookahead, q_cols;
+    int NP, nslot, npbuf, lookahead, q_cols, vstack;
     uint32_t off_q, off_p, off_bar, off_red, total, tmem_cols;
     bool ok;
 };
@@ -558,7 +715,6 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], const int rows[kNumKinds]) {
     SmemPlan s{};
     s.NP = round_up(Hq, 16);
-    const int NQ = 2 * s.NP;
     int qc = 0, nmb = 0, need = 0;
     for (int k = 0; k < kNumKinds; ++k) {
         if (rows[k] <= 0) continue;
@@ -567,16 +723,20 @@ SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], con
         need = std::max(need, (dk[k] + 127) / 128 + (dv[k] + 127) / 128);
     }
     s.q_cols = round_up(qc, 64);
-    const int q_bytes = NQ * s.q_cols * 2;
-    const int tmem = 2 * NQ + nmb * s.NP;
+    const int q_bytes = 2 * s.NP * s.q_cols * 2;   // hi and lo parts
+    // TMEM: two score buffers of 2*NP columns, then the accumulator; hi / lo parts of
+    // the accumulator side by side when they fit, else summed in place
+    s.vstack = (4 * s.NP + nmb * 2 * s.NP) <= 512 ? 1 : 0;
+    const int tmem = 4 * s.NP + nmb * (s.vstack ? 2 : 1) * s.NP;
     s.tmem_cols = 32;
     while ((int)s.tmem_cols < tmem) s.tmem_cols *= 2;
     s.ok = false;
     if (s.NP > 64 || s.tmem_cols > 512) return s;
+    const int misc_bytes = (6 * s.NP + 16) * 4;
     for (s.npbuf = 2; s.npbuf >= 1; --s.npbuf) {
         const int p_bytes = s.npbuf * 2 * s.NP * 256;
         const int nbars = 2 * 16 + 13;   // up to 16 ring slots
-        const int misc = nbars * 8 + (6 * s.NP + 16) * 4 + 1024;   // + alignment slack
+        const int misc = nbars * 8 + misc_bytes + 1024;   // + alignment slack
         const int avail = kSmemMax - q_bytes - p_bytes - misc;
         s.nslot = std::min(16, avail / kSlot);
         if (s.nslot >= 2) break;
@@ -587,7 +747,7 @@ SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], con
     s.off_p = s.off_q + q_bytes;
     s.off_bar = s.off_p + s.npbuf * 2 * s.NP * 256;
     s.off_red = s.off_bar + round_up((2 * s.nslot + 13) * 8, 16);
-    s.total = s.off_red + (6 * s.NP + 16) * 4 + 1024;
+    s.total = s.off_red + misc_bytes + 1024;
     s.ok = s.total <= (uint32_t)kSmemMax;
     return s;
 }
@@ -610,9 +770,9 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 3-D bf16 tensor [B][rows][cols] (cols contiguous) read in boxes of 128 rows x 64
-// columns with the 128-byte swizzle; rows/columns past the end read as zero.
-bool make_map(CUtensorMap* tm, const void* base, int cols, int rows, int B) {
+// Latent operand: 3-D bf16 tensor [B][rows][cols] (cols contiguous) read in boxes of
+// 128 rows x 64 columns with the 128-byte swizzle; rows/columns past the end read as zero.
+bool make_map_latent(CUtensorMap* tm, const void* base, int cols, int rows, int B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)B};
@@ -624,6 +784,20 @@ bool make_map(CUtensorMap* tm, const void* base, int cols, int rows, int B) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Raw operand: 4-D bf16 tensor [B][T][Hkv][d] read per KV head in boxes of 128
+// tokens x 64 columns (one head), 128-byte swizzle; tokens past the end read as zero.
+bool make_map_raw(CUtensorMap* tm, const void* base, int d, int Hkv, int T, int B) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * d * 2, (cuuint64_t)T * Hkv * d * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
@@ -631,47 +805,49 @@ int sm_count() {
     return n > 0 ? n : 148;
 }
 
-// Work plan: contiguous unit ranges per CTA with balanced bytes, partial slots per
-// (CTA, segment piece) and per batch element.
+// Work plan: contiguous unit ranges per CTA with balanced cost, one partial slot
+// per (CTA, segment piece), and the slot range of every batch element.
 struct WorkPlan {
     int n_ctas = 0;
     std::vector<int> u_begin, slot_base, batch_slot;
     int slots = 0;
 };
 
-WorkPlan make_plan(int B, const int tiles[kNumKinds], const int cost[kNumKinds], int max_ctas) {
-    // runs of equal-cost units in unit order (batch-major, then kind)
-    std::vector<std::pair<int, int>> runs;   // (count, cost)
-    int64_t total = 0;
+// Segments of one batch element in unit order: (tiles, cost per tile).
+struct SegList {
+    std::vector<std::pair<int, int>> segs;
+};
+
+WorkPlan make_plan(int B, const SegList& sl, int max_ctas) {
+    // runs of equal-cost units in unit order (batch-major, then segment)
+    int64_t total = 0, units = 0;
     int cmax = 1;
     for (int b = 0; b < B; ++b)
-        for (int k = 0; k < kNumKinds; ++k)
-            if (tiles[k] > 0) {
-                runs.push_back({tiles[k], cost[k]});
-                total += (int64_t)tiles[k] * cost[k];
-                cmax = std::max(cmax, cost[k]);
-            }
-    int64_t units = 0;
-    for (auto& r : runs) units += r.first;
+        for (auto& r : sl.segs) {
+            total += (int64_t)r.first * r.second;
+            units += r.first;
+            cmax = std::max(cmax, r.second);
+        }
     const int G = (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, units));
     // number of CTAs greedy packing needs with per-CTA budget T
     auto count = [&](int64_t T) {
         int ctas = 1;
         int64_t cur = 0;
-        for (auto& r : runs) {
-            int n = r.first;
-            while (n > 0) {
-                int64_t room = (T - cur) / r.second;
-                if (room == 0) {
-                    ++ctas;
-                    cur = 0;
-                    room = T / r.second;
+        for (int b = 0; b < B; ++b)
+            for (auto& r : sl.segs) {
+                int n = r.first;
+                while (n > 0) {
+                    int64_t room = (T - cur) / r.second;
+                    if (room == 0) {
+                        ++ctas;
+                        cur = 0;
+                        room = T / r.second;
+                    }
+                    const int take = (int)std::min<int64_t>(n, room);
+                    cur += (int64_t)take * r.second;
+                    n -= take;
                 }
-                const int take = (int)std::min<int64_t>(n, room);
-                cur += (int64_t)take * r.second;
-                n -= take;
             }
-        }
         return ctas;
     };
     int64_t lo = std::max<int64_t>(cmax, (total + G - 1) / G), hi = std::max<int64_t>(lo, total);
@@ -683,68 +859,64 @@ WorkPlan make_plan(int B, const int tiles[kNumKinds], const int cost[kNumKinds],
     const int64_t T = lo;
     WorkPlan w;
     w.u_begin.push_back(0);
+    // pieces: a CTA boundary or a segment boundary starts a new one
+    std::vector<int> piece_cta;   // CTA of each piece, in unit order
+    std::vector<int> piece_b;
     int64_t cur = 0, u = 0;
-    for (auto& r : runs) {
-        int n = r.first;
-        while (n > 0) {
-            int64_t room = (T - cur) / r.second;
-            if (room == 0) {
-                w.u_begin.push_back((int)u);
-                cur = 0;
-                room = T / r.second;
+    bool fresh = true;
+    for (int b = 0; b < B; ++b)
+        for (auto& r : sl.segs) {
+            int n = r.first;
+            fresh = true;
+            while (n > 0) {
+                int64_t room = (T - cur) / r.second;
+                if (room == 0) {
+                    w.u_begin.push_back((int)u);
+                    cur = 0;
+                    room = T / r.second;
+                    fresh = true;
+                }
+                const int take = (int)std::min<int64_t>(n, room);
+                if (fresh) {
+                    piece_cta.push_back((int)w.u_begin.size() - 1);
+                    piece_b.push_back(b);
+                    fresh = false;
+                }
+                cur += (int64_t)take * r.second;
+                u += take;
+                n -= take;
             }
-            const int take = (int)std::min<int64_t>(n, room);
-            cur += (int64_t)take * r.second;
-            u += take;
-            n -= take;
         }
-    }
     w.u_begin.push_back((int)u);
     w.n_ctas = (int)w.u_begin.size() - 1;
-    // partial slots: one per (CTA, segment piece), consecutive; batch b owns a
+    // slots in piece order: CTA i's pieces are consecutive, and batch b owns a
     // contiguous slot range because units are batch-major
-    int tiles_per_b = 0;
-    for (int k = 0; k < kNumKinds; ++k) tiles_per_b += tiles[k];
+    w.slot_base.assign(w.n_ctas, -1);
     w.batch_slot.assign(B + 1, -1);
-    int slot = 0;
-    for (int i = 0; i < w.n_ctas; ++i) {
-        w.slot_base.push_back(slot);
-        int uu = w.u_begin[i];
-        while (uu < w.u_begin[i + 1]) {
-            const int b = uu / tiles_per_b;
-            int t = uu - b * tiles_per_b, k = 0;
-            while (k < kNumKinds - 1 && t >= tiles[k]) {
-                t -= tiles[k];
-                ++k;
-            }
-            const int n = std::min(w.u_begin[i + 1] - uu, tiles[k] - t);
-            if (w.batch_slot[b] < 0) w.batch_slot[b] = slot;
-            ++slot;
-            uu += n;
-        }
+    for (int s = 0; s < (int)piece_cta.size(); ++s) {
+        if (w.slot_base[piece_cta[s]] < 0) w.slot_base[piece_cta[s]] = s;
+        if (w.batch_slot[piece_b[s]] < 0) w.batch_slot[piece_b[s]] = s;
     }
-    w.batch_slot[B] = slot;
-    w.slots = slot;
+    w.batch_slot[B] = (int)piece_cta.size();
+    w.slots = (int)piece_cta.size();
     return w;
 }
 
 struct PlanKey {
-    int B, tiles[kNumKinds], cost[kNumKinds], max_ctas;
-    bool operator<(const PlanKey& o) const {
-        return std::tie(B, tiles[0], tiles[1], tiles[2], cost[0], cost[1], cost[2], max_ctas) <
-               std::tie(o.B, o.tiles[0], o.tiles[1], o.tiles[2], o.cost[0], o.cost[1], o.cost[2], o.max_ctas);
-    }
+    int B, max_ctas;
+    std::vector<std::pair<int, int>> segs;
+    bool operator<(const PlanKey& o) const { return std::tie(B, max_ctas, segs) < std::tie(o.B, o.max_ctas, o.segs); }
 };
 
-const WorkPlan& cached_plan(int B, const int tiles[kNumKinds], const int cost[kNumKinds], int max_ctas) {
+const WorkPlan& cached_plan(int B, const SegList& sl, int max_ctas) {
     static std::mutex mu;
     static std::map<PlanKey, WorkPlan> cache;
-    PlanKey key{B, {tiles[0], tiles[1], tiles[2]}, {cost[0], cost[1], cost[2]}, max_ctas};
+    PlanKey key{B, max_ctas, sl.segs};
     std::lock_guard<std::mutex> g(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     if (cache.size() > 256) cache.clear();
-    return cache.emplace(key, make_plan(B, tiles, cost, max_ctas)).first->second;
+    return cache.emplace(key, make_plan(B, sl, max_ctas)).first->second;
 }
 
 template <int NP>
@@ -769,9 +941,10 @@ cudaError_t launch_decode(const TcParams& prm, int grid, uint32_t smem, cudaStre
     return cudaLaunchKernelEx(&cfg, tc_decode_kernel<NP>, prm);
 }
 
-// Kinds of key rows of one call: rows / widths per batch element and operands.
+// Kinds of key rows of one call: rows / widths per segment and operands.
 struct Kinds {
     int rows[kNumKinds] = {0, 0, 0};
+    int ngroups[kNumKinds] = {0, 0, 0};
     int dk[kNumKinds] = {0, 0, 0};
     int dv[kNumKinds] = {0, 0, 0};
     const void* K[kNumKinds] = {nullptr, nullptr, nullptr};
@@ -780,42 +953,37 @@ struct Kinds {
 
 Kinds kinds_of(const TcCall& c) {
     Kinds s;
+    auto raw = [&](int k, int T, const void* K, const void* V) {
+        if (T <= 0) return;
+        s.rows[k] = T;
+        s.ngroups[k] = c.Hkv;
+        s.dk[k] = s.dv[k] = c.d;
+        s.K[k] = K;
+        s.V[k] = V;
+    };
     if (c.which == SLIMKV_LATENT) {
         if (c.N_b > 0) {
             s.rows[0] = c.N_b;
+            s.ngroups[0] = 1;
             s.dk[0] = c.r_k;
             s.dv[0] = c.r_v;
             s.K[0] = c.C_K;
             s.V[0] = c.C_V;
         }
-        if (c.W > 0) {
-            s.rows[1] = c.W * c.Hkv;
-            s.K[1] = c.K_raw;
-            s.V[1] = c.V_raw;
-        }
+        raw(1, c.W, c.K_raw, c.V_raw);
     } else if (c.which == SLIMKV_RECONSTRUCT) {
-        s.rows[1] = c.N_b * c.Hkv;
-        s.K[1] = c.kb;
-        s.V[1] = c.vb;
-        if (c.W > 0) {
-            s.rows[2] = c.W * c.Hkv;
-            s.K[2] = c.K_raw;
-            s.V[2] = c.V_raw;
-        }
+        raw(1, c.N_b, c.kb, c.vb);
+        raw(2, c.W, c.K_raw, c.V_raw);
     } else {
-        s.rows[1] = c.W * c.Hkv;
-        s.K[1] = c.K_raw;
-        s.V[1] = c.V_raw;
+        raw(1, c.W, c.K_raw, c.V_raw);
     }
-    for (int k = 1; k < kNumKinds; ++k)
-        if (s.rows[k] > 0) s.dk[k] = s.dv[k] = c.d;
     return s;
 }
 
 }  // namespace
 
 bool tc_supported(int Hq, int Hkv, int d, int N_b, int r_k, int r_v) {
-    if (d != 128 || Hq > 64 || Hkv > 128) return false;
+    if (d != 128 || Hq > 64 || Hkv > 128 || Hq / Hkv > kNG) return false;
     int rows[kNumKinds] = {N_b, 1, 1}, dk[kNumKinds] = {r_k, d, d}, dv[kNumKinds] = {r_v, d, d};
     if (N_b <= 0) rows[0] = 0;
     return plan_smem(Hq, dk, dv, rows).ok;
@@ -825,8 +993,8 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     typedef __nv_bfloat16 bf16;
     const bool lat = c.which == SLIMKV_LATENT && c.N_b > 0;
     cudaError_t e = launch_qproj<bf16>((const bf16*)c.q, lat ? (const bf16*)c.U_K : nullptr, c.q_pos, c.q_rot,
-                                       lat ? c.q_lat : nullptr, c.B, c.Hq, c.Hkv, c.d, c.r_k, c.rope_base, st,
-                                       true);
+                                       lat ? c.q_lat : nullptr, c.B, c.Hq, c.Hkv, c.d, c.r_k, c.rope_base,
+                                       c.scale_log2, st, true);
     if (e != cudaSuccess) return e;
     if (c.which == SLIMKV_RECONSTRUCT) {
         // plain launches (no early trigger): the decode below reads K_b / V_b
@@ -843,29 +1011,34 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
 
     TcParams prm;   // copied into the launch's parameter space
     memset(&prm, 0, sizeof(prm));
-    int tiles[kNumKinds], cost[kNumKinds];
+    SegList sl;
     prm.tiles_per_b = 0;
     for (int k = 0; k < kNumKinds; ++k) {
         prm.rows[k] = s.rows[k];
+        prm.ngroups[k] = s.ngroups[k];
         prm.dk[k] = s.dk[k];
         prm.dv[k] = s.dv[k];
-        tiles[k] = s.rows[k] > 0 ? (s.rows[k] + kTile - 1) / kTile : 0;
-        prm.tiles[k] = tiles[k];
-        prm.tiles_per_b += tiles[k];
+        const int tiles = s.rows[k] > 0 ? (s.rows[k] + kTile - 1) / kTile : 0;
+        prm.tiles[k] = tiles;
+        prm.tiles_per_b += tiles * s.ngroups[k];
         // cost of a tile: the 32 KB slots it streams (+1 for its fixed per-tile work)
-        cost[k] = (s.dk[k] + 127) / 128 + (s.dv[k] + 127) / 128 + 1;
+        const int cost = (s.dk[k] + 127) / 128 + (s.dv[k] + 127) / 128 + 1;
+        for (int g = 0; g < s.ngroups[k]; ++g) sl.segs.push_back({tiles, cost});
         if (s.rows[k] > 0) {
-            if (!make_map(&prm.tm[2 * k], s.K[k], s.dk[k], s.rows[k], c.B)) return cudaErrorInvalidValue;
-            if (!make_map(&prm.tm[2 * k + 1], s.V[k], s.dv[k], s.rows[k], c.B)) return cudaErrorInvalidValue;
+            const bool ok = k == 0
+                                ? make_map_latent(&prm.tm[0], s.K[0], s.dk[0], s.rows[0], c.B) &&
+                                      make_map_latent(&prm.tm[1], s.V[0], s.dv[0], s.rows[0], c.B)
+                                : make_map_raw(&prm.tm[2 * k], s.K[k], c.d, c.Hkv, s.rows[k], c.B) &&
+                                      make_map_raw(&prm.tm[2 * k + 1], s.V[k], c.d, c.Hkv, s.rows[k], c.B);
+            if (!ok) return cudaErrorInvalidValue;
         }
     }
-    const WorkPlan& w = cached_plan(c.B, tiles, cost, std::min(kMaxCtas, sm_count()));
+    const WorkPlan& w = cached_plan(c.B, sl, std::min(kMaxCtas, sm_count()));
     if (w.slots > c.slots) return cudaErrorInvalidValue;
     prm.B = c.B;
     prm.Hq = c.Hq;
     prm.Hkv = c.Hkv;
     prm.G = c.Hq / c.Hkv;
-    prm.scale_log2 = c.scale_log2;
     prm.q_lat = c.q_lat;
     prm.q_rot = c.q_rot;
     prm.acc = c.acc;
@@ -881,6 +1054,7 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     prm.off_bar = sp.off_bar;
     prm.off_red = sp.off_red;
     prm.tmem_cols = sp.tmem_cols;
+    prm.vstack = sp.vstack;
     for (int i = 0; i <= w.n_ctas; ++i) prm.u_begin[i] = w.u_begin[i];
     for (int i = 0; i < w.n_ctas; ++i) prm.slot_base[i] = w.slot_base[i];
 
