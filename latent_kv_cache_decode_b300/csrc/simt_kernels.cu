@@ -12,6 +12,7 @@
 #include <algorithm>
 
 #include "slimkv_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace slimkv {
 
@@ -169,12 +170,37 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
     // the previous call's kernels may still read this workspace; every CTA waits
     // (so this grid completes only after its predecessor) before writing it
     pdl_wait();
-    if (cb == 0) {
+    if (cb == 0 && a.q_rot != nullptr) {
         for (int idx = tid; idx < rows * (d / 4); idx += kQpThreads) {
             const int r = idx / (d / 4), e = (idx - r * (d / 4)) * 4;
             const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
             *reinterpret_cast<float4*>(a.q_rot + ((size_t)(b0 + bl) * a.Hq + h) * d + e) =
                 *reinterpret_cast<const float4*>(&qr_s[r][e]);
+        }
+    }
+    if (cb == 0 && a.raw_img != nullptr) {
+        // raw image of (b, g): 32 rows x d, rows [0,16) high parts, [16,32) low parts of the
+        // group's G (<= 16) heads; rows of absent heads are zero
+        const size_t ib = raw_img_bytes(d);
+        const int units = d / 8;
+        for (int idx = tid; idx < nb * 16 * units; idx += kQpThreads) {
+            const int bl = idx / (16 * units), rem = idx - bl * 16 * units;
+            const int i = rem / units, u = rem - i * units;
+            uint8_t* img = a.raw_img + ((size_t)(b0 + bl) * a.Hkv + g) * ib;
+            uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+            if (i < G) {
+                const float* src = &qr_s[bl * ni + i][u * 8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(src[2 * k], src[2 * k + 1]);
+                    const float2 hf = __bfloat1622float2(h2);
+                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(src[2 * k] - hf.x, src[2 * k + 1] - hf.y);
+                    hi[k] = *reinterpret_cast<const uint32_t*>(&h2);
+                    lo[k] = *reinterpret_cast<const uint32_t*>(&l2);
+                }
+            }
+            *reinterpret_cast<uint4*>(img + ptx::sw128_offset(i, u * 8, 32)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(img + ptx::sw128_offset(16 + i, u * 8, 32)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
     }
     if (a.U_K == nullptr) return;
@@ -191,12 +217,20 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
             acc[k] = fmaf(q4.x, u0, fmaf(q4.y, u1, fmaf(q4.z, u2, fmaf(q4.w, u3, acc[k]))));
         }
     }
+    const int col = cb * kQpCols + c;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int r = rg * 8 + k;
         if (r < rows) {
             const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
-            a.q_lat[((size_t)(b0 + bl) * a.Hq + h) * a.r_k + cb * kQpCols + c] = acc[k];
+            if (a.q_lat != nullptr) a.q_lat[((size_t)(b0 + bl) * a.Hq + h) * a.r_k + col] = acc[k];
+            if (a.lat_img != nullptr) {
+                uint8_t* img = a.lat_img + (size_t)(b0 + bl) * lat_img_bytes(a.NP, a.r_k);
+                const __nv_bfloat16 hv = __float2bfloat16_rn(acc[k]);
+                const __nv_bfloat16 lv = __float2bfloat16_rn(acc[k] - __bfloat162float(hv));
+                *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(h, col, 2 * a.NP)) = hv;
+                *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(a.NP + h, col, 2 * a.NP)) = lv;
+            }
         }
     }
 }
@@ -503,8 +537,12 @@ __global__ void __launch_bounds__(256) simt_reconstruct_kernel(const T* __restri
 template <typename T>
 cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* q_rot,
                          float* q_lat, int B, int Hq, int Hkv, int d, int r_k, double base,
-                         float scale_log2, cudaStream_t st, bool pdl) {
+                         float scale_log2, cudaStream_t st, bool pdl, uint8_t* lat_img,
+                         uint8_t* raw_img, int NP) {
     QprojArgs a;
+    a.lat_img = lat_img;
+    a.raw_img = raw_img;
+    a.NP = NP;
     a.q = q;
     a.U_K = U_K;
     a.q_pos = q_pos;
@@ -565,7 +603,8 @@ cudaError_t launch_simt_reconstruct(const T* C, const T* U, T* out, int rows, in
 
 #define SLIMKV_INST(T)                                                                           \
     template cudaError_t launch_qproj<T>(const T*, const T*, const int32_t*, float*, float*, int, \
-                                         int, int, int, int, double, float, cudaStream_t, bool);  \
+                                         int, int, int, int, double, float, cudaStream_t, bool,   \
+                                         uint8_t*, uint8_t*, int);                                \
     template cudaError_t launch_simt_decode<T>(const SimtDecodeArgs&, cudaStream_t);              \
     template cudaError_t launch_combine<T>(const CombineArgs&, cudaStream_t, bool);               \
     template cudaError_t launch_simt_reconstruct<T>(const T*, const T*, T*, int, int, int,        \

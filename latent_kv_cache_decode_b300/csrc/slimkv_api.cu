@@ -69,6 +69,11 @@ WsLayout layout(const slimkv_shape* s, int which) {
     off = align_up(off + sizeof(float) * s->B * s->Hq * s->d);
     L.q_lat = off;
     if (lat) off = align_up(off + sizeof(float) * s->B * s->Hq * s->r_k);
+    const int NP = (s->Hq + 15) / 16 * 16;
+    L.lat_img = off;
+    if (lat) off = align_up(off + (size_t)s->B * lat_img_bytes(NP, s->r_k));
+    L.raw_img = off;
+    off = align_up(off + (size_t)s->B * s->Hkv * raw_img_bytes(s->d));
     L.acc = off;
     off = align_up(off + sizeof(float) * (size_t)L.slots * s->Hq * L.Dmax);
     L.ml = off;
@@ -251,6 +256,8 @@ slimkv_status run(const slimkv_shape* s, int which, const Ptrs& p, void* stream)
         char* ws = static_cast<char*>(p.ws);
         c.q_rot = reinterpret_cast<float*>(ws + L.q_rot);
         c.q_lat = reinterpret_cast<float*>(ws + L.q_lat);
+        c.lat_img = reinterpret_cast<uint8_t*>(ws + L.lat_img);
+        c.raw_img = reinterpret_cast<uint8_t*>(ws + L.raw_img);
         c.acc = reinterpret_cast<float*>(ws + L.acc);
         c.ml = reinterpret_cast<float*>(ws + L.ml);
         c.kind = reinterpret_cast<int*>(ws + L.kind);

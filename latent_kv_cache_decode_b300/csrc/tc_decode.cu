@@ -58,9 +58,11 @@ constexpr int kSlot = 2 * kBox;       // ring slot: 128 rows x 128 columns
 constexpr int kThreads = 192;
 constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory we may use per CTA
 constexpr int kNumKinds = 3;          // latent, raw source 0, raw source 1
-constexpr int kNG = 16;               // MMA N of a raw tile: the group's heads, padded
+constexpr int kNG = 16;               // heads of a raw tile's query operand (the group's heads, padded)
 constexpr float kLazy = 8.f;          // m_ref moves only when a score exceeds it by this (log2)
 constexpr int kPAtom = 128 * 32;      // bytes of one 16-head column block of P (128 rows x 32 B)
+constexpr int kR = 16;                // depth of the per-tile barrier rings
+constexpr int kMaxSlots = 16;
 
 struct TcParams {
     CUtensorMap tm[2 * kNumKinds];    // per kind: keys, values (latent 3-D, raw 4-D)
@@ -70,17 +72,19 @@ struct TcParams {
     int ngroups[kNumKinds];           // segments of this kind per batch element
     int dk[kNumKinds], dv[kNumKinds]; // key / value width
     int tiles_per_b;
-    const float* q_lat;               // [B, Hq, r_k]  (scaled)
-    const float* q_rot;               // [B, Hq, d]    (scaled)
+    const uint8_t* lat_img;           // query images (bf16 hi / lo, operand layout)
+    const uint8_t* raw_img;
+    uint32_t lat_img_bytes, raw_img_bytes;
     float* acc;                       // [slots, Hq, Dmax]
     float* ml;                        // [slots, 2, Hq]
     int* kind;                        // [slots]
     int Dmax;
-    int nslot, npbuf, lookahead;
-    int q_cols;                       // columns of each query operand part (multiple of 64)
+    int nslot;                        // ring slots of 32 KB
+    int vstack;                       // value accumulator keeps hi / lo parts side by side
+    int accbuf;                       // TMEM accumulator buffers (1 or 2)
+    int accstride;                    // TMEM columns of one accumulator buffer
     uint32_t off_q, off_p, off_bar, off_red;
     uint32_t tmem_cols;
-    int vstack;                       // value accumulator keeps hi / lo parts side by side
     int u_begin[kMaxCtas + 1];        // CTA i owns units (tiles) [u_begin[i], u_begin[i+1])
     int slot_base[kMaxCtas];          // first partial slot of CTA i
 };
@@ -106,39 +110,69 @@ __device__ __forceinline__ Piece piece_at(const TcParams& p, int u, int u1) {
     return r;
 }
 
-struct TileInfo {
-    int k, nK, nV;
-    bool first, last;
-    int seg;
+// Walks a CTA's tiles in order: tile j (0-based), its piece index and position.
+struct TileIter {
+    const TcParams* p;
+    int u, u1;
+    Piece pc;
+    int t, j, piece;
+    __device__ __forceinline__ void init(const TcParams& prm, int u0, int u1_) {
+        p = &prm;
+        u = u0;
+        u1 = u1_;
+        j = 0;
+        piece = 0;
+        if (u < u1) {
+            pc = piece_at(prm, u, u1);
+            t = pc.t0;
+        }
+    }
+    __device__ __forceinline__ bool valid() const { return u < u1; }
+    __device__ __forceinline__ bool first() const { return t == pc.t0; }
+    __device__ __forceinline__ void next() {
+        ++j;
+        ++t;
+        if (t == pc.t0 + pc.n) {
+            u += pc.n;
+            ++piece;
+            if (u < u1) {
+                pc = piece_at(*p, u, u1);
+                t = pc.t0;
+            }
+        }
+    }
 };
 
-// A tile's coordinates for the producer.
-struct TileRef {
-    int b, k, g, t;
+// Barriers (all in shared memory), per tile j of the CTA, ring index j % kR:
+//   kready  K tile (and, for a piece's first tile, its query image) landed   [TMA tx]
+//   vready  V tile landed and P(j) written by the softmax warps             [TMA tx + 128 arrivals]
+//   kfree   score MMAs of tile j complete: K slots reusable, S(j) readable  [commit]
+//   vfree   value MMAs of tile j complete: V slots and P buffer reusable     [commit]
+//   accfree[2] the softmax warps have read a piece's accumulator             [128 arrivals]
+struct Bars {
+    uint64_t* kready;
+    uint64_t* vready;
+    uint64_t* kfree;
+    uint64_t* vfree;
+    uint64_t* accfree;
+    uint64_t* drain;
 };
+__device__ __forceinline__ uint32_t ph_of(int j) { return (uint32_t)(j / kR) & 1u; }
 
 // Shared state of the softmax warps.
 struct SoftCtx {
-    uint64_t* s_full;
-    uint64_t* s_empty;
-    uint64_t* p_full;
-    uint64_t* p_empty;
+    Bars bar;
     uint8_t* pbuf;
-    float* red;         // [4][NP] per-warp reductions
-    float* m_ref_s;     // [NP] reference max (log2 domain) of the current piece
-    float* alpha_s;     // [NP] rescale factors
+    float* red;           // [4][NP] per-warp reductions
+    float* m_ref_s;       // [NP] reference max (log2 domain) of the current piece
+    float* alpha_s;       // [NP] rescale factors
     volatile int* flags;  // [2][4] per-tile "needs a new reference max" votes
     volatile int* abort;
-    uint32_t t_S, t_acc, lane_off;
-    int tid, wq, lane, myrow, npbuf, nMB;
-    int aw;             // TMEM columns per 128 value rows of the accumulator
-    bool vstack;        // accumulator holds hi and lo parts side by side
+    uint32_t t_S, t_accp, lane_off;   // t_accp: accumulator of the current piece
+    int tid, wq, lane, myrow, nMB;
+    int aw;               // TMEM columns per 128 value rows of the accumulator
+    bool vstack;
 };
-
-__device__ __forceinline__ int pbuf_index(int j, int npbuf) { return npbuf == 2 ? (j & 1) : 0; }
-__device__ __forceinline__ uint32_t pbuf_parity(int j, int npbuf) {
-    return (uint32_t)(npbuf == 2 ? (j >> 1) : j) & 1u;
-}
 
 // bf16 high part of x and the bf16 rounding of the remainder, packed in pairs.
 __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -149,16 +183,17 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// Softmax of tile j (rows t*128 ..) of the current piece, NS heads wide, `nvalid`
-// of them real. Reads S^T from TMEM, writes P (hi, lo) as the MN-major B operand
-// of the value MMA: 16-head column blocks of 128 rows x 32 bytes, 32-byte swizzle.
+// Softmax of tile j of the current piece, NS heads wide, `nvalid` of them real.
+// Reads S^T from TMEM (hi scores at +0, lo scores at +NS), writes P (hi, lo) as the
+// MN-major B operand of the value MMA (16-head column blocks of 128 rows x 32 bytes,
+// 32-byte swizzle), then signals vready[j].
 template <int NS, int NP>
 __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, bool valid, bool has_prev,
                                              int nvalid, float (&l_part)[NP], float (&mref)[NP]) {
-    const int sb = j & 1;
-    ptx::mbar_wait(&c.s_full[sb], (j >> 1) & 1, c.abort);
+    const int jr = j % kR;
+    ptx::mbar_wait(&c.bar.kfree[jr], ph_of(j), c.abort);   // S(j) complete
     ptx::tc_fence_after();
-    const uint32_t tS = c.t_S + c.lane_off + sb * (2 * NP);   // hi scores, then lo scores at +NS
+    const uint32_t tS = c.t_S + c.lane_off + (j & 1) * (2 * NP);
 
     // pass 1: does a score of this row exceed its head's reference by more than kLazy?
     float dmax = -INFINITY;
@@ -210,8 +245,7 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, bool valid
         if (has_prev) {
             // the accumulator holds earlier tiles of this piece: wait until their
             // value MMAs are done, then scale each head's column(s)
-            const int jp = j - 1;
-            ptx::mbar_wait(&c.p_empty[pbuf_index(jp, c.npbuf)], pbuf_parity(jp, c.npbuf), c.abort);
+            ptx::mbar_wait(&c.bar.vfree[(j - 1) % kR], ph_of(j - 1), c.abort);
             ptx::tc_fence_after();
             for (int cc = 0; cc < c.nMB; ++cc) {
 #pragma unroll
@@ -220,7 +254,7 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, bool valid
 #pragma unroll
                     for (int hc = 0; hc < NS / 16; ++hc) {
                         float v[16];
-                        const uint32_t ta = c.t_acc + c.lane_off + cc * c.aw + part * NS + hc * 16;
+                        const uint32_t ta = c.t_accp + c.lane_off + cc * c.aw + part * NS + hc * 16;
                         ptx::tmem_ld16(ta, v);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[i] *= c.alpha_s[hc * 16 + i];
@@ -228,14 +262,13 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, bool valid
                     }
                 }
             }
-            ptx::tc_fence_before();
         }
     }
 
-    // pass 2: probabilities against the reference, as bf16 high + low parts
-    const int pb = pbuf_index(j, c.npbuf);
-    if (j >= c.npbuf) ptx::mbar_wait(&c.p_empty[pb], pbuf_parity(j, c.npbuf) ^ 1u, c.abort);
-    uint8_t* phi = c.pbuf + pb * (2 * NP * 256);
+    // pass 2: probabilities against the reference, as bf16 high + low parts; the P
+    // buffer (j & 1) is free once the value MMAs of tile j - 2 are done
+    if (j >= 2) ptx::mbar_wait(&c.bar.vfree[(j - 2) % kR], ph_of(j - 2), c.abort);
+    uint8_t* phi = c.pbuf + (j & 1) * (2 * NP * 256);
     uint8_t* plo = phi + NS * 256;
     const uint32_t row_off = c.myrow * 32;
     const uint32_t sw = ((c.myrow >> 2) & 1) << 4;
@@ -260,10 +293,9 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, bool valid
         *reinterpret_cast<uint4*>(plo + o0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         *reinterpret_cast<uint4*>(plo + o1) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
     }
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(&c.s_empty[sb]);
-    ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive(&c.p_full[pb]);
+    ptx::tc_fence_before();          // TMEM reads / writes of this tile before the signal
+    ptx::fence_proxy_async_smem();   // P stores visible to the tensor core
+    ptx::mbar_arrive(&c.bar.vready[jr]);
 }
 
 // End of a piece: reduce the row sums, write (m, l) and the accumulator columns of
@@ -290,7 +322,7 @@ __device__ __forceinline__ void write_partial(const TcParams& p, const SoftCtx& 
 #pragma unroll
         for (int hc = 0; hc < NS / 16; ++hc) {
             float v[16];
-            const uint32_t ta = c.t_acc + c.lane_off + cc * c.aw + hc * 16;
+            const uint32_t ta = c.t_accp + c.lane_off + cc * c.aw + hc * 16;
             if (c.vstack) {
                 float w[16];
                 ptx::tmem_ld16x2(ta, ta + NS, v, w);
@@ -310,14 +342,19 @@ __device__ __forceinline__ void write_partial(const TcParams& p, const SoftCtx& 
     }
 }
 
-template <int NP>
+// NP: query heads rounded up to 16; VS: the value accumulator keeps hi / lo parts
+// side by side (one MMA per k-step) instead of summing them in place (two MMAs).
+// Both are template parameters so that the MMA issue sequences are straight-line
+// code: a conditional branch between two tcgen05.mma instructions costs the
+// issuing thread tens of cycles per MMA.
+template <int NP, int VS>
 __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
-    uint8_t* qbuf = smem + p.off_q;          // query operand: 2 NS rows (hi parts, lo parts)
-    uint8_t* pbuf = smem + p.off_p;          // [npbuf][hi, lo][NP/16 blocks][128 rows x 32 B]
+    uint8_t* qbuf = smem + p.off_q;          // query operand of the current piece (image copy)
+    uint8_t* pbuf = smem + p.off_p;          // [2][hi, lo][NP/16 blocks][128 rows x 32 B]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     float* red = reinterpret_cast<float*>(smem + p.off_red);   // [4][NP]
     float* m_ref_s = red + 4 * NP;                             // [NP]
@@ -326,40 +363,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
     // one tile's votes never sees the next tile's)
     volatile int* flag = reinterpret_cast<volatile int*>(alpha_s + NP);
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(alpha_s + NP) + 12;
+    int* owner = reinterpret_cast<int*>(alpha_s + NP) + 16;    // [kMaxSlots] producer's slot owners
 
-    uint64_t* full = bars;
-    uint64_t* empty = bars + p.nslot;
-    uint64_t* s_full = bars + 2 * p.nslot;
-    uint64_t* s_empty = s_full + 2;
-    uint64_t* p_full = s_empty + 2;
-    uint64_t* p_empty = p_full + 2;
-    uint64_t* q_full = p_empty + 2;
-    uint64_t* q_empty = q_full + 1;
-    uint64_t* acc_full = q_empty + 1;
-    uint64_t* acc_empty = acc_full + 1;
-    uint64_t* drain = acc_empty + 1;
+    Bars bar;
+    bar.kready = bars;
+    bar.vready = bars + kR;
+    bar.kfree = bars + 2 * kR;
+    bar.vfree = bars + 3 * kR;
+    bar.accfree = bars + 4 * kR;
+    bar.drain = bars + 4 * kR + 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
     const int u0 = p.u_begin[cta], u1 = p.u_begin[cta + 1];
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < p.nslot; ++i) {
-            ptx::mbar_init(&full[i], 1);
-            ptx::mbar_init(&empty[i], 1);
+        for (int i = 0; i < kR; ++i) {
+            ptx::mbar_init(&bar.kready[i], 1);
+            ptx::mbar_init(&bar.vready[i], 1 + 128);
+            ptx::mbar_init(&bar.kfree[i], 1);
+            ptx::mbar_init(&bar.vfree[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(&s_full[i], 1);
-            ptx::mbar_init(&s_empty[i], 128);
-            ptx::mbar_init(&p_full[i], 128);
-            ptx::mbar_init(&p_empty[i], 1);
-        }
-        ptx::mbar_init(q_full, 1);
-        ptx::mbar_init(q_empty, 1);
-        ptx::mbar_init(acc_full, 1);
-        ptx::mbar_init(acc_empty, 128);
-        ptx::mbar_init(drain, 1);
+        ptx::mbar_init(&bar.accfree[0], 128);
+        ptx::mbar_init(&bar.accfree[1], 128);
+        ptx::mbar_init(bar.drain, 1);
         for (int i = 0; i < 9; ++i) flag[i] = 0;
+        for (int i = 0; i < kMaxSlots; ++i) owner[i] = -1;
         ptx::fence_mbar_init();
     }
     if (warp == 1) ptx::tmem_alloc(tmem_base_s, p.tmem_cols);
@@ -368,200 +397,235 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_base_s;
     const uint32_t t_S = tmem;             // 2 score buffers, 2*NP columns each (hi, lo)
-    const uint32_t t_acc = tmem + 4 * NP;  // value accumulators, aw columns per 128 value rows
+    const uint32_t t_acc = tmem + 4 * NP;  // accumulator buffers
     const int aw = p.vstack ? 2 * NP : NP;
     volatile int* abort_flag = &flag[0];
     pdl_trigger();
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
+        // Ring loads in the order the MMAs consume them: K(0), K(1), V(0), K(2), V(1),
+        // ..., V(n-1). A piece's query image is copied into the single query buffer
+        // once the score MMAs of the previous piece are done; its bytes are part of
+        // the kready phase of the piece's first tile.
         if (lane == 0) {
             for (int i = 0; i < 2 * kNumKinds; ++i)
                 if (p.rows[i >> 1] > 0) ptx::tma_prefetch_desc(&p.tm[i]);
-            // Ring loads follow the MMA issue order exactly: with lookahead that is
-            // K(0), K(1), V(0), K(2), V(1), ..., V(n-1), so a value tile arrives about
-            // when its probabilities are ready instead of idling in the ring.
-            uint32_t ld = 0;
-            int slot = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            auto load = [&](const TileRef& r, int part) {
-                const CUtensorMap* tm = &p.tm[2 * r.k + part];
-                const int nc = ((part ? p.dv[r.k] : p.dk[r.k]) + 127) >> 7;
-                for (int c = 0; ok && c < nc; ++c) {
-                    if (!ptx::mbar_wait(&empty[slot], ph ^ 1u, abort_flag)) {
-                        ok = false;
-                        break;
+            int pos = 0;                     // ring position of the next slot
+            bool pdl_done = false;
+            // pending query-image copy
+            bool q_pend = false;
+            int q_tile = 0, q_after = -1;    // kready tile; tile whose score MMAs must finish first
+            const uint8_t* q_src = nullptr;
+            uint32_t q_bytes = 0;
+            auto try_q = [&](bool block) {
+                if (!q_pend) return;
+                if (q_after < 0) {
+                    if (!pdl_done) {
+                        pdl_wait();          // the images come from the preceding kernel
+                        pdl_done = true;
                     }
-                    uint8_t* dst = ring + (size_t)slot * kSlot;
-                    ptx::mbar_expect_tx(&full[slot], kSlot);
-                    if (r.k == 0) {
-                        ptx::tma_load_3d(dst, tm, c * 128, r.t * kTile, r.b, &full[slot]);
-                        ptx::tma_load_3d(dst + kBox, tm, c * 128 + 64, r.t * kTile, r.b, &full[slot]);
-                    } else {
-                        ptx::tma_load_4d(dst, tm, c * 128, r.g, r.t * kTile, r.b, &full[slot]);
-                        ptx::tma_load_4d(dst + kBox, tm, c * 128 + 64, r.g, r.t * kTile, r.b, &full[slot]);
-                    }
-                    ++ld;
-                    if (++slot == p.nslot) {
-                        slot = 0;
-                        ph ^= 1u;
+                } else if (block) {
+                    ptx::mbar_wait(&bar.kfree[q_after % kR], ph_of(q_after), abort_flag);
+                } else if (!ptx::mbar_test(&bar.kfree[q_after % kR], ph_of(q_after))) {
+                    return;
+                }
+                ptx::bulk_load(qbuf, q_src, q_bytes, &bar.kready[q_tile % kR]);
+                q_pend = false;
+            };
+            // wait until ring slot s is free (its previous tile part is consumed)
+            auto slot_free = [&](int s) {
+                const int o = owner[s];
+                if (o < 0) return;
+                const int oj = o >> 1;
+                uint64_t* fb = (o & 1) ? &bar.vfree[oj % kR] : &bar.kfree[oj % kR];
+                const uint32_t par = ph_of(oj);
+                if (ptx::mbar_test(fb, par)) return;
+                const uint64_t t0 = ptx::globaltimer();
+                for (uint32_t spins = 1; !ptx::mbar_test(fb, par); ++spins) {
+                    try_q(false);
+                    if ((spins & 63u) == 0) {
+                        if (*abort_flag) return;
+                        if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+                            *abort_flag = 1;
+                            return;
+                        }
                     }
                 }
             };
-            TileRef prev{0, 0, 0, 0};
-            bool has_prev = false;
-            for (int u = u0; ok && u < u1;) {
-                const Piece pc = piece_at(p, u, u1);
-                for (int t = pc.t0; ok && t < pc.t0 + pc.n; ++t) {
-                    const TileRef cur{pc.b, pc.k, pc.g, t};
-                    load(cur, 0);
-                    if (p.lookahead) {
-                        if (has_prev) load(prev, 1);
-                        prev = cur;
-                        has_prev = true;
-                    } else {
-                        load(cur, 1);
+            auto load = [&](const TileIter& it, int part) {
+                const int k = it.pc.k;
+                const CUtensorMap* tm = &p.tm[2 * k + part];
+                const int nc = ((part ? p.dv[k] : p.dk[k]) + 127) >> 7;
+                for (int c = 0; c < nc; ++c) slot_free((pos + c) % p.nslot);
+                const int jr = it.j % kR;
+                if (part == 0) {
+                    if (it.first()) {
+                        if (q_pend) try_q(true);   // the previous piece's image goes first
+                        q_pend = true;
+                        q_tile = it.j;
+                        q_after = it.j - 1;        // -1 for the CTA's first piece
+                        if (k == 0) {
+                            q_src = p.lat_img + (size_t)it.pc.b * p.lat_img_bytes;
+                            q_bytes = p.lat_img_bytes;
+                        } else {
+                            q_src = p.raw_img + ((size_t)it.pc.b * p.Hkv + it.pc.g) * p.raw_img_bytes;
+                            q_bytes = p.raw_img_bytes;
+                        }
+                        ptx::mbar_expect_tx_only(&bar.kready[jr], q_bytes);
                     }
+                    ptx::mbar_expect_tx(&bar.kready[jr], nc * kSlot);
+                } else {
+                    ptx::mbar_expect_tx(&bar.vready[jr], nc * kSlot);
                 }
-                u += pc.n;
+                uint64_t* rb = part ? &bar.vready[jr] : &bar.kready[jr];
+                for (int c = 0; c < nc; ++c) {
+                    const int s = (pos + c) % p.nslot;
+                    uint8_t* dst = ring + (size_t)s * kSlot;
+                    if (k == 0) {
+                        ptx::tma_load_3d(dst, tm, c * 128, it.t * kTile, it.pc.b, rb);
+                        ptx::tma_load_3d(dst + kBox, tm, c * 128 + 64, it.t * kTile, it.pc.b, rb);
+                    } else {
+                        ptx::tma_load_4d(dst, tm, c * 128, it.pc.g, it.t * kTile, it.pc.b, rb);
+                        ptx::tma_load_4d(dst + kBox, tm, c * 128 + 64, it.pc.g, it.t * kTile, it.pc.b, rb);
+                    }
+                    owner[s] = (it.j << 1) | part;
+                }
+                pos = (pos + nc) % p.nslot;
+                try_q(false);
+            };
+            TileIter it, prev;
+            it.init(p, u0, u1);
+            bool has_prev = false;
+            int kiss = 0, viss = 0;   // tiles whose K / V loads were issued
+            for (; it.valid() && !*abort_flag; it.next()) {
+                load(it, 0);
+                kiss = it.j + 1;
+                if (has_prev) {
+                    load(prev, 1);
+                    viss = prev.j + 1;
+                }
+                prev = it;
+                has_prev = true;
             }
-            if (ok && has_prev) load(prev, 1);
-            if (!ok) {
-                // let the copies already in flight land before the CTA winds down
-                const uint32_t first = ld > (uint32_t)p.nslot ? ld - p.nslot : 0u;
-                for (uint32_t i = first; i < ld; ++i) {
-                    volatile int never = 0;
-                    ptx::mbar_wait(&full[i % p.nslot], (i / p.nslot) & 1, &never);
-                }
+            if (has_prev && !*abort_flag) {
+                load(prev, 1);
+                viss = prev.j + 1;
+            }
+            try_q(true);
+            if (!pdl_done) pdl_wait();
+            if (*abort_flag) {
+                // let copies still in flight land before the CTA winds down (bounded waits;
+                // a phase whose other arrivals never come just times out)
+                volatile int never = 0;
+                for (int j = max(0, kiss - kR / 2); j < kiss; ++j) ptx::mbar_wait(&bar.kready[j % kR], ph_of(j), &never);
+                for (int j = max(0, viss - kR / 2); j < viss; ++j) ptx::mbar_wait(&bar.vready[j % kR], ph_of(j), &never);
             }
         }
     } else if (warp == 1) {
         // --------------------------------------------------------------------- MMA
+        // Per tile: one wait + one commit for the scores, one wait + one commit for
+        // the values. Waits and commits stall the issuing thread behind the tensor
+        // core's in-flight operand reads, so there are as few of them as possible.
         if (lane == 0) {
             const uint32_t idS_lat = ptx::idesc_bf16(128, 2 * NP, false, false);
             const uint32_t idS_raw = ptx::idesc_bf16(128, 2 * kNG, false, false);
-            const int vs = p.vstack;
-            const uint32_t idV_lat = ptx::idesc_bf16(128, vs ? 2 * NP : NP, true, true);
-            const uint32_t idV_raw = ptx::idesc_bf16(128, vs ? 2 * kNG : kNG, true, true);
+            const uint32_t idV_lat = ptx::idesc_bf16(128, VS ? 2 * NP : NP, true, true);
+            const uint32_t idV_raw = ptx::idesc_bf16(128, VS ? 2 * kNG : kNG, true, true);
             // base descriptors; a k-step or ring slot only adds (byte offset >> 4) to
             // the start-address field, which stays below 2^14 for shared memory
             const uint64_t dA_S = ptx::sdesc_sw128(ptx::smem_u32(ring), 16, 1024);      // K tile, K-major
             const uint64_t dA_V = ptx::sdesc_sw128(ptx::smem_u32(ring), kBox, 1024);    // V tile, MN-major
             const uint64_t dB_Q = ptx::sdesc_sw128(ptx::smem_u32(qbuf), 16, 1024);      // Q, K-major
             const uint64_t dB_P = ptx::sdesc_sw32(ptx::smem_u32(pbuf), kPAtom, 256);    // P, MN-major
-            // ring cursor: the MMAs consume the ring strictly in load order
-            int sl = 0;
-            uint32_t phs = 0;
-            auto advance = [&]() {
-                if (++sl == p.nslot) {
-                    sl = 0;
-                    phs ^= 1u;
-                }
-            };
+            int pos = 0;   // ring position, same sequence as the producer
 
-            // scores: S^T[tile row, (part, head)] = K_tile[row, :] . Q[(part, head), :]
-            auto issue_S = [&](const TileInfo& ti, int jj) -> bool {
-                if (ti.first && !ptx::mbar_wait(q_full, ti.seg & 1, abort_flag)) return false;
-                const int sb = jj & 1;
-                if (!ptx::mbar_wait(&s_empty[sb], ((jj >> 1) & 1) ^ 1, abort_flag)) return false;
-                ptx::tc_fence_after();
-                const bool lat = ti.k == 0;
+            auto issue_S = [&](const TileIter& ti) {
+                const int jr = ti.j % kR;
+                ptx::mbar_wait(&bar.kready[jr], ph_of(ti.j), abort_flag);
+                const bool lat = ti.pc.k == 0;
                 const uint32_t idS = lat ? idS_lat : idS_raw;
                 const uint32_t qstride = (lat ? 2 * NP : 2 * kNG) * 128 >> 4;   // 64-column chunk of Q
-                const int ksteps = p.dk[ti.k] >> 4;
-                const uint32_t dS = t_S + sb * (2 * NP);
-                for (int c = 0; c < ti.nK; ++c) {
-                    if (!ptx::mbar_wait(&full[sl], phs, abort_flag)) return false;
-                    ptx::tc_fence_after();
-                    const uint64_t a0 = dA_S + (uint64_t)((sl * kSlot) >> 4);
+                const int ksteps = p.dk[ti.pc.k] >> 4;
+                const int nK = (p.dk[ti.pc.k] + 127) >> 7;
+                const int nfull = ksteps >> 3;   // whole 128-column chunks
+                const uint32_t dS = t_S + (ti.j & 1) * (2 * NP);
+                for (int c = 0; c < nfull; ++c) {
+                    const int s = (pos + c) % p.nslot;
+                    const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
                     const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
+                    const uint32_t acc0 = c != 0 ? 1u : 0u;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        if (c * 8 + kk < ksteps)
-                            ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
-                                          b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS,
-                                          (c | kk) != 0 ? 1u : 0u);
-                    }
-                    ptx::mma_commit(&empty[sl]);
-                    advance();
+                    for (int kk = 0; kk < 8; ++kk)
+                        ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
+                                      b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS, kk == 0 ? acc0 : 1u);
                 }
-                ptx::mma_commit(&s_full[sb]);
-                if (ti.last) ptx::mma_commit(q_empty);
-                return true;
+                if (nfull < nK) {
+                    // a last, partial chunk (key width not a multiple of 128)
+                    const int c = nfull;
+                    const int s = (pos + c) % p.nslot;
+                    const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
+                    const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
+                    for (int kk = 0; kk < ksteps - 8 * c; ++kk)
+                        ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
+                                      b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS,
+                                      (c | kk) != 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(&bar.kfree[jr]);
+                pos = (pos + nK) % p.nslot;
             };
-            // values: acc^T[value row, (part, head)] += V_tile[:, value row]^T . P
-            auto issue_V = [&](const TileInfo& ti, int jj) -> bool {
-                const int pb = pbuf_index(jj, p.npbuf);
-                if (!ptx::mbar_wait(&p_full[pb], pbuf_parity(jj, p.npbuf), abort_flag)) return false;
-                if (ti.first && ti.seg > 0 && !ptx::mbar_wait(acc_empty, (ti.seg - 1) & 1, abort_flag))
-                    return false;
+            auto issue_V = [&](const TileIter& ti) {
+                const int jr = ti.j % kR;
+                ptx::mbar_wait(&bar.vready[jr], ph_of(ti.j), abort_flag);
+                const int pc = ti.piece;
+                if (ti.first()) {
+                    // the accumulator buffer of this piece must have been read out
+                    if (p.accbuf == 2) {
+                        if (pc >= 2) ptx::mbar_wait(&bar.accfree[pc & 1], (uint32_t)((pc >> 1) - 1) & 1u, abort_flag);
+                    } else if (pc >= 1) {
+                        ptx::mbar_wait(&bar.accfree[0], (uint32_t)(pc - 1) & 1u, abort_flag);
+                    }
+                }
                 ptx::tc_fence_after();
-                const bool lat = ti.k == 0;
+                const bool lat = ti.pc.k == 0;
                 const uint32_t idV = lat ? idV_lat : idV_raw;
                 const uint32_t lo_off = (lat ? NP : kNG) * 256 >> 4;   // lo part of P
-                const uint64_t pd = dB_P + (uint64_t)((pb * (2 * NP * 256)) >> 4);
-                for (int c = 0; c < ti.nV; ++c) {
-                    if (!ptx::mbar_wait(&full[sl], phs, abort_flag)) return false;
-                    ptx::tc_fence_after();
-                    const uint64_t vd = dA_V + (uint64_t)((sl * kSlot) >> 4);
-                    const uint32_t dacc = t_acc + c * aw;
+                const uint64_t pd = dB_P + (uint64_t)(((ti.j & 1) * (2 * NP * 256)) >> 4);
+                const int nV = (p.dv[ti.pc.k] + 127) >> 7;
+                const uint32_t abase = t_acc + (uint32_t)((p.accbuf == 2 ? (pc & 1) : 0) * p.accstride);
+                const uint32_t acc0 = ti.first() ? 0u : 1u;
+                for (int c = 0; c < nV; ++c) {
+                    const int s = (pos + c) % p.nslot;
+                    const uint64_t vd = dA_V + (uint64_t)((s * kSlot) >> 4);
+                    const uint32_t d0 = abase + c * aw;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t accum = (ti.first && kk == 0) ? 0u : 1u;
                         const uint64_t a = vd + (uint64_t)(kk * (2048 >> 4));
                         const uint64_t b = pd + (uint64_t)(kk * (512 >> 4));
-                        ptx::mma_bf16(dacc, a, b, idV, accum);
-                        if (!vs) ptx::mma_bf16(dacc, a, b + lo_off, idV, 1u);
+                        ptx::mma_bf16(d0, a, b, idV, kk == 0 ? acc0 : 1u);
+                        if (!VS) ptx::mma_bf16(d0, a, b + lo_off, idV, 1u);
                     }
-                    ptx::mma_commit(&empty[sl]);
-                    advance();
                 }
-                ptx::mma_commit(&p_empty[pb]);
-                if (ti.last) ptx::mma_commit(acc_full);
-                return true;
+                ptx::mma_commit(&bar.vfree[jr]);
+                pos = (pos + nV) % p.nslot;
             };
 
-            bool ok = true;
-            int jS = 0, jV = 0, seg = 0;
-            TileInfo pend;
-            bool has_pend = false;
-            for (int u = u0; ok && u < u1; ++seg) {
-                const Piece pc = piece_at(p, u, u1);
-                for (int t = pc.t0; ok && t < pc.t0 + pc.n; ++t) {
-                    TileInfo ti;
-                    ti.k = pc.k;
-                    ti.nK = (p.dk[pc.k] + 127) >> 7;
-                    ti.nV = (p.dv[pc.k] + 127) >> 7;
-                    ti.first = (t == pc.t0);
-                    ti.last = (t == pc.t0 + pc.n - 1);
-                    ti.seg = seg;
-                    ok = issue_S(ti, jS++);
-                    if (ok && has_pend) {
-                        ok = issue_V(pend, jV++);
-                        has_pend = false;
-                    }
-                    if (ok) {
-                        if (p.lookahead) {
-                            pend = ti;
-                            has_pend = true;
-                        } else {
-                            ok = issue_V(ti, jV++);
-                        }
-                    }
-                }
-                u += pc.n;
+            TileIter it, prev;
+            it.init(p, u0, u1);
+            bool has_prev = false;
+            for (; it.valid(); it.next()) {
+                issue_S(it);
+                if (has_prev) issue_V(prev);
+                prev = it;
+                has_prev = true;
             }
-            if (ok && has_pend) ok = issue_V(pend, jV++);
-            ptx::mma_commit(drain);   // arrives once every MMA issued above has completed
+            if (has_prev) issue_V(prev);
+            ptx::mma_commit(bar.drain);   // arrives once every MMA issued above has completed
         }
     } else {
         // ----------------------------------------------------------------- softmax
         SoftCtx c;
-        c.s_full = s_full;
-        c.s_empty = s_empty;
-        c.p_full = p_full;
-        c.p_empty = p_empty;
+        c.bar = bar;
         c.pbuf = pbuf;
         c.red = red;
         c.m_ref_s = m_ref_s;
@@ -575,72 +639,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         c.myrow = q4 * 32 + lane;            // tile row (S) / value row (acc) of this thread
         c.lane_off = (uint32_t)(q4 * 32) << 16;
         c.t_S = t_S;
-        c.t_acc = t_acc;
-        c.npbuf = p.npbuf;
         c.aw = aw;
         c.vstack = p.vstack != 0;
         const int G = p.G;
         float l_part[NP], mref[NP];
 
-        pdl_wait();   // q_lat / q_rot come from the preceding kernel
+        pdl_wait();   // the workspace partials may still be read by the preceding calls' kernels
 
-        // bf16 high / low parts of the query operand of segment (b, k, g): NS rows
-        auto write_q = [&](int b, int k, int g) {
-            const int dk = p.dk[k];
-            const int NS = k == 0 ? NP : kNG;   // rows [0, NS) hi parts, [NS, 2 NS) lo parts
-            const int nvalid = k == 0 ? p.Hq : G;
-            const float* src = k == 0 ? p.q_lat + (size_t)b * p.Hq * dk
-                                      : p.q_rot + ((size_t)b * p.Hq + (size_t)g * G) * dk;
-            const int units = dk >> 3, total = NS * units;
-            // batches of 8 units per thread: all loads of a batch are in flight together
-            for (int base = c.tid; base < total; base += 128 * 8) {
-                float4 va[8], vb[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int task = base + q * 128;
-                    const int h = task / units, u = task - h * units;
-                    va[q] = vb[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (task < total && h < nvalid) {
-                        const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)h * dk + u * 8);
-                        va[q] = s4[0];
-                        vb[q] = s4[1];
-                    }
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int task = base + q * 128;
-                    if (task >= total) break;
-                    const int h = task / units, u = task - h * units;
-                    uint32_t hi[4], lo[4];
-                    split_pair(va[q].x, va[q].y, hi[0], lo[0]);
-                    split_pair(va[q].z, va[q].w, hi[1], lo[1]);
-                    split_pair(vb[q].x, vb[q].y, hi[2], lo[2]);
-                    split_pair(vb[q].z, vb[q].w, hi[3], lo[3]);
-                    *reinterpret_cast<uint4*>(qbuf + ptx::sw128_offset(h, u * 8, 2 * NS)) =
-                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(qbuf + ptx::sw128_offset(NS + h, u * 8, 2 * NS)) =
-                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::named_bar(1, 128);
-            if (c.tid == 0) ptx::mbar_arrive(q_full);
-        };
-
-        // A failed wait (abort) does not leave the loop: every softmax thread keeps
-        // the same control flow so the named barriers stay matched; results are
-        // poisoned at the end instead.
-        if (u0 < u1) {
-            const Piece p0 = piece_at(p, u0, u1);
-            write_q(p0.b, p0.k, p0.g);
-        }
-        int j = 0, seg = 0;
-        for (int u = u0; u < u1; ++seg) {
-            const Piece pc = piece_at(p, u, u1);
+        TileIter it;
+        it.init(p, u0, u1);
+        while (it.valid()) {
+            const Piece pc = it.pc;
+            const int piece = it.piece;
             const int k = pc.k;
             const bool lat = (k == 0);
             const int nvalid = lat ? p.Hq : G;
             c.nMB = (p.dv[k] + 127) >> 7;
+            c.t_accp = t_acc + (uint32_t)((p.accbuf == 2 ? (piece & 1) : 0) * p.accstride);
             if (c.tid < NP) m_ref_s[c.tid] = -INFINITY;
 #pragma unroll
             for (int h = 0; h < NP; ++h) {
@@ -648,28 +663,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 mref[h] = -INFINITY;
             }
             ptx::named_bar(1, 128);
-            for (int t = pc.t0; t < pc.t0 + pc.n; ++t, ++j) {
+            int jl = it.j;
+            for (int n = 0; n < pc.n; ++n) {
+                const int t = it.t;
                 const bool valid = t * kTile + c.myrow < p.rows[k];
-                if (lat) softmax_tile<NP, NP>(c, j, valid, t > pc.t0, nvalid, l_part, mref);
-                else softmax_tile<kNG, NP>(c, j, valid, t > pc.t0, nvalid, l_part, mref);
-            }
-            // the next piece's query operand goes in before this piece's partial is
-            // written, so its score MMAs overlap the write-out
-            if (u + pc.n < u1) {
-                ptx::mbar_wait(q_empty, seg & 1, abort_flag);
-                const Piece nx = piece_at(p, u + pc.n, u1);
-                write_q(nx.b, nx.k, nx.g);
+                jl = it.j;
+                if (lat) softmax_tile<NP, NP>(c, it.j, valid, t > pc.t0, nvalid, l_part, mref);
+                else softmax_tile<kNG, NP>(c, it.j, valid, t > pc.t0, nvalid, l_part, mref);
+                it.next();
             }
             // ---- partial of (CTA, piece): reference max, row sum and accumulator
-            ptx::mbar_wait(acc_full, seg & 1, abort_flag);
+            ptx::mbar_wait(&bar.vfree[jl % kR], ph_of(jl), abort_flag);   // V(jl) complete
             ptx::tc_fence_after();
-            const int slot = p.slot_base[cta] + seg;
+            const int slot = p.slot_base[cta] + piece;
             if (lat) write_partial<NP, NP>(p, c, slot, kSlotLatent, 0, nvalid, p.dv[k], l_part);
             else write_partial<kNG, NP>(p, c, slot, kSlotRawGroup + pc.g, pc.g * G, nvalid, p.dv[k], l_part);
             ptx::tc_fence_before();
-            ptx::mbar_arrive(acc_empty);
+            ptx::mbar_arrive(&bar.accfree[p.accbuf == 2 ? (piece & 1) : 0]);
             ptx::named_bar(1, 128);
-            u += pc.n;
         }
     }
 
@@ -680,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         ptx::tc_fence_after();
         if (lane == 0) {
             volatile int never = 0;
-            ptx::mbar_wait(drain, 0, &never);   // every MMA of this CTA has completed
+            ptx::mbar_wait(bar.drain, 0, &never);   // every MMA of this CTA has completed
         }
         __syncwarp();
         ptx::tmem_dealloc(tmem, p.tmem_cols);
@@ -705,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
 
 // Shared-memory plan of one launch.
 struct SmemPlan {
-    int NP, nslot, npbuf, lookahead, q_cols, vstack;
+    int NP, nslot, q_cols, vstack, accbuf, accstride;
     uint32_t off_q, off_p, off_bar, off_red, total, tmem_cols;
     bool ok;
 };
@@ -715,38 +726,42 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], const int rows[kNumKinds]) {
     SmemPlan s{};
     s.NP = round_up(Hq, 16);
-    int qc = 0, nmb = 0, need = 0;
+    int qc = 0, nmb = 0, maxK = 0, maxV = 0;
     for (int k = 0; k < kNumKinds; ++k) {
         if (rows[k] <= 0) continue;
         qc = std::max(qc, dk[k]);
         nmb = std::max(nmb, (dv[k] + 127) / 128);
-        need = std::max(need, (dk[k] + 127) / 128 + (dv[k] + 127) / 128);
+        maxK = std::max(maxK, (dk[k] + 127) / 128);
+        maxV = std::max(maxV, (dv[k] + 127) / 128);
     }
     s.q_cols = round_up(qc, 64);
-    const int q_bytes = 2 * s.NP * s.q_cols * 2;   // hi and lo parts
-    // TMEM: two score buffers of 2*NP columns, then the accumulator; hi / lo parts of
-    // the accumulator side by side when they fit, else summed in place
-    s.vstack = (4 * s.NP + nmb * 2 * s.NP) <= 512 ? 1 : 0;
-    const int tmem = 4 * s.NP + nmb * (s.vstack ? 2 : 1) * s.NP;
+    s.ok = false;
+    if (s.NP > 64) return s;
+    // TMEM: two score buffers of 2*NP columns, then one or two accumulator buffers;
+    // prefer hi / lo accumulator parts side by side and two buffers
+    const int opts[4][2] = {{1, 2}, {1, 1}, {0, 2}, {0, 1}};
+    int tmem = 0;
+    for (auto& o : opts) {
+        s.vstack = o[0];
+        s.accbuf = o[1];
+        s.accstride = nmb * (s.vstack ? 2 : 1) * s.NP;
+        tmem = 4 * s.NP + s.accbuf * s.accstride;
+        if (tmem <= 512) break;
+    }
+    if (tmem > 512) return s;
     s.tmem_cols = 32;
     while ((int)s.tmem_cols < tmem) s.tmem_cols *= 2;
-    s.ok = false;
-    if (s.NP > 64 || s.tmem_cols > 512) return s;
-    const int misc_bytes = (6 * s.NP + 16) * 4;
-    for (s.npbuf = 2; s.npbuf >= 1; --s.npbuf) {
-        const int p_bytes = s.npbuf * 2 * s.NP * 256;
-        const int nbars = 2 * 16 + 13;   // up to 16 ring slots
-        const int misc = nbars * 8 + misc_bytes + 1024;   // + alignment slack
-        const int avail = kSmemMax - q_bytes - p_bytes - misc;
-        s.nslot = std::min(16, avail / kSlot);
-        if (s.nslot >= 2) break;
-    }
-    if (s.nslot < 2) return s;
-    s.lookahead = (s.nslot >= need) ? 1 : 0;
+    const int q_bytes = 2 * s.NP * s.q_cols * 2;   // hi and lo parts
+    const int p_bytes = 2 * 2 * s.NP * 256;        // two P buffers, hi and lo parts
+    const int nbars = 4 * kR + 3;
+    const int misc_bytes = (6 * s.NP + 32) * 4;
+    const int avail = kSmemMax - q_bytes - p_bytes - round_up(nbars * 8, 16) - misc_bytes - 1024;
+    s.nslot = std::min(kMaxSlots, avail / kSlot);
+    if (s.nslot < maxK + maxV) return s;
     s.off_q = s.nslot * kSlot;
     s.off_p = s.off_q + q_bytes;
-    s.off_bar = s.off_p + s.npbuf * 2 * s.NP * 256;
-    s.off_red = s.off_bar + round_up((2 * s.nslot + 13) * 8, 16);
+    s.off_bar = s.off_p + p_bytes;
+    s.off_red = s.off_bar + round_up(nbars * 8, 16);
     s.total = s.off_red + misc_bytes + 1024;
     s.ok = s.total <= (uint32_t)kSmemMax;
     return s;
@@ -919,11 +934,11 @@ const WorkPlan& cached_plan(int B, const SegList& sl, int max_ctas) {
     return cache.emplace(key, make_plan(B, sl, max_ctas)).first->second;
 }
 
-template <int NP>
+template <int NP, int VS>
 cudaError_t launch_decode(const TcParams& prm, int grid, uint32_t smem, cudaStream_t st) {
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<NP, VS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemMax);
         if (e != cudaSuccess) return e;
         attr_done = true;
@@ -938,7 +953,7 @@ cudaError_t launch_decode(const TcParams& prm, int grid, uint32_t smem, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<NP>, prm);
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<NP, VS>, prm);
 }
 
 // Kinds of key rows of one call: rows / widths per segment and operands.
@@ -992,9 +1007,10 @@ bool tc_supported(int Hq, int Hkv, int d, int N_b, int r_k, int r_v) {
 cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     typedef __nv_bfloat16 bf16;
     const bool lat = c.which == SLIMKV_LATENT && c.N_b > 0;
-    cudaError_t e = launch_qproj<bf16>((const bf16*)c.q, lat ? (const bf16*)c.U_K : nullptr, c.q_pos, c.q_rot,
-                                       lat ? c.q_lat : nullptr, c.B, c.Hq, c.Hkv, c.d, c.r_k, c.rope_base,
-                                       c.scale_log2, st, true);
+    const int NPq = (c.Hq + 15) / 16 * 16;
+    cudaError_t e = launch_qproj<bf16>((const bf16*)c.q, lat ? (const bf16*)c.U_K : nullptr, c.q_pos, nullptr,
+                                       nullptr, c.B, c.Hq, c.Hkv, c.d, c.r_k, c.rope_base, c.scale_log2, st, true,
+                                       lat ? c.lat_img : nullptr, c.raw_img, NPq);
     if (e != cudaSuccess) return e;
     if (c.which == SLIMKV_RECONSTRUCT) {
         // plain launches (no early trigger): the decode below reads K_b / V_b
@@ -1039,16 +1055,17 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     prm.Hq = c.Hq;
     prm.Hkv = c.Hkv;
     prm.G = c.Hq / c.Hkv;
-    prm.q_lat = c.q_lat;
-    prm.q_rot = c.q_rot;
+    prm.lat_img = c.lat_img;
+    prm.raw_img = c.raw_img;
+    prm.lat_img_bytes = (uint32_t)lat_img_bytes(sp.NP, c.r_k);
+    prm.raw_img_bytes = (uint32_t)raw_img_bytes(c.d);
     prm.acc = c.acc;
     prm.ml = c.ml;
     prm.kind = c.kind;
     prm.Dmax = c.Dmax;
     prm.nslot = sp.nslot;
-    prm.npbuf = sp.npbuf;
-    prm.lookahead = sp.lookahead;
-    prm.q_cols = sp.q_cols;
+    prm.accbuf = sp.accbuf;
+    prm.accstride = sp.accstride;
     prm.off_q = sp.off_q;
     prm.off_p = sp.off_p;
     prm.off_bar = sp.off_bar;
@@ -1060,10 +1077,14 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
 
     timer_before(st);
     switch (sp.NP) {
-        case 16: e = launch_decode<16>(prm, w.n_ctas, sp.total, st); break;
-        case 32: e = launch_decode<32>(prm, w.n_ctas, sp.total, st); break;
-        case 48: e = launch_decode<48>(prm, w.n_ctas, sp.total, st); break;
-        case 64: e = launch_decode<64>(prm, w.n_ctas, sp.total, st); break;
+        case 16: e = sp.vstack ? launch_decode<16, 1>(prm, w.n_ctas, sp.total, st)
+                               : launch_decode<16, 0>(prm, w.n_ctas, sp.total, st); break;
+        case 32: e = sp.vstack ? launch_decode<32, 1>(prm, w.n_ctas, sp.total, st)
+                               : launch_decode<32, 0>(prm, w.n_ctas, sp.total, st); break;
+        case 48: e = sp.vstack ? launch_decode<48, 1>(prm, w.n_ctas, sp.total, st)
+                               : launch_decode<48, 0>(prm, w.n_ctas, sp.total, st); break;
+        case 64: e = sp.vstack ? launch_decode<64, 1>(prm, w.n_ctas, sp.total, st)
+                               : launch_decode<64, 0>(prm, w.n_ctas, sp.total, st); break;
         default: e = cudaErrorInvalidValue;
     }
     timer_after(st);

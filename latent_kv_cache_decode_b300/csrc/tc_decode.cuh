@@ -23,6 +23,8 @@ struct TcCall {
     float* out;
     float* q_rot;
     float* q_lat;
+    uint8_t* lat_img;          // query images written by the query kernel
+    uint8_t* raw_img;
     float* acc;
     float* ml;
     int* kind;
