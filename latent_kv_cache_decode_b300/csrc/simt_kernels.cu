@@ -226,10 +226,7 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
             if (a.q_lat != nullptr) a.q_lat[((size_t)(b0 + bl) * a.Hq + h) * a.r_k + col] = acc[k];
             if (a.lat_img != nullptr) {
                 uint8_t* img = a.lat_img + (size_t)(b0 + bl) * lat_img_bytes(a.NP, a.r_k);
-                const __nv_bfloat16 hv = __float2bfloat16_rn(acc[k]);
-                const __nv_bfloat16 lv = __float2bfloat16_rn(acc[k] - __bfloat162float(hv));
-                *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(h, col, 2 * a.NP)) = hv;
-                *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(a.NP + h, col, 2 * a.NP)) = lv;
+                *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(h, col, a.NP)) = __float2bfloat16_rn(acc[k]);
             }
         }
     }

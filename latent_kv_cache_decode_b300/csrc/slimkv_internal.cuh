@@ -39,7 +39,7 @@ struct WsLayout {
     size_t acc = 0;      // float [slots, Hq, Dmax]   per-split value accumulators
     size_t ml = 0;       // float [slots, 2, Hq]      per-split running max (log2) and sum
     size_t kind = 0;     // int   [slots]             what a partial covers (SlotKind)
-    size_t lat_img = 0;  // bf16  [B][2 NP x r_k]     latent query image (tensor-core path)
+    size_t lat_img = 0;  // bf16  [B][NP x r_k]       latent query image (tensor-core path)
     size_t raw_img = 0;  // bf16  [B][Hkv][32 x d]    raw query images (tensor-core path)
     size_t kb = 0;       // T     [B, N_b, Hkv, d]    materialised beacon keys (reconstruct)
     size_t vb = 0;       // T     [B, N_b, Hkv, d]    materialised beacon values (reconstruct)
@@ -101,7 +101,7 @@ struct QprojArgs {
     // Query operands of the tensor-core decode kernel, as bf16 high / low parts laid
     // out exactly as that kernel's shared-memory operand (128-byte swizzled rows of
     // 64 columns, for a 1024-byte aligned destination), so it can copy them in bulk:
-    uint8_t* lat_img;            // per b: rows [0, NP) high, [NP, 2 NP) low parts of q_lat[b]
+    uint8_t* lat_img;            // per b: NP rows, bf16 of q_lat[b] (heads past Hq unused)
     uint8_t* raw_img;            // per (b, g): rows [0, 16) high, [16, 32) low parts of q_rot of group g
     int NP;                      // heads of the latent image, rounded up to 16
     int B, Hq, Hkv, d, r_k;
@@ -136,7 +136,7 @@ cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* 
                          uint8_t* raw_img = nullptr, int NP = 0);
 
 // Bytes of the query images (latent: per batch element; raw: per (batch element, KV group)).
-__host__ __device__ inline size_t lat_img_bytes(int NP, int r_k) { return (size_t)2 * NP * ((r_k + 63) / 64 * 64) * 2; }
+__host__ __device__ inline size_t lat_img_bytes(int NP, int r_k) { return (size_t)NP * ((r_k + 63) / 64 * 64) * 2; }
 __host__ __device__ inline size_t raw_img_bytes(int d) { return (size_t)2 * 16 * d * 2; }
 template <typename T>
 cudaError_t launch_simt_decode(const SimtDecodeArgs& a, cudaStream_t st);

@@ -20,11 +20,13 @@
 // the float32 query, which already carries scale * log2(e)), stacked along N:
 //   scores  S^T[row, (part, head)] = tile[row, :] . Q[(part, head), :]
 //           (one tcgen05.mma per 16-wide k-step, M = 128 rows, N = 2 x heads); the
-//           softmax adds the two parts;
-//   softmax P[row, head] = exp2(S^T - m_ref[head]), split into bf16 high + low parts,
-//           again stacked along N;
-//   values  acc^T[value dim, (part, head)] += tile_V[:, value dim]^T . P (M = 128
-//           value dims); the two parts are added when the partial is written.
+//           softmax adds the two parts. The latent query is rounded to bf16 in one
+//           part: latent scores are not peaked, so its rounding stays far inside the
+//           error bar, while the raw window (whose keys can be large) keeps both;
+//   softmax P[row, head] = exp2(S^T - m_ref[head]), rounded to bf16 (the rounding
+//           of P, unlike that of the query, stays far inside the error bar: the
+//           relative error of a weight is at most 2^-9 and averages out);
+//   values  acc^T[value dim, head] += tile_V[:, value dim]^T . P (M = 128 value dims).
 // Issuing few, wide MMAs matters: the issuing thread, not the tensor core, is the
 // limit for narrow ones.
 // m_ref is a lazy running maximum: it moves (and the TMEM accumulator is rescaled)
@@ -55,12 +57,17 @@ namespace {
 constexpr int kTile = 128;            // rows per tile (MMA M)
 constexpr int kBox = 16384;           // one TMA box: 128 rows x 64 bf16 columns, 128B-swizzled
 constexpr int kSlot = 2 * kBox;       // ring slot: 128 rows x 128 columns
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory we may use per CTA
 constexpr int kNumKinds = 3;          // latent, raw source 0, raw source 1
 constexpr int kNG = 16;               // heads of a raw tile's query operand (the group's heads, padded)
-constexpr float kLazy = 8.f;          // m_ref moves only when a score exceeds it by this (log2)
-constexpr int kPAtom = 128 * 32;      // bytes of one 16-head column block of P (128 rows x 32 B)
+// m_ref moves only when a score exceeds it by more than this (log2 units). P values up
+// to 2^20 are exact enough in bf16 high + low parts and far from fp32 overflow, so a
+// generous margin keeps the rescale path (which waits for the previous value MMAs)
+// off the common path even for peaked score distributions.
+constexpr float kLazy = 20.f;
+constexpr int kPAtom = 128 * 32;      // bytes of one 16-head column block of P per 128 rows (x 32 B)
+constexpr int kRBRaw = 2;             // 128-row blocks per raw tile: a raw tile is 256 tokens of one KV head
 constexpr int kR = 16;                // depth of the per-tile barrier rings
 constexpr int kMaxSlots = 16;
 
@@ -71,6 +78,7 @@ struct TcParams {
     int tiles[kNumKinds];             // tiles of one segment
     int ngroups[kNumKinds];           // segments of this kind per batch element
     int dk[kNumKinds], dv[kNumKinds]; // key / value width
+    int rb[kNumKinds];                // 128-row blocks per tile (1 latent, kRBRaw raw)
     int tiles_per_b;
     const uint8_t* lat_img;           // query images (bf16 hi / lo, operand layout)
     const uint8_t* raw_img;
@@ -80,7 +88,6 @@ struct TcParams {
     int* kind;                        // [slots]
     int Dmax;
     int nslot;                        // ring slots of 32 KB
-    int vstack;                       // value accumulator keeps hi / lo parts side by side
     int accbuf;                       // TMEM accumulator buffers (1 or 2)
     int accstride;                    // TMEM columns of one accumulator buffer
     uint32_t off_q, off_p, off_bar, off_red;
@@ -171,131 +178,216 @@ struct SoftCtx {
     uint32_t t_S, t_accp, lane_off;   // t_accp: accumulator of the current piece
     int tid, wq, lane, myrow, nMB;
     int aw;               // TMEM columns per 128 value rows of the accumulator
-    bool vstack;
 };
 
-// bf16 high part of x and the bf16 rounding of the remainder, packed in pairs.
-__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    const float2 hf = __bfloat1622float2(h);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-    hi = *reinterpret_cast<const uint32_t*>(&h);
-    lo = *reinterpret_cast<const uint32_t*>(&l);
+
+// TMEM columns of one score buffer: hi and lo scores (2 x NS columns) for each of
+// the tile's row blocks; at least 64.
+template <int NP> struct SBuf {
+    // latent tiles: NP score columns; raw tiles: hi and lo columns of kNG heads per row block
+    static constexpr int W = NP > 2 * kNG * kRBRaw ? NP : 2 * kNG * kRBRaw;
+    // bytes of one P buffer: NP heads x 128 rows (latent) or kNG heads x 256 rows (raw), bf16
+    static constexpr int PB = (NP > kNG * kRBRaw ? NP : kNG * kRBRaw) * 256;
+};
+
+// The rare path of the softmax, kept out of line so that the hot loop stays small in
+// the instruction cache: a new reference maximum per head from this tile's scores,
+// the rescale factors alpha = exp2(m_old - m_new), and, when the accumulator already
+// holds earlier tiles of the piece (nMB > 0), the rescale of its columns once the
+// previous value MMAs are done. All 128 softmax threads call it together.
+template <int NS, int NP, int RB, bool LO>
+__device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* alpha_s, uint64_t* vfree,
+                                             volatile int* abort, uint32_t tS0, uint32_t t_acc_lane, int row0,
+                                             int rows, int nvalid, int j, int nMB, int aw, int tid,
+                                             int lane, int wq) {
+#pragma unroll 1
+    for (int hc = 0; hc < NS / 16; ++hc) {
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = -INFINITY;
+#pragma unroll 1
+        for (int rb = 0; rb < RB; ++rb) {
+            const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
+            const bool valid = row0 + rb * 128 < rows;
+            float hi[16], lo[16];
+            if (LO) {
+                ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi, lo);
+            } else {
+                ptx::tmem_ld16(tS + hc * 16, hi);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) lo[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (valid && hc * 16 + i < nvalid) x[i] = fmaxf(x[i], hi[i] + lo[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float v = x[i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) red[wq * NP + hc * 16 + i] = v;
+        }
+    }
+    ptx::named_bar(1, 128);
+    if (tid < NS) {
+        const float M = fmaxf(fmaxf(red[tid], red[NP + tid]), fmaxf(red[2 * NP + tid], red[3 * NP + tid]));
+        const float mo = m_ref_s[tid];
+        float a = 1.f;
+        if (M > mo) {
+            a = (mo == -INFINITY) ? 0.f : exp2f(mo - M);
+            m_ref_s[tid] = M;
+        }
+        alpha_s[tid] = a;
+    }
+    ptx::named_bar(1, 128);
+    if (nMB > 0) {
+        ptx::mbar_wait(&vfree[(j - 1) % kR], ph_of(j - 1), abort);
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < nMB; ++cc) {
+#pragma unroll 1
+            for (int hc = 0; hc < NS / 16; ++hc) {
+                float v[16];
+                const uint32_t ta = t_acc_lane + cc * aw + hc * 16;
+                ptx::tmem_ld16(ta, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] *= alpha_s[hc * 16 + i];
+                ptx::tmem_st16(ta, v);
+            }
+        }
+    }
 }
 
-// Softmax of tile j of the current piece, NS heads wide, `nvalid` of them real.
-// Reads S^T from TMEM (hi scores at +0, lo scores at +NS), writes P (hi, lo) as the
-// MN-major B operand of the value MMA (16-head column blocks of 128 rows x 32 bytes,
-// 32-byte swizzle), then signals vready[j].
-template <int NS, int NP>
-__device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, bool valid, bool has_prev,
+// Softmax of tile j of the current piece: RB row blocks of 128 rows, NS heads wide,
+// `nvalid` of them real; row0 is this thread's row index (segment-wide) in block 0.
+// Reads S^T from TMEM (block rb: hi scores at +rb*2NS, lo at +rb*2NS+NS), writes P
+// (hi, lo) as the MN-major B operand of the value MMA (16-head column blocks of
+// 128*RB rows x 32 bytes, 32-byte swizzle), then signals vready[j].
+template <int NS, int NP, int RB, bool LO>
+__device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, int rows, bool has_prev,
                                              int nvalid, float (&l_part)[NP], float (&mref)[NP]) {
+    constexpr int SW = SBuf<NP>::W;
     const int jr = j % kR;
     ptx::mbar_wait(&c.bar.kfree[jr], ph_of(j), c.abort);   // S(j) complete
     ptx::tc_fence_after();
-    const uint32_t tS = c.t_S + c.lane_off + (j & 1) * (2 * NP);
+    const uint32_t tS0 = c.t_S + c.lane_off + (j & 1) * SW;
 
-    // pass 1: does a score of this row exceed its head's reference by more than kLazy?
+    // pass 1: does a score of this thread's rows exceed its head's reference by more than kLazy?
     float dmax = -INFINITY;
 #pragma unroll
-    for (int hc = 0; hc < NS / 16; ++hc) {
-        float hi[16], lo[16];
-        ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi, lo);
+    for (int rb = 0; rb < RB; ++rb) {
+        const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
+        const bool valid = row0 + rb * 128 < rows;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (hc * 16 + i < nvalid) dmax = fmaxf(dmax, (hi[i] + lo[i]) - mref[hc * 16 + i]);
+        for (int hc = 0; hc < NS / 16; ++hc) {
+            float hi[16], lo[16];
+            if (LO) {
+                ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi, lo);
+            } else {
+                ptx::tmem_ld16(tS + hc * 16, hi);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) lo[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (valid && hc * 16 + i < nvalid) dmax = fmaxf(dmax, (hi[i] + lo[i]) - mref[hc * 16 + i]);
+        }
     }
-    if (!valid) dmax = -INFINITY;
     const bool any = __any_sync(0xffffffffu, dmax > kLazy);
     volatile int* fl = c.flags + (j & 1) * 4;
     if (c.lane == 0) fl[c.wq] = any ? 1 : 0;
     ptx::named_bar(1, 128);
     if (fl[0] | fl[1] | fl[2] | fl[3]) {
-        // new reference: the exact per-head maximum over this tile's valid rows
-#pragma unroll
-        for (int hc = 0; hc < NS / 16; ++hc) {
-            float hi[16], lo[16];
-            ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi, lo);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float x = (valid && hc * 16 + i < nvalid) ? hi[i] + lo[i] : -INFINITY;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-                if (c.lane == 0) c.red[c.wq * NP + hc * 16 + i] = x;
-            }
-        }
-        ptx::named_bar(1, 128);
-        if (c.tid < NS) {
-            const float M = fmaxf(fmaxf(c.red[c.tid], c.red[NP + c.tid]),
-                                  fmaxf(c.red[2 * NP + c.tid], c.red[3 * NP + c.tid]));
-            const float mo = c.m_ref_s[c.tid];
-            float a = 1.f;
-            if (M > mo) {
-                a = (mo == -INFINITY) ? 0.f : exp2f(mo - M);
-                c.m_ref_s[c.tid] = M;
-            }
-            c.alpha_s[c.tid] = a;
-        }
-        ptx::named_bar(1, 128);
+        softmax_new_ref<NS, NP, RB, LO>(c.red, c.m_ref_s, c.alpha_s, c.bar.vfree, c.abort, tS0, c.t_accp + c.lane_off,
+                                    row0, rows, nvalid, j, has_prev ? c.nMB : 0, c.aw, c.tid, c.lane,
+                                    c.wq);
 #pragma unroll
         for (int h = 0; h < NS; ++h) {
             mref[h] = c.m_ref_s[h];
             l_part[h] *= c.alpha_s[h];
-        }
-        if (has_prev) {
-            // the accumulator holds earlier tiles of this piece: wait until their
-            // value MMAs are done, then scale each head's column(s)
-            ptx::mbar_wait(&c.bar.vfree[(j - 1) % kR], ph_of(j - 1), c.abort);
-            ptx::tc_fence_after();
-            for (int cc = 0; cc < c.nMB; ++cc) {
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    if (part == 1 && !c.vstack) break;
-#pragma unroll
-                    for (int hc = 0; hc < NS / 16; ++hc) {
-                        float v[16];
-                        const uint32_t ta = c.t_accp + c.lane_off + cc * c.aw + part * NS + hc * 16;
-                        ptx::tmem_ld16(ta, v);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= c.alpha_s[hc * 16 + i];
-                        ptx::tmem_st16(ta, v);
-                    }
-                }
-            }
         }
     }
 
     // pass 2: probabilities against the reference, as bf16 high + low parts; the P
     // buffer (j & 1) is free once the value MMAs of tile j - 2 are done
     if (j >= 2) ptx::mbar_wait(&c.bar.vfree[(j - 2) % kR], ph_of(j - 2), c.abort);
-    uint8_t* phi = c.pbuf + (j & 1) * (2 * NP * 256);
-    uint8_t* plo = phi + NS * 256;
-    const uint32_t row_off = c.myrow * 32;
-    const uint32_t sw = ((c.myrow >> 2) & 1) << 4;
+    uint8_t* phi = c.pbuf + (j & 1) * SBuf<NP>::PB;
 #pragma unroll
-    for (int hc = 0; hc < NS / 16; ++hc) {
-        float hi_s[16], lo_s[16];
-        ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi_s, lo_s);
-        float pr[16];
+    for (int rb = 0; rb < RB; ++rb) {
+        const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
+        const bool valid = row0 + rb * 128 < rows;
+        const int row = rb * 128 + c.myrow;
+        const uint32_t row_off = row * 32;
+        const uint32_t sw = ((row >> 2) & 1) << 4;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int h = hc * 16 + i;
-            pr[i] = (valid && h < nvalid) ? exp2f((hi_s[i] + lo_s[i]) - mref[h]) : 0.f;
-            l_part[h] += pr[i];
+        for (int hc = 0; hc < NS / 16; ++hc) {
+            float hi_s[16], lo_s[16];
+            if (LO) {
+                ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi_s, lo_s);
+            } else {
+                ptx::tmem_ld16(tS + hc * 16, hi_s);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) lo_s[i] = 0.f;
+            }
+            float pr[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int h = hc * 16 + i;
+                pr[i] = 0.f;
+                if (h < nvalid) {   // uniform: padding heads need no exponential
+                    pr[i] = valid ? exp2f((hi_s[i] + lo_s[i]) - mref[h]) : 0.f;
+                    l_part[h] += pr[i];
+                }
+            }
+            uint32_t hi[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[2 * i], pr[2 * i + 1]);
+                hi[i] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            const uint32_t o0 = hc * (kPAtom * RB) + row_off + (0u ^ sw);
+            const uint32_t o1 = hc * (kPAtom * RB) + row_off + (16u ^ sw);
+            *reinterpret_cast<uint4*>(phi + o0) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(phi + o1) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
         }
-        uint32_t hi[8], lo[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) split_pair(pr[2 * i], pr[2 * i + 1], hi[i], lo[i]);
-        const uint32_t o0 = hc * kPAtom + row_off + (0u ^ sw);
-        const uint32_t o1 = hc * kPAtom + row_off + (16u ^ sw);
-        *reinterpret_cast<uint4*>(phi + o0) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(phi + o1) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-        *reinterpret_cast<uint4*>(plo + o0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        *reinterpret_cast<uint4*>(plo + o1) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
     }
     ptx::tc_fence_before();          // TMEM reads / writes of this tile before the signal
     ptx::fence_proxy_async_smem();   // P stores visible to the tensor core
     ptx::mbar_arrive(&c.bar.vready[jr]);
+}
+
+// Partial write-out of a piece, out of line (once per piece): (m, l) of the piece's
+// real heads from the per-warp row-sum reductions in `red`, and the accumulator
+// columns (hi + lo parts when side by side) read from TMEM.
+template <int NS, int NP>
+__device__ __noinline__ void write_partial_acc(float* ml, float* acc, int* kindp, const float* red,
+                                               const float* m_ref_s, int Hq, int Dmax, int slot, int kind, int h0,
+                                               int nvalid, int dv, int nMB, int aw, uint32_t t_acc_lane,
+                                               int tid, int myrow) {
+    if (tid < nvalid) {
+        const float L = red[tid] + red[NP + tid] + red[2 * NP + tid] + red[3 * NP + tid];
+        ml[((size_t)slot * 2) * Hq + h0 + tid] = m_ref_s[tid];
+        ml[((size_t)slot * 2 + 1) * Hq + h0 + tid] = L;
+    }
+    if (tid == 0) kindp[slot] = kind;
+#pragma unroll 1
+    for (int cc = 0; cc < nMB; ++cc) {
+        const int r = cc * 128 + myrow;
+#pragma unroll 1
+        for (int hc = 0; hc < NS / 16; ++hc) {
+            float v[16];
+            const uint32_t ta = t_acc_lane + cc * aw + hc * 16;
+            ptx::tmem_ld16(ta, v);
+            if (r < dv) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int h = hc * 16 + i;
+                    if (h < nvalid) acc[((size_t)slot * Hq + h0 + h) * Dmax + r] = v[i];
+                }
+            }
+        }
+    }
 }
 
 // End of a piece: reduce the row sums, write (m, l) and the accumulator columns of
@@ -311,43 +403,14 @@ __device__ __forceinline__ void write_partial(const TcParams& p, const SoftCtx& 
         if (c.lane == 0) c.red[c.wq * NP + h] = v;
     }
     ptx::named_bar(1, 128);
-    if (c.tid < nvalid) {
-        const float L = c.red[c.tid] + c.red[NP + c.tid] + c.red[2 * NP + c.tid] + c.red[3 * NP + c.tid];
-        p.ml[((size_t)slot * 2) * p.Hq + h0 + c.tid] = c.m_ref_s[c.tid];
-        p.ml[((size_t)slot * 2 + 1) * p.Hq + h0 + c.tid] = L;
-    }
-    if (c.tid == 0) p.kind[slot] = kind;
-    for (int cc = 0; cc < c.nMB; ++cc) {
-        const int r = cc * 128 + c.myrow;
-#pragma unroll
-        for (int hc = 0; hc < NS / 16; ++hc) {
-            float v[16];
-            const uint32_t ta = c.t_accp + c.lane_off + cc * c.aw + hc * 16;
-            if (c.vstack) {
-                float w[16];
-                ptx::tmem_ld16x2(ta, ta + NS, v, w);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] += w[i];
-            } else {
-                ptx::tmem_ld16(ta, v);
-            }
-            if (r < dv) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int h = hc * 16 + i;
-                    if (h < nvalid) p.acc[((size_t)slot * p.Hq + h0 + h) * p.Dmax + r] = v[i];
-                }
-            }
-        }
-    }
+    write_partial_acc<NS, NP>(p.ml, p.acc, p.kind, c.red, c.m_ref_s, p.Hq, p.Dmax, slot, kind, h0, nvalid, dv, c.nMB,
+                              c.aw, c.t_accp + c.lane_off, c.tid, c.myrow);
 }
 
-// NP: query heads rounded up to 16; VS: the value accumulator keeps hi / lo parts
-// side by side (one MMA per k-step) instead of summing them in place (two MMAs).
-// Both are template parameters so that the MMA issue sequences are straight-line
-// code: a conditional branch between two tcgen05.mma instructions costs the
-// issuing thread tens of cycles per MMA.
-template <int NP, int VS>
+// NP: query heads rounded up to 16 (a template parameter, so the MMA issue sequences
+// are straight-line code: a conditional branch between two tcgen05.mma instructions
+// costs the issuing thread tens of cycles per MMA).
+template <int NP>
 __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -371,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
     bar.kfree = bars + 2 * kR;
     bar.vfree = bars + 3 * kR;
     bar.accfree = bars + 4 * kR;
-    bar.drain = bars + 4 * kR + 2;
+    bar.drain = bars + 4 * kR + 2;      // [0] score issuer, [1] value issuer
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
@@ -386,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         }
         ptx::mbar_init(&bar.accfree[0], 128);
         ptx::mbar_init(&bar.accfree[1], 128);
-        ptx::mbar_init(bar.drain, 1);
+        ptx::mbar_init(&bar.drain[0], 1);
+        ptx::mbar_init(&bar.drain[1], 1);
         for (int i = 0; i < 9; ++i) flag[i] = 0;
         for (int i = 0; i < kMaxSlots; ++i) owner[i] = -1;
         ptx::fence_mbar_init();
@@ -396,9 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_base_s;
-    const uint32_t t_S = tmem;             // 2 score buffers, 2*NP columns each (hi, lo)
-    const uint32_t t_acc = tmem + 4 * NP;  // accumulator buffers
-    const int aw = p.vstack ? 2 * NP : NP;
+    constexpr int SW = SBuf<NP>::W;
+    const uint32_t t_S = tmem;             // 2 score buffers of SW columns
+    const uint32_t t_acc = tmem + 2 * SW;  // accumulator buffers
+    const int aw = NP;   // TMEM columns per 128 value rows of the accumulator
     volatile int* abort_flag = &flag[0];
     pdl_trigger();
 
@@ -412,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
             for (int i = 0; i < 2 * kNumKinds; ++i)
                 if (p.rows[i >> 1] > 0) ptx::tma_prefetch_desc(&p.tm[i]);
             int pos = 0;                     // ring position of the next slot
+            const uint64_t pol = ptx::policy_evict_first();   // the cache is streamed once
             bool pdl_done = false;
             // pending query-image copy
             bool q_pend = false;
@@ -456,7 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
             auto load = [&](const TileIter& it, int part) {
                 const int k = it.pc.k;
                 const CUtensorMap* tm = &p.tm[2 * k + part];
-                const int nc = ((part ? p.dv[k] : p.dk[k]) + 127) >> 7;
+                const int ncols = ((part ? p.dv[k] : p.dk[k]) + 127) >> 7;
+                const int RBk = p.rb[k];
+                const int nc = ncols * RBk;   // slots: column chunks x row blocks
                 for (int c = 0; c < nc; ++c) slot_free((pos + c) % p.nslot);
                 const int jr = it.j % kR;
                 if (part == 0) {
@@ -482,12 +550,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 for (int c = 0; c < nc; ++c) {
                     const int s = (pos + c) % p.nslot;
                     uint8_t* dst = ring + (size_t)s * kSlot;
+                    const int col = (c % ncols) * 128;
+                    const int row = (it.t * RBk + c / ncols) * kTile;
                     if (k == 0) {
-                        ptx::tma_load_3d(dst, tm, c * 128, it.t * kTile, it.pc.b, rb);
-                        ptx::tma_load_3d(dst + kBox, tm, c * 128 + 64, it.t * kTile, it.pc.b, rb);
+                        ptx::tma_load_3d_hint(dst, tm, col, row, it.pc.b, rb, pol);
+                        ptx::tma_load_3d_hint(dst + kBox, tm, col + 64, row, it.pc.b, rb, pol);
                     } else {
-                        ptx::tma_load_4d(dst, tm, c * 128, it.pc.g, it.t * kTile, it.pc.b, rb);
-                        ptx::tma_load_4d(dst + kBox, tm, c * 128 + 64, it.pc.g, it.t * kTile, it.pc.b, rb);
+                        ptx::tma_load_4d_hint(dst, tm, col, it.pc.g, row, it.pc.b, rb, pol);
+                        ptx::tma_load_4d_hint(dst + kBox, tm, col + 64, it.pc.g, row, it.pc.b, rb, pol);
                     }
                     owner[s] = (it.j << 1) | part;
                 }
@@ -522,57 +592,86 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 for (int j = max(0, viss - kR / 2); j < viss; ++j) ptx::mbar_wait(&bar.vready[j % kR], ph_of(j), &never);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 6) {
         // --------------------------------------------------------------------- MMA
-        // Per tile: one wait + one commit for the scores, one wait + one commit for
-        // the values. Waits and commits stall the issuing thread behind the tensor
-        // core's in-flight operand reads, so there are as few of them as possible.
+        // Two issuing threads: warp 1 issues the score MMAs, warp 6 the value MMAs, so
+        // the two streams do not wait for each other. Per tile each issues after one
+        // wait and ends with one commit; waits and commits stall an issuing thread
+        // behind the tensor core's in-flight operand reads, so they are kept few.
+        const bool s_issuer = warp == 1;
         if (lane == 0) {
-            const uint32_t idS_lat = ptx::idesc_bf16(128, 2 * NP, false, false);
+            const uint32_t idS_lat = ptx::idesc_bf16(128, NP, false, false);
             const uint32_t idS_raw = ptx::idesc_bf16(128, 2 * kNG, false, false);
-            const uint32_t idV_lat = ptx::idesc_bf16(128, VS ? 2 * NP : NP, true, true);
-            const uint32_t idV_raw = ptx::idesc_bf16(128, VS ? 2 * kNG : kNG, true, true);
+            const uint32_t idV_lat = ptx::idesc_bf16(128, NP, true, true);
+            const uint32_t idV_raw = ptx::idesc_bf16(128, kNG, true, true);
             // base descriptors; a k-step or ring slot only adds (byte offset >> 4) to
             // the start-address field, which stays below 2^14 for shared memory
             const uint64_t dA_S = ptx::sdesc_sw128(ptx::smem_u32(ring), 16, 1024);      // K tile, K-major
             const uint64_t dA_V = ptx::sdesc_sw128(ptx::smem_u32(ring), kBox, 1024);    // V tile, MN-major
             const uint64_t dB_Q = ptx::sdesc_sw128(ptx::smem_u32(qbuf), 16, 1024);      // Q, K-major
-            const uint64_t dB_P = ptx::sdesc_sw32(ptx::smem_u32(pbuf), kPAtom, 256);    // P, MN-major
+            const uint64_t dB_P = ptx::sdesc_sw32(ptx::smem_u32(pbuf), kPAtom, 256);    // P (latent), MN-major
+            const uint64_t dB_Pr = ptx::sdesc_sw32(ptx::smem_u32(pbuf), kPAtom * kRBRaw, 256);  // P (raw)
             int pos = 0;   // ring position, same sequence as the producer
 
+            // ring slots of a tile's keys / values (same walk as the producer)
+            auto nslots = [&](const TileIter& ti, int part) {
+                const int k = ti.pc.k;
+                return (((part ? p.dv[k] : p.dk[k]) + 127) >> 7) * p.rb[k];
+            };
             auto issue_S = [&](const TileIter& ti) {
                 const int jr = ti.j % kR;
-                ptx::mbar_wait(&bar.kready[jr], ph_of(ti.j), abort_flag);
-                const bool lat = ti.pc.k == 0;
-                const uint32_t idS = lat ? idS_lat : idS_raw;
-                const uint32_t qstride = (lat ? 2 * NP : 2 * kNG) * 128 >> 4;   // 64-column chunk of Q
-                const int ksteps = p.dk[ti.pc.k] >> 4;
-                const int nK = (p.dk[ti.pc.k] + 127) >> 7;
-                const int nfull = ksteps >> 3;   // whole 128-column chunks
-                const uint32_t dS = t_S + (ti.j & 1) * (2 * NP);
-                for (int c = 0; c < nfull; ++c) {
-                    const int s = (pos + c) % p.nslot;
-                    const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
-                    const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
-                    const uint32_t acc0 = c != 0 ? 1u : 0u;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
-                                      b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS, kk == 0 ? acc0 : 1u);
+                if (ti.j >= 2) {
+                    // score buffer (j & 1) is free once the softmax warps have read S(j - 2)
+                    ptx::mbar_wait(&bar.vready[(ti.j - 2) % kR], ph_of(ti.j - 2), abort_flag);
+                    ptx::tc_fence_after();
                 }
-                if (nfull < nK) {
-                    // a last, partial chunk (key width not a multiple of 128)
-                    const int c = nfull;
-                    const int s = (pos + c) % p.nslot;
-                    const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
-                    const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
-                    for (int kk = 0; kk < ksteps - 8 * c; ++kk)
-                        ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
-                                      b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS,
-                                      (c | kk) != 0 ? 1u : 0u);
+                ptx::mbar_wait(&bar.kready[jr], ph_of(ti.j), abort_flag);
+                const uint32_t dS = t_S + (ti.j & 1) * SW;
+                if (ti.pc.k == 0) {
+                    // latent tile: 128 beacons, key width r_k in 128-column chunks
+                    const uint32_t qstride = NP * 128 >> 4;   // 64-column chunk of Q
+                    const int ksteps = p.dk[0] >> 4;
+                    const int nK = (p.dk[0] + 127) >> 7;
+                    const int nfull = ksteps >> 3;   // whole 128-column chunks
+                    for (int c = 0; c < nfull; ++c) {
+                        const int s = (pos + c) % p.nslot;
+                        const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
+                        const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
+                        const uint32_t acc0 = c != 0 ? 1u : 0u;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
+                                          b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS_lat,
+                                          kk == 0 ? acc0 : 1u);
+                    }
+                    if (nfull < nK) {
+                        // a last, partial chunk (key width not a multiple of 128)
+                        const int c = nfull;
+                        const int s = (pos + c) % p.nslot;
+                        const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
+                        const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
+                        for (int kk = 0; kk < ksteps - 8 * c; ++kk)
+                            ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
+                                          b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS_lat,
+                                          (c | kk) != 0 ? 1u : 0u);
+                    }
+                    pos = (pos + nK) % p.nslot;
+                } else {
+                    // raw tile: kRBRaw blocks of 128 tokens of one KV head, key width d = 128
+                    const uint32_t qstride = 2 * kNG * 128 >> 4;
+#pragma unroll
+                    for (int rb = 0; rb < kRBRaw; ++rb) {
+                        const int s = (pos + rb) % p.nslot;
+                        const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            ptx::mma_bf16(dS + rb * 2 * kNG, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
+                                          dB_Q + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS_raw,
+                                          kk == 0 ? 0u : 1u);
+                    }
+                    pos = (pos + kRBRaw) % p.nslot;
                 }
                 ptx::mma_commit(&bar.kfree[jr]);
-                pos = (pos + nK) % p.nslot;
             };
             auto issue_V = [&](const TileIter& ti) {
                 const int jr = ti.j % kR;
@@ -587,40 +686,59 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                     }
                 }
                 ptx::tc_fence_after();
-                const bool lat = ti.pc.k == 0;
-                const uint32_t idV = lat ? idV_lat : idV_raw;
-                const uint32_t lo_off = (lat ? NP : kNG) * 256 >> 4;   // lo part of P
-                const uint64_t pd = dB_P + (uint64_t)(((ti.j & 1) * (2 * NP * 256)) >> 4);
-                const int nV = (p.dv[ti.pc.k] + 127) >> 7;
                 const uint32_t abase = t_acc + (uint32_t)((p.accbuf == 2 ? (pc & 1) : 0) * p.accstride);
                 const uint32_t acc0 = ti.first() ? 0u : 1u;
-                for (int c = 0; c < nV; ++c) {
-                    const int s = (pos + c) % p.nslot;
-                    const uint64_t vd = dA_V + (uint64_t)((s * kSlot) >> 4);
-                    const uint32_t d0 = abase + c * aw;
+                const uint32_t pboff = (uint32_t)(((ti.j & 1) * SBuf<NP>::PB) >> 4);
+                if (ti.pc.k == 0) {
+                    const uint64_t pd = dB_P + (uint64_t)pboff;
+                    const int nV = (p.dv[0] + 127) >> 7;
+                    for (int c = 0; c < nV; ++c) {
+                        const int s = (pos + c) % p.nslot;
+                        const uint64_t vd = dA_V + (uint64_t)((s * kSlot) >> 4);
+                        const uint32_t d0 = abase + c * aw;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t a = vd + (uint64_t)(kk * (2048 >> 4));
-                        const uint64_t b = pd + (uint64_t)(kk * (512 >> 4));
-                        ptx::mma_bf16(d0, a, b, idV, kk == 0 ? acc0 : 1u);
-                        if (!VS) ptx::mma_bf16(d0, a, b + lo_off, idV, 1u);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t a = vd + (uint64_t)(kk * (2048 >> 4));
+                            const uint64_t b = pd + (uint64_t)(kk * (512 >> 4));
+                            ptx::mma_bf16(d0, a, b, idV_lat, kk == 0 ? acc0 : 1u);
+                        }
                     }
+                    pos = (pos + nV) % p.nslot;
+                } else {
+                    // 256 tokens: k-steps 0-7 from block 0's slot, 8-15 from block 1's
+                    const uint64_t pd = dB_Pr + (uint64_t)pboff;
+#pragma unroll
+                    for (int rb = 0; rb < kRBRaw; ++rb) {
+                        const int s = (pos + rb) % p.nslot;
+                        const uint64_t vd = dA_V + (uint64_t)((s * kSlot) >> 4);
+                        const uint32_t accr = rb == 0 ? acc0 : 1u;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t a = vd + (uint64_t)(kk * (2048 >> 4));
+                            const uint64_t b = pd + (uint64_t)((rb * 8 + kk) * (512 >> 4));
+                            ptx::mma_bf16(abase, a, b, idV_raw, kk == 0 ? accr : 1u);
+                        }
+                    }
+                    pos = (pos + kRBRaw) % p.nslot;
                 }
                 ptx::mma_commit(&bar.vfree[jr]);
-                pos = (pos + nV) % p.nslot;
             };
 
             TileIter it, prev;
             it.init(p, u0, u1);
             bool has_prev = false;
             for (; it.valid(); it.next()) {
-                issue_S(it);
-                if (has_prev) issue_V(prev);
+                if (s_issuer) issue_S(it);
+                else pos = (pos + nslots(it, 0)) % p.nslot;
+                if (has_prev) {
+                    if (!s_issuer) issue_V(prev);
+                    else pos = (pos + nslots(prev, 1)) % p.nslot;
+                }
                 prev = it;
                 has_prev = true;
             }
-            if (has_prev) issue_V(prev);
-            ptx::mma_commit(bar.drain);   // arrives once every MMA issued above has completed
+            if (has_prev && !s_issuer) issue_V(prev);
+            ptx::mma_commit(&bar.drain[s_issuer ? 0 : 1]);   // arrives once this thread's MMAs completed
         }
     } else {
         // ----------------------------------------------------------------- softmax
@@ -640,7 +758,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         c.lane_off = (uint32_t)(q4 * 32) << 16;
         c.t_S = t_S;
         c.aw = aw;
-        c.vstack = p.vstack != 0;
         const int G = p.G;
         float l_part[NP], mref[NP];
 
@@ -666,10 +783,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
             int jl = it.j;
             for (int n = 0; n < pc.n; ++n) {
                 const int t = it.t;
-                const bool valid = t * kTile + c.myrow < p.rows[k];
+                const int row0 = t * kTile * p.rb[k] + c.myrow;
                 jl = it.j;
-                if (lat) softmax_tile<NP, NP>(c, it.j, valid, t > pc.t0, nvalid, l_part, mref);
-                else softmax_tile<kNG, NP>(c, it.j, valid, t > pc.t0, nvalid, l_part, mref);
+                if (lat) softmax_tile<NP, NP, 1, false>(c, it.j, row0, p.rows[k], t > pc.t0, nvalid, l_part, mref);
+                else softmax_tile<kNG, NP, kRBRaw, true>(c, it.j, row0, p.rows[k], t > pc.t0, nvalid, l_part, mref);
                 it.next();
             }
             // ---- partial of (CTA, piece): reference max, row sum and accumulator
@@ -691,12 +808,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         ptx::tc_fence_after();
         if (lane == 0) {
             volatile int never = 0;
-            ptx::mbar_wait(bar.drain, 0, &never);   // every MMA of this CTA has completed
+            ptx::mbar_wait(&bar.drain[0], 0, &never);   // every MMA of this CTA has completed
+            ptx::mbar_wait(&bar.drain[1], 0, &never);
         }
         __syncwarp();
         ptx::tmem_dealloc(tmem, p.tmem_cols);
     }
-    if (*abort_flag && warp >= 2) {
+    if (*abort_flag && warp >= 2 && warp <= 5) {
         // a wait ran out: poison this CTA's partials so the result is NaN, not stale
         const int tid = threadIdx.x - 64;
         int npieces = 0;
@@ -716,12 +834,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
 
 // Shared-memory plan of one launch.
 struct SmemPlan {
-    int NP, nslot, q_cols, vstack, accbuf, accstride;
+    int NP, nslot, q_cols, accbuf, accstride;
     uint32_t off_q, off_p, off_bar, off_red, total, tmem_cols;
     bool ok;
 };
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// TMEM columns of one score buffer (host copy of SBuf<NP>::W).
+int sbuf_w(int NP) { return std::max(NP, 2 * kNG * kRBRaw); }
 
 SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], const int rows[kNumKinds]) {
     SmemPlan s{};
@@ -729,31 +850,30 @@ SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], con
     int qc = 0, nmb = 0, maxK = 0, maxV = 0;
     for (int k = 0; k < kNumKinds; ++k) {
         if (rows[k] <= 0) continue;
+        const int rbk = k == 0 ? 1 : kRBRaw;
         qc = std::max(qc, dk[k]);
         nmb = std::max(nmb, (dv[k] + 127) / 128);
-        maxK = std::max(maxK, (dk[k] + 127) / 128);
-        maxV = std::max(maxV, (dv[k] + 127) / 128);
+        maxK = std::max(maxK, (dk[k] + 127) / 128 * rbk);   // ring slots of a tile's keys
+        maxV = std::max(maxV, (dv[k] + 127) / 128 * rbk);
     }
     s.q_cols = round_up(qc, 64);
     s.ok = false;
     if (s.NP > 64) return s;
     // TMEM: two score buffers of 2*NP columns, then one or two accumulator buffers;
     // prefer hi / lo accumulator parts side by side and two buffers
-    const int opts[4][2] = {{1, 2}, {1, 1}, {0, 2}, {0, 1}};
+    s.accstride = nmb * s.NP;
     int tmem = 0;
-    for (auto& o : opts) {
-        s.vstack = o[0];
-        s.accbuf = o[1];
-        s.accstride = nmb * (s.vstack ? 2 : 1) * s.NP;
-        tmem = 4 * s.NP + s.accbuf * s.accstride;
+    for (s.accbuf = 2; s.accbuf >= 1; --s.accbuf) {
+        tmem = 2 * sbuf_w(s.NP) + s.accbuf * s.accstride;
         if (tmem <= 512) break;
     }
     if (tmem > 512) return s;
     s.tmem_cols = 32;
     while ((int)s.tmem_cols < tmem) s.tmem_cols *= 2;
-    const int q_bytes = 2 * s.NP * s.q_cols * 2;   // hi and lo parts
-    const int p_bytes = 2 * 2 * s.NP * 256;        // two P buffers, hi and lo parts
-    const int nbars = 4 * kR + 3;
+    // query buffer: the latent image (NP rows, bf16) or a raw image (hi and lo parts of kNG heads)
+    const int q_bytes = std::max(rows[0] > 0 ? s.NP * round_up(dk[0], 64) * 2 : 0, 2 * kNG * 128 * 2);
+    const int p_bytes = 2 * std::max(s.NP, kNG * kRBRaw) * 256;   // two P buffers (bf16)
+    const int nbars = 4 * kR + 4;
     const int misc_bytes = (6 * s.NP + 32) * 4;
     const int avail = kSmemMax - q_bytes - p_bytes - round_up(nbars * 8, 16) - misc_bytes - 1024;
     s.nslot = std::min(kMaxSlots, avail / kSlot);
@@ -934,11 +1054,11 @@ const WorkPlan& cached_plan(int B, const SegList& sl, int max_ctas) {
     return cache.emplace(key, make_plan(B, sl, max_ctas)).first->second;
 }
 
-template <int NP, int VS>
+template <int NP>
 cudaError_t launch_decode(const TcParams& prm, int grid, uint32_t smem, cudaStream_t st) {
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<NP, VS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemMax);
         if (e != cudaSuccess) return e;
         attr_done = true;
@@ -953,7 +1073,7 @@ cudaError_t launch_decode(const TcParams& prm, int grid, uint32_t smem, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<NP, VS>, prm);
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<NP>, prm);
 }
 
 // Kinds of key rows of one call: rows / widths per segment and operands.
@@ -1034,11 +1154,13 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
         prm.ngroups[k] = s.ngroups[k];
         prm.dk[k] = s.dk[k];
         prm.dv[k] = s.dv[k];
-        const int tiles = s.rows[k] > 0 ? (s.rows[k] + kTile - 1) / kTile : 0;
+        prm.rb[k] = k == 0 ? 1 : kRBRaw;
+        const int tile_rows = kTile * prm.rb[k];
+        const int tiles = s.rows[k] > 0 ? (s.rows[k] + tile_rows - 1) / tile_rows : 0;
         prm.tiles[k] = tiles;
         prm.tiles_per_b += tiles * s.ngroups[k];
         // cost of a tile: the 32 KB slots it streams (+1 for its fixed per-tile work)
-        const int cost = (s.dk[k] + 127) / 128 + (s.dv[k] + 127) / 128 + 1;
+        const int cost = ((s.dk[k] + 127) / 128 + (s.dv[k] + 127) / 128) * prm.rb[k] + 1;
         for (int g = 0; g < s.ngroups[k]; ++g) sl.segs.push_back({tiles, cost});
         if (s.rows[k] > 0) {
             const bool ok = k == 0
@@ -1071,20 +1193,15 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     prm.off_bar = sp.off_bar;
     prm.off_red = sp.off_red;
     prm.tmem_cols = sp.tmem_cols;
-    prm.vstack = sp.vstack;
     for (int i = 0; i <= w.n_ctas; ++i) prm.u_begin[i] = w.u_begin[i];
     for (int i = 0; i < w.n_ctas; ++i) prm.slot_base[i] = w.slot_base[i];
 
     timer_before(st);
     switch (sp.NP) {
-        case 16: e = sp.vstack ? launch_decode<16, 1>(prm, w.n_ctas, sp.total, st)
-                               : launch_decode<16, 0>(prm, w.n_ctas, sp.total, st); break;
-        case 32: e = sp.vstack ? launch_decode<32, 1>(prm, w.n_ctas, sp.total, st)
-                               : launch_decode<32, 0>(prm, w.n_ctas, sp.total, st); break;
-        case 48: e = sp.vstack ? launch_decode<48, 1>(prm, w.n_ctas, sp.total, st)
-                               : launch_decode<48, 0>(prm, w.n_ctas, sp.total, st); break;
-        case 64: e = sp.vstack ? launch_decode<64, 1>(prm, w.n_ctas, sp.total, st)
-                               : launch_decode<64, 0>(prm, w.n_ctas, sp.total, st); break;
+        case 16: e = launch_decode<16>(prm, w.n_ctas, sp.total, st); break;
+        case 32: e = launch_decode<32>(prm, w.n_ctas, sp.total, st); break;
+        case 48: e = launch_decode<48>(prm, w.n_ctas, sp.total, st); break;
+        case 64: e = launch_decode<64>(prm, w.n_ctas, sp.total, st); break;
         default: e = cudaErrorInvalidValue;
     }
     timer_after(st);
