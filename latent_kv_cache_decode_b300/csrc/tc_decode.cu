@@ -441,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
     const int u0 = p.u_begin[cta], u1 = p.u_begin[cta + 1];
 
     if (threadIdx.x == 0) {
+        #pragma unroll 1
         for (int i = 0; i < kR; ++i) {
             ptx::mbar_init(&bar.kready[i], 1);
             ptx::mbar_init(&bar.vready[i], 1 + 128);
@@ -451,7 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         ptx::mbar_init(&bar.accfree[1], 128);
         ptx::mbar_init(&bar.drain[0], 1);
         ptx::mbar_init(&bar.drain[1], 1);
+        #pragma unroll 1
         for (int i = 0; i < 9; ++i) flag[i] = 0;
+        #pragma unroll 1
         for (int i = 0; i < kMaxSlots; ++i) owner[i] = -1;
         ptx::fence_mbar_init();
     }
@@ -474,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         // once the score MMAs of the previous piece are done; its bytes are part of
         // the kready phase of the piece's first tile.
         if (lane == 0) {
+            #pragma unroll 1
             for (int i = 0; i < 2 * kNumKinds; ++i)
                 if (p.rows[i >> 1] > 0) ptx::tma_prefetch_desc(&p.tm[i]);
             int pos = 0;                     // ring position of the next slot
@@ -508,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 const uint32_t par = ph_of(oj);
                 if (ptx::mbar_test(fb, par)) return;
                 const uint64_t t0 = ptx::globaltimer();
+                #pragma unroll 1
                 for (uint32_t spins = 1; !ptx::mbar_test(fb, par); ++spins) {
                     try_q(false);
                     if ((spins & 63u) == 0) {
@@ -525,6 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 const int ncols = ((part ? p.dv[k] : p.dk[k]) + 127) >> 7;
                 const int RBk = p.rb[k];
                 const int nc = ncols * RBk;   // slots: column chunks x row blocks
+                #pragma unroll 1
                 for (int c = 0; c < nc; ++c) slot_free((pos + c) % p.nslot);
                 const int jr = it.j % kR;
                 if (part == 0) {
@@ -547,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                     ptx::mbar_expect_tx(&bar.vready[jr], nc * kSlot);
                 }
                 uint64_t* rb = part ? &bar.vready[jr] : &bar.kready[jr];
+                #pragma unroll 1
                 for (int c = 0; c < nc; ++c) {
                     const int s = (pos + c) % p.nslot;
                     uint8_t* dst = ring + (size_t)s * kSlot;
@@ -568,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
             it.init(p, u0, u1);
             bool has_prev = false;
             int kiss = 0, viss = 0;   // tiles whose K / V loads were issued
+            #pragma unroll 1
             for (; it.valid() && !*abort_flag; it.next()) {
                 load(it, 0);
                 kiss = it.j + 1;
@@ -588,7 +596,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 // let copies still in flight land before the CTA winds down (bounded waits;
                 // a phase whose other arrivals never come just times out)
                 volatile int never = 0;
+                #pragma unroll 1
                 for (int j = max(0, kiss - kR / 2); j < kiss; ++j) ptx::mbar_wait(&bar.kready[j % kR], ph_of(j), &never);
+                #pragma unroll 1
                 for (int j = max(0, viss - kR / 2); j < viss; ++j) ptx::mbar_wait(&bar.vready[j % kR], ph_of(j), &never);
             }
         }
@@ -633,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                     const int ksteps = p.dk[0] >> 4;
                     const int nK = (p.dk[0] + 127) >> 7;
                     const int nfull = ksteps >> 3;   // whole 128-column chunks
+                    #pragma unroll 1
                     for (int c = 0; c < nfull; ++c) {
                         const int s = (pos + c) % p.nslot;
                         const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
@@ -650,6 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                         const int s = (pos + c) % p.nslot;
                         const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
                         const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
+                        #pragma unroll 1
                         for (int kk = 0; kk < ksteps - 8 * c; ++kk)
                             ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
                                           b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS_lat,
@@ -692,6 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 if (ti.pc.k == 0) {
                     const uint64_t pd = dB_P + (uint64_t)pboff;
                     const int nV = (p.dv[0] + 127) >> 7;
+                    #pragma unroll 1
                     for (int c = 0; c < nV; ++c) {
                         const int s = (pos + c) % p.nslot;
                         const uint64_t vd = dA_V + (uint64_t)((s * kSlot) >> 4);
@@ -727,6 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
             TileIter it, prev;
             it.init(p, u0, u1);
             bool has_prev = false;
+            #pragma unroll 1
             for (; it.valid(); it.next()) {
                 if (s_issuer) issue_S(it);
                 else pos = (pos + nslots(it, 0)) % p.nslot;
@@ -781,6 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
             }
             ptx::named_bar(1, 128);
             int jl = it.j;
+            #pragma unroll 1
             for (int n = 0; n < pc.n; ++n) {
                 const int t = it.t;
                 const int row0 = t * kTile * p.rb[k] + c.myrow;
@@ -818,11 +833,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         // a wait ran out: poison this CTA's partials so the result is NaN, not stale
         const int tid = threadIdx.x - 64;
         int npieces = 0;
+        #pragma unroll 1
         for (int u = u0; u < u1;) {
             const Piece pc = piece_at(p, u, u1);
             u += pc.n;
             ++npieces;
         }
+        #pragma unroll 1
         for (int i = tid; i < npieces * p.Hq; i += 128) {
             const int slot = p.slot_base[cta] + i / p.Hq;
             p.ml[((size_t)slot * 2 + 1) * p.Hq + (i % p.Hq)] = __int_as_float(0x7fc00000);
