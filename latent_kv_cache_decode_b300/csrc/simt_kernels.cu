@@ -203,6 +203,17 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
             *reinterpret_cast<uint4*>(img + ptx::sw128_offset(16 + i, u * 8, 32)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
     }
+    if (a.lat_img != nullptr && g == 0 && (a.hcn == 1 || rb % a.hcn == 0) && a.NP > a.Hq) {
+        // rows of absent heads (Hq <= h < NP) of the latent image are zero, so that the
+        // tensor-core path may treat every head column alike
+        const int npad = a.NP - a.Hq;
+        for (int idx = tid; idx < nb * npad * kQpCols; idx += kQpThreads) {
+            const int bl = idx / (npad * kQpCols), rem = idx - bl * npad * kQpCols;
+            const int h = a.Hq + rem / kQpCols, col = cb * kQpCols + rem % kQpCols;
+            uint8_t* img = a.lat_img + (size_t)(b0 + bl) * lat_img_bytes(a.NP, a.r_k);
+            *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(h, col, a.NP)) = __float2bfloat16_rn(0.f);
+        }
+    }
     if (a.U_K == nullptr) return;
     // q_lat block: 32 rows x 32 columns; thread = (column, group of 8 rows)
     const int c = tid & 31, rg = tid >> 5;

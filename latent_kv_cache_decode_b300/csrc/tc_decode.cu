@@ -30,12 +30,16 @@
 // Issuing few, wide MMAs matters: the issuing thread, not the tensor core, is the
 // limit for narrow ones.
 // m_ref is a lazy running maximum: it moves (and the TMEM accumulator is rescaled)
-// only when some score exceeds it by more than 2^8, which one warp vote per tile
-// detects; so most tiles need no cross-row reduction at all.
+// only when some score exceeds it by more than kLazy (log2 units), which one warp
+// vote per tile detects; so most tiles need no cross-row reduction at all.
 //
-// Roles (192 threads): warp 0 issues TMA loads into a ring of 32 KB slots, warp 1
-// issues the MMAs and owns TMEM, warps 2-5 (one per TMEM lane quadrant; thread =
-// tile row) run the softmax and write the partials.
+// Roles (224 threads): warp 0 issues TMA loads into a ring of 32 KB slots, warp 1
+// issues the score MMAs and owns TMEM, warp 6 issues the value MMAs, warps 2-5 (one
+// per TMEM lane quadrant; thread = tile row) run the softmax and write the partials.
+// The hot loops are kept small: with four roles running different code on one SM,
+// the instruction cache, not the arithmetic, limits a kernel whose loops the
+// compiler unrolls freely, so runtime-trip loops stay rolled and rare paths are
+// out of line.
 #include <cuda.h>
 #include <string.h>
 
@@ -150,6 +154,22 @@ struct TileIter {
     }
 };
 
+// Ring position s (< 2 n) modulo n.
+__device__ __forceinline__ int ring_wrap(int s, int n) { return s >= n ? s - n : s; }
+
+// Query operand image of a piece: the latent image of its batch element, or the raw
+// image of its (batch element, KV group).
+__device__ __forceinline__ void query_image(const TcParams& p, const Piece& pc, const uint8_t*& src,
+                                            uint32_t& bytes) {
+    if (pc.k == 0) {
+        src = p.lat_img + (size_t)pc.b * p.lat_img_bytes;
+        bytes = p.lat_img_bytes;
+    } else {
+        src = p.raw_img + ((size_t)pc.b * p.Hkv + pc.g) * p.raw_img_bytes;
+        bytes = p.raw_img_bytes;
+    }
+}
+
 // Barriers (all in shared memory), per tile j of the CTA, ring index j % kR:
 //   kready  K tile (and, for a piece's first tile, its query image) landed   [TMA tx]
 //   vready  V tile landed and P(j) written by the softmax warps             [TMA tx + 128 arrivals]
@@ -163,8 +183,9 @@ struct Bars {
     uint64_t* vfree;
     uint64_t* accfree;
     uint64_t* drain;
+    uint64_t* qready;   // the CTA's first query image landed                       [TMA tx]
 };
-__device__ __forceinline__ uint32_t ph_of(int j) { return (uint32_t)(j / kR) & 1u; }
+__device__ __forceinline__ uint32_t ph_of(int j) { return ((uint32_t)j / kR) & 1u; }
 
 // Shared state of the softmax warps.
 struct SoftCtx {
@@ -190,6 +211,46 @@ template <int NP> struct SBuf {
     static constexpr int PB = (NP > kNG * kRBRaw ? NP : kNG * kRBRaw) * 256;
 };
 
+// Scores of 16 heads of this thread's row: hi + lo parts (raw tiles) or one part.
+template <bool LO, int NS>
+__device__ __forceinline__ void load_scores(uint32_t tS, float (&x)[16]) {
+    if (LO) {
+        float lo[16];
+        ptx::tmem_ld16x2(tS, tS + NS, x, lo);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] += lo[i];
+    } else {
+        ptx::tmem_ld16(tS, x);
+    }
+}
+
+// Reduction across the 32 lanes of 16 values per lane, one result per value:
+// afterwards lane l holds the reduction of value l % 16 over all lanes. Butterfly that
+// halves the values per lane at each step (15 shuffles down to one value, then one
+// plain step across the two half-warps).
+template <bool MAX>
+__device__ __forceinline__ float warp_reduce16(float* v, int lane) {
+    constexpr int N = 16;
+#pragma unroll
+    for (int w = N / 2; w >= 1; w /= 2) {
+        const bool upper = (lane & w) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float send = upper ? v[i] : v[i + w];
+            const float keep = upper ? v[i + w] : v[i];
+            const float got = __shfl_xor_sync(0xffffffffu, send, w);
+            v[i] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int w = N; w < 32; w *= 2) {
+        const float got = __shfl_xor_sync(0xffffffffu, r, w);
+        r = MAX ? fmaxf(r, got) : r + got;
+    }
+    return r;
+}
+
 // The rare path of the softmax, kept out of line so that the hot loop stays small in
 // the instruction cache: a new reference maximum per head from this tile's scores,
 // the rescale factors alpha = exp2(m_old - m_new), and, when the accumulator already
@@ -198,36 +259,28 @@ template <int NP> struct SBuf {
 template <int NS, int NP, int RB, bool LO>
 __device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* alpha_s, uint64_t* vfree,
                                              volatile int* abort, uint32_t tS0, uint32_t t_acc_lane, int row0,
-                                             int rows, int nvalid, int j, int nMB, int aw, int tid,
-                                             int lane, int wq) {
+                                             int rows, int j, int nMB, int aw, int tid, int lane, int wq) {
+    // per-head maximum over this warp's valid rows, then over the four warps
+    float x[NS];
+#pragma unroll
+    for (int h = 0; h < NS; ++h) x[h] = -INFINITY;
+    // (the TMEM loads are warp-collective: every lane loads, invalid rows are masked after)
 #pragma unroll 1
+    for (int rb = 0; rb < RB; ++rb) {
+        const bool valid = row0 + rb * 128 < rows;
+        const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
+#pragma unroll
+        for (int hc = 0; hc < NS / 16; ++hc) {
+            float sc[16];
+            load_scores<LO, NS>(tS + hc * 16, sc);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[hc * 16 + i] = valid ? fmaxf(x[hc * 16 + i], sc[i]) : x[hc * 16 + i];
+        }
+    }
+#pragma unroll
     for (int hc = 0; hc < NS / 16; ++hc) {
-        float x[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = -INFINITY;
-#pragma unroll 1
-        for (int rb = 0; rb < RB; ++rb) {
-            const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
-            const bool valid = row0 + rb * 128 < rows;
-            float hi[16], lo[16];
-            if (LO) {
-                ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi, lo);
-            } else {
-                ptx::tmem_ld16(tS + hc * 16, hi);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) lo[i] = 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (valid && hc * 16 + i < nvalid) x[i] = fmaxf(x[i], hi[i] + lo[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float v = x[i];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0) red[wq * NP + hc * 16 + i] = v;
-        }
+        const float wmax = warp_reduce16<true>(x + hc * 16, lane);
+        if (lane < 16) red[wq * NP + hc * 16 + lane] = wmax;
     }
     ptx::named_bar(1, 128);
     if (tid < NS) {
@@ -259,14 +312,16 @@ __device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* 
     }
 }
 
-// Softmax of tile j of the current piece: RB row blocks of 128 rows, NS heads wide,
-// `nvalid` of them real; row0 is this thread's row index (segment-wide) in block 0.
-// Reads S^T from TMEM (block rb: hi scores at +rb*2NS, lo at +rb*2NS+NS), writes P
-// (hi, lo) as the MN-major B operand of the value MMA (16-head column blocks of
-// 128*RB rows x 32 bytes, 32-byte swizzle), then signals vready[j].
+// Softmax of tile j of the current piece: RB row blocks of 128 rows, NS heads wide;
+// row0 is this thread's row index (segment-wide) in block 0. Reads S^T from TMEM
+// (block rb at +rb*NS, or hi at +rb*2NS and lo at +rb*2NS+NS for raw tiles), writes P
+// as the MN-major B operand of the value MMA (16-head column blocks of 128*RB rows x
+// 32 bytes, 32-byte swizzle), then signals vready[j]. Every head column is processed
+// alike: the query rows of absent heads are zero, so their scores are finite and
+// their columns, which are never written out, cost no branches.
 template <int NS, int NP, int RB, bool LO>
 __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, int rows, bool has_prev,
-                                             int nvalid, float (&l_part)[NP], float (&mref)[NP]) {
+                                             float (&l_part)[NP], float (&mref)[NP]) {
     constexpr int SW = SBuf<NP>::W;
     const int jr = j % kR;
     ptx::mbar_wait(&c.bar.kfree[jr], ph_of(j), c.abort);   // S(j) complete
@@ -278,21 +333,15 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
 #pragma unroll
     for (int rb = 0; rb < RB; ++rb) {
         const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
-        const bool valid = row0 + rb * 128 < rows;
+        float dm = -INFINITY;
 #pragma unroll
         for (int hc = 0; hc < NS / 16; ++hc) {
-            float hi[16], lo[16];
-            if (LO) {
-                ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi, lo);
-            } else {
-                ptx::tmem_ld16(tS + hc * 16, hi);
+            float sc[16];
+            load_scores<LO, NS>(tS + hc * 16, sc);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) lo[i] = 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (valid && hc * 16 + i < nvalid) dmax = fmaxf(dmax, (hi[i] + lo[i]) - mref[hc * 16 + i]);
+            for (int i = 0; i < 16; ++i) dm = fmaxf(dm, sc[i] - mref[hc * 16 + i]);
         }
+        dmax = (row0 + rb * 128 < rows) ? fmaxf(dmax, dm) : dmax;
     }
     const bool any = __any_sync(0xffffffffu, dmax > kLazy);
     volatile int* fl = c.flags + (j & 1) * 4;
@@ -300,8 +349,7 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
     ptx::named_bar(1, 128);
     if (fl[0] | fl[1] | fl[2] | fl[3]) {
         softmax_new_ref<NS, NP, RB, LO>(c.red, c.m_ref_s, c.alpha_s, c.bar.vfree, c.abort, tS0, c.t_accp + c.lane_off,
-                                    row0, rows, nvalid, j, has_prev ? c.nMB : 0, c.aw, c.tid, c.lane,
-                                    c.wq);
+                                        row0, rows, j, has_prev ? c.nMB : 0, c.aw, c.tid, c.lane, c.wq);
 #pragma unroll
         for (int h = 0; h < NS; ++h) {
             mref[h] = c.m_ref_s[h];
@@ -309,8 +357,8 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
         }
     }
 
-    // pass 2: probabilities against the reference, as bf16 high + low parts; the P
-    // buffer (j & 1) is free once the value MMAs of tile j - 2 are done
+    // pass 2: probabilities against the reference, rounded to bf16; the P buffer
+    // (j & 1) is free once the value MMAs of tile j - 2 are done
     if (j >= 2) ptx::mbar_wait(&c.bar.vfree[(j - 2) % kR], ph_of(j - 2), c.abort);
     uint8_t* phi = c.pbuf + (j & 1) * SBuf<NP>::PB;
 #pragma unroll
@@ -322,34 +370,23 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
         const uint32_t sw = ((row >> 2) & 1) << 4;
 #pragma unroll
         for (int hc = 0; hc < NS / 16; ++hc) {
-            float hi_s[16], lo_s[16];
-            if (LO) {
-                ptx::tmem_ld16x2(tS + hc * 16, tS + NS + hc * 16, hi_s, lo_s);
-            } else {
-                ptx::tmem_ld16(tS + hc * 16, hi_s);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) lo_s[i] = 0.f;
-            }
-            float pr[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int h = hc * 16 + i;
-                pr[i] = 0.f;
-                if (h < nvalid) {   // uniform: padding heads need no exponential
-                    pr[i] = valid ? exp2f((hi_s[i] + lo_s[i]) - mref[h]) : 0.f;
-                    l_part[h] += pr[i];
-                }
-            }
-            uint32_t hi[8];
+            float sc[16];
+            load_scores<LO, NS>(tS + hc * 16, sc);
+            uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[2 * i], pr[2 * i + 1]);
-                hi[i] = *reinterpret_cast<const uint32_t*>(&h2);
+                const int h = hc * 16 + 2 * i;
+                const float p0 = valid ? exp2f(sc[2 * i] - mref[h]) : 0.f;
+                const float p1 = valid ? exp2f(sc[2 * i + 1] - mref[h + 1]) : 0.f;
+                l_part[h] += p0;
+                l_part[h + 1] += p1;
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
             }
             const uint32_t o0 = hc * (kPAtom * RB) + row_off + (0u ^ sw);
             const uint32_t o1 = hc * (kPAtom * RB) + row_off + (16u ^ sw);
-            *reinterpret_cast<uint4*>(phi + o0) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(phi + o1) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+            *reinterpret_cast<uint4*>(phi + o0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(phi + o1) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
     }
     ptx::tc_fence_before();          // TMEM reads / writes of this tile before the signal
@@ -359,7 +396,7 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
 
 // Partial write-out of a piece, out of line (once per piece): (m, l) of the piece's
 // real heads from the per-warp row-sum reductions in `red`, and the accumulator
-// columns (hi + lo parts when side by side) read from TMEM.
+// columns read from TMEM.
 template <int NS, int NP>
 __device__ __noinline__ void write_partial_acc(float* ml, float* acc, int* kindp, const float* red,
                                                const float* m_ref_s, int Hq, int Dmax, int slot, int kind, int h0,
@@ -394,13 +431,14 @@ __device__ __noinline__ void write_partial_acc(float* ml, float* acc, int* kindp
 // the piece's real heads to partial slot `slot`.
 template <int NS, int NP>
 __device__ __forceinline__ void write_partial(const TcParams& p, const SoftCtx& c, int slot, int kind,
-                                              int h0, int nvalid, int dv, const float (&l_part)[NP]) {
+                                              int h0, int nvalid, int dv, float (&l_part)[NP]) {
+    float v[NS];
 #pragma unroll
-    for (int h = 0; h < NS; ++h) {
-        float v = l_part[h];
+    for (int h = 0; h < NS; ++h) v[h] = l_part[h];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (c.lane == 0) c.red[c.wq * NP + h] = v;
+    for (int hc = 0; hc < NS / 16; ++hc) {
+        const float wsum = warp_reduce16<false>(v + hc * 16, c.lane);
+        if (c.lane < 16) c.red[c.wq * NP + hc * 16 + c.lane] = wsum;
     }
     ptx::named_bar(1, 128);
     write_partial_acc<NS, NP>(p.ml, p.acc, p.kind, c.red, c.m_ref_s, p.Hq, p.Dmax, slot, kind, h0, nvalid, dv, c.nMB,
@@ -435,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
     bar.vfree = bars + 3 * kR;
     bar.accfree = bars + 4 * kR;
     bar.drain = bars + 4 * kR + 2;      // [0] score issuer, [1] value issuer
+    bar.qready = bars + 4 * kR + 4;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
@@ -452,6 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         ptx::mbar_init(&bar.accfree[1], 128);
         ptx::mbar_init(&bar.drain[0], 1);
         ptx::mbar_init(&bar.drain[1], 1);
+        ptx::mbar_init(bar.qready, 1);
         #pragma unroll 1
         for (int i = 0; i < 9; ++i) flag[i] = 0;
         #pragma unroll 1
@@ -473,32 +513,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
         // Ring loads in the order the MMAs consume them: K(0), K(1), V(0), K(2), V(1),
-        // ..., V(n-1). A piece's query image is copied into the single query buffer
-        // once the score MMAs of the previous piece are done; its bytes are part of
-        // the kready phase of the piece's first tile.
+        // ..., V(n-1) (keys run at most two tiles ahead of values). A piece's query
+        // image is copied into the single query buffer once the score MMAs of the
+        // previous piece are done (the CTA's first image is copied by the score
+        // issuer, so that the key and value loads need not wait for the preceding
+        // kernel); its bytes are part of the kready phase of the piece's first tile.
         if (lane == 0) {
-            #pragma unroll 1
+#pragma unroll 1
             for (int i = 0; i < 2 * kNumKinds; ++i)
                 if (p.rows[i >> 1] > 0) ptx::tma_prefetch_desc(&p.tm[i]);
             int pos = 0;                     // ring position of the next slot
             const uint64_t pol = ptx::policy_evict_first();   // the cache is streamed once
             bool pdl_done = false;
-            // pending query-image copy
+            // pending query-image copy (pieces after the first)
             bool q_pend = false;
-            int q_tile = 0, q_after = -1;    // kready tile; tile whose score MMAs must finish first
+            int q_tile = 0, q_after = 0;     // kready tile; tile whose score MMAs must finish first
             const uint8_t* q_src = nullptr;
             uint32_t q_bytes = 0;
             auto try_q = [&](bool block) {
                 if (!q_pend) return;
-                if (q_after < 0) {
-                    if (!pdl_done) {
-                        pdl_wait();          // the images come from the preceding kernel
-                        pdl_done = true;
-                    }
-                } else if (block) {
+                if (block) {
                     ptx::mbar_wait(&bar.kfree[q_after % kR], ph_of(q_after), abort_flag);
                 } else if (!ptx::mbar_test(&bar.kfree[q_after % kR], ph_of(q_after))) {
                     return;
+                }
+                if (!pdl_done) {
+                    pdl_wait();              // the images come from the preceding kernel
+                    pdl_done = true;
                 }
                 ptx::bulk_load(qbuf, q_src, q_bytes, &bar.kready[q_tile % kR]);
                 q_pend = false;
@@ -512,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 const uint32_t par = ph_of(oj);
                 if (ptx::mbar_test(fb, par)) return;
                 const uint64_t t0 = ptx::globaltimer();
-                #pragma unroll 1
+#pragma unroll 1
                 for (uint32_t spins = 1; !ptx::mbar_test(fb, par); ++spins) {
                     try_q(false);
                     if ((spins & 63u) == 0) {
@@ -524,81 +565,68 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                     }
                 }
             };
-            auto load = [&](const TileIter& it, int part) {
-                const int k = it.pc.k;
+            TileIter kit, vit;
+            kit.init(p, u0, u1);
+            vit.init(p, u0, u1);
+            int kiss = 0, viss = 0;   // tiles whose K / V loads were issued
+#pragma unroll 1
+            while (vit.valid() && !*abort_flag) {
+                const bool isK = kit.valid() && kit.j <= vit.j + 1;
+                TileIter ti = isK ? kit : vit;
+                const int part = isK ? 0 : 1;
+                const int k = ti.pc.k;
                 const CUtensorMap* tm = &p.tm[2 * k + part];
                 const int ncols = ((part ? p.dv[k] : p.dk[k]) + 127) >> 7;
                 const int RBk = p.rb[k];
                 const int nc = ncols * RBk;   // slots: column chunks x row blocks
-                #pragma unroll 1
-                for (int c = 0; c < nc; ++c) slot_free((pos + c) % p.nslot);
-                const int jr = it.j % kR;
+#pragma unroll 1
+                for (int c = 0; c < nc; ++c) slot_free(ring_wrap(pos + c, p.nslot));
+                const int jr = ti.j % kR;
                 if (part == 0) {
-                    if (it.first()) {
+                    if (ti.first() && ti.j > 0) {
                         if (q_pend) try_q(true);   // the previous piece's image goes first
-                        q_pend = true;
-                        q_tile = it.j;
-                        q_after = it.j - 1;        // -1 for the CTA's first piece
-                        if (k == 0) {
-                            q_src = p.lat_img + (size_t)it.pc.b * p.lat_img_bytes;
-                            q_bytes = p.lat_img_bytes;
-                        } else {
-                            q_src = p.raw_img + ((size_t)it.pc.b * p.Hkv + it.pc.g) * p.raw_img_bytes;
-                            q_bytes = p.raw_img_bytes;
-                        }
+                        query_image(p, ti.pc, q_src, q_bytes);
                         ptx::mbar_expect_tx_only(&bar.kready[jr], q_bytes);
+                        q_pend = true;
+                        q_tile = ti.j;
+                        q_after = ti.j - 1;
                     }
                     ptx::mbar_expect_tx(&bar.kready[jr], nc * kSlot);
                 } else {
                     ptx::mbar_expect_tx(&bar.vready[jr], nc * kSlot);
                 }
                 uint64_t* rb = part ? &bar.vready[jr] : &bar.kready[jr];
-                #pragma unroll 1
+#pragma unroll 1
                 for (int c = 0; c < nc; ++c) {
-                    const int s = (pos + c) % p.nslot;
+                    const int s = ring_wrap(pos + c, p.nslot);
                     uint8_t* dst = ring + (size_t)s * kSlot;
                     const int col = (c % ncols) * 128;
-                    const int row = (it.t * RBk + c / ncols) * kTile;
+                    const int row = (ti.t * RBk + c / ncols) * kTile;
                     if (k == 0) {
-                        ptx::tma_load_3d_hint(dst, tm, col, row, it.pc.b, rb, pol);
-                        ptx::tma_load_3d_hint(dst + kBox, tm, col + 64, row, it.pc.b, rb, pol);
+                        ptx::tma_load_3d_hint(dst, tm, col, row, ti.pc.b, rb, pol);
+                        ptx::tma_load_3d_hint(dst + kBox, tm, col + 64, row, ti.pc.b, rb, pol);
                     } else {
-                        ptx::tma_load_4d_hint(dst, tm, col, it.pc.g, row, it.pc.b, rb, pol);
-                        ptx::tma_load_4d_hint(dst + kBox, tm, col + 64, it.pc.g, row, it.pc.b, rb, pol);
+                        ptx::tma_load_4d_hint(dst, tm, col, ti.pc.g, row, ti.pc.b, rb, pol);
+                        ptx::tma_load_4d_hint(dst + kBox, tm, col + 64, ti.pc.g, row, ti.pc.b, rb, pol);
                     }
-                    owner[s] = (it.j << 1) | part;
+                    owner[s] = (ti.j << 1) | part;
                 }
-                pos = (pos + nc) % p.nslot;
+                pos = ring_wrap(pos + nc, p.nslot);
                 try_q(false);
-            };
-            TileIter it, prev;
-            it.init(p, u0, u1);
-            bool has_prev = false;
-            int kiss = 0, viss = 0;   // tiles whose K / V loads were issued
-            #pragma unroll 1
-            for (; it.valid() && !*abort_flag; it.next()) {
-                load(it, 0);
-                kiss = it.j + 1;
-                if (has_prev) {
-                    load(prev, 1);
-                    viss = prev.j + 1;
-                }
-                prev = it;
-                has_prev = true;
-            }
-            if (has_prev && !*abort_flag) {
-                load(prev, 1);
-                viss = prev.j + 1;
+                if (isK) kiss = ti.j + 1;
+                else viss = ti.j + 1;
+                ti.next();
+                if (isK) kit = ti;
+                else vit = ti;
             }
             try_q(true);
-            if (!pdl_done) pdl_wait();
             if (*abort_flag) {
                 // let copies still in flight land before the CTA winds down (bounded waits;
                 // a phase whose other arrivals never come just times out)
                 volatile int never = 0;
-                #pragma unroll 1
+#pragma unroll 1
                 for (int j = max(0, kiss - kR / 2); j < kiss; ++j) ptx::mbar_wait(&bar.kready[j % kR], ph_of(j), &never);
-                #pragma unroll 1
+#pragma unroll 1
                 for (int j = max(0, viss - kR / 2); j < viss; ++j) ptx::mbar_wait(&bar.vready[j % kR], ph_of(j), &never);
             }
         }
@@ -607,7 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         // Two issuing threads: warp 1 issues the score MMAs, warp 6 the value MMAs, so
         // the two streams do not wait for each other. Per tile each issues after one
         // wait and ends with one commit; waits and commits stall an issuing thread
-        // behind the tensor core's in-flight operand reads, so they are kept few.
+        // behind the tensor core's in-flight operand reads, so they are kept few. Both
+        // walk the producer's sequence of tile parts to track ring positions.
         const bool s_issuer = warp == 1;
         if (lane == 0) {
             const uint32_t idS_lat = ptx::idesc_bf16(128, NP, false, false);
@@ -623,11 +652,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
             const uint64_t dB_Pr = ptx::sdesc_sw32(ptx::smem_u32(pbuf), kPAtom * kRBRaw, 256);  // P (raw)
             int pos = 0;   // ring position, same sequence as the producer
 
-            // ring slots of a tile's keys / values (same walk as the producer)
-            auto nslots = [&](const TileIter& ti, int part) {
-                const int k = ti.pc.k;
-                return (((part ? p.dv[k] : p.dk[k]) + 127) >> 7) * p.rb[k];
-            };
             auto issue_S = [&](const TileIter& ti) {
                 const int jr = ti.j % kR;
                 if (ti.j >= 2) {
@@ -643,9 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                     const int ksteps = p.dk[0] >> 4;
                     const int nK = (p.dk[0] + 127) >> 7;
                     const int nfull = ksteps >> 3;   // whole 128-column chunks
-                    #pragma unroll 1
+#pragma unroll 1
                     for (int c = 0; c < nfull; ++c) {
-                        const int s = (pos + c) % p.nslot;
+                        const int s = ring_wrap(pos + c, p.nslot);
                         const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
                         const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
                         const uint32_t acc0 = c != 0 ? 1u : 0u;
@@ -658,22 +682,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                     if (nfull < nK) {
                         // a last, partial chunk (key width not a multiple of 128)
                         const int c = nfull;
-                        const int s = (pos + c) % p.nslot;
+                        const int s = ring_wrap(pos + c, p.nslot);
                         const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
                         const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
-                        #pragma unroll 1
+#pragma unroll 1
                         for (int kk = 0; kk < ksteps - 8 * c; ++kk)
                             ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
                                           b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS_lat,
                                           (c | kk) != 0 ? 1u : 0u);
                     }
-                    pos = (pos + nK) % p.nslot;
+                    pos = ring_wrap(pos + nK, p.nslot);
                 } else {
                     // raw tile: kRBRaw blocks of 128 tokens of one KV head, key width d = 128
                     const uint32_t qstride = 2 * kNG * 128 >> 4;
 #pragma unroll
                     for (int rb = 0; rb < kRBRaw; ++rb) {
-                        const int s = (pos + rb) % p.nslot;
+                        const int s = ring_wrap(pos + rb, p.nslot);
                         const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
@@ -681,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                                           dB_Q + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS_raw,
                                           kk == 0 ? 0u : 1u);
                     }
-                    pos = (pos + kRBRaw) % p.nslot;
+                    pos = ring_wrap(pos + kRBRaw, p.nslot);
                 }
                 ptx::mma_commit(&bar.kfree[jr]);
             };
@@ -704,9 +728,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 if (ti.pc.k == 0) {
                     const uint64_t pd = dB_P + (uint64_t)pboff;
                     const int nV = (p.dv[0] + 127) >> 7;
-                    #pragma unroll 1
+#pragma unroll 1
                     for (int c = 0; c < nV; ++c) {
-                        const int s = (pos + c) % p.nslot;
+                        const int s = ring_wrap(pos + c, p.nslot);
                         const uint64_t vd = dA_V + (uint64_t)((s * kSlot) >> 4);
                         const uint32_t d0 = abase + c * aw;
 #pragma unroll
@@ -716,13 +740,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                             ptx::mma_bf16(d0, a, b, idV_lat, kk == 0 ? acc0 : 1u);
                         }
                     }
-                    pos = (pos + nV) % p.nslot;
+                    pos = ring_wrap(pos + nV, p.nslot);
                 } else {
                     // 256 tokens: k-steps 0-7 from block 0's slot, 8-15 from block 1's
                     const uint64_t pd = dB_Pr + (uint64_t)pboff;
 #pragma unroll
                     for (int rb = 0; rb < kRBRaw; ++rb) {
-                        const int s = (pos + rb) % p.nslot;
+                        const int s = ring_wrap(pos + rb, p.nslot);
                         const uint64_t vd = dA_V + (uint64_t)((s * kSlot) >> 4);
                         const uint32_t accr = rb == 0 ? acc0 : 1u;
 #pragma unroll
@@ -732,26 +756,40 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                             ptx::mma_bf16(abase, a, b, idV_raw, kk == 0 ? accr : 1u);
                         }
                     }
-                    pos = (pos + kRBRaw) % p.nslot;
+                    pos = ring_wrap(pos + kRBRaw, p.nslot);
                 }
                 ptx::mma_commit(&bar.vfree[jr]);
             };
 
-            TileIter it, prev;
-            it.init(p, u0, u1);
-            bool has_prev = false;
-            #pragma unroll 1
-            for (; it.valid(); it.next()) {
-                if (s_issuer) issue_S(it);
-                else pos = (pos + nslots(it, 0)) % p.nslot;
-                if (has_prev) {
-                    if (!s_issuer) issue_V(prev);
-                    else pos = (pos + nslots(prev, 1)) % p.nslot;
-                }
-                prev = it;
-                has_prev = true;
+            TileIter kit, vit;
+            kit.init(p, u0, u1);
+            vit.init(p, u0, u1);
+            if (s_issuer && kit.valid()) {
+                // the CTA's first query image, once the preceding kernel has written it
+                // (its own barrier: the key and value loads never wait for it)
+                const uint8_t* q_src;
+                uint32_t q_bytes;
+                query_image(p, kit.pc, q_src, q_bytes);
+                pdl_wait();
+                ptx::mbar_expect_tx(bar.qready, q_bytes);
+                ptx::bulk_load(qbuf, q_src, q_bytes, bar.qready);
+                ptx::mbar_wait(bar.qready, 0, abort_flag);
             }
-            if (has_prev && !s_issuer) issue_V(prev);
+#pragma unroll 1
+            while (vit.valid()) {
+                const bool isK = kit.valid() && kit.j <= vit.j + 1;
+                TileIter ti = isK ? kit : vit;
+                if (isK == s_issuer) {
+                    if (isK) issue_S(ti);
+                    else issue_V(ti);
+                } else {
+                    const int k = ti.pc.k;
+                    pos = ring_wrap(pos + (((isK ? p.dk[k] : p.dv[k]) + 127) >> 7) * p.rb[k], p.nslot);
+                }
+                ti.next();
+                if (isK) kit = ti;
+                else vit = ti;
+            }
             ptx::mma_commit(&bar.drain[s_issuer ? 0 : 1]);   // arrives once this thread's MMAs completed
         }
     } else {
@@ -800,8 +838,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 const int t = it.t;
                 const int row0 = t * kTile * p.rb[k] + c.myrow;
                 jl = it.j;
-                if (lat) softmax_tile<NP, NP, 1, false>(c, it.j, row0, p.rows[k], t > pc.t0, nvalid, l_part, mref);
-                else softmax_tile<kNG, NP, kRBRaw, true>(c, it.j, row0, p.rows[k], t > pc.t0, nvalid, l_part, mref);
+                if (lat) softmax_tile<NP, NP, 1, false>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref);
+                else softmax_tile<kNG, NP, kRBRaw, true>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref);
                 it.next();
             }
             // ---- partial of (CTA, piece): reference max, row sum and accumulator
@@ -825,6 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
             volatile int never = 0;
             ptx::mbar_wait(&bar.drain[0], 0, &never);   // every MMA of this CTA has completed
             ptx::mbar_wait(&bar.drain[1], 0, &never);
+            if (u0 < u1) ptx::mbar_wait(bar.qready, 0, &never);   // the first query copy has landed
         }
         __syncwarp();
         ptx::tmem_dealloc(tmem, p.tmem_cols);
@@ -890,7 +929,7 @@ SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], con
     // query buffer: the latent image (NP rows, bf16) or a raw image (hi and lo parts of kNG heads)
     const int q_bytes = std::max(rows[0] > 0 ? s.NP * round_up(dk[0], 64) * 2 : 0, 2 * kNG * 128 * 2);
     const int p_bytes = 2 * std::max(s.NP, kNG * kRBRaw) * 256;   // two P buffers (bf16)
-    const int nbars = 4 * kR + 4;
+    const int nbars = 4 * kR + 5;
     const int misc_bytes = (6 * s.NP + 32) * 4;
     const int avail = kSmemMax - q_bytes - p_bytes - round_up(nbars * 8, 16) - misc_bytes - 1024;
     s.nslot = std::min(kMaxSlots, avail / kSlot);

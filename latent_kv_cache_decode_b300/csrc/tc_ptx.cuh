@@ -68,8 +68,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Wait until the phase with the given parity has completed. Returns false if the
 // wait ran past kWaitLimitNs (then *abort is set) or *abort was raised elsewhere.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The first probe is inline; the bounded spin is out of line, so that the many wait
+// sites of a kernel share one copy of it in the instruction cache.
+static __device__ __noinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -81,6 +82,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
             }
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_spin(bar, parity, abort);
 }
 
 // ------------------------------------------------------------------- TMA
