@@ -51,16 +51,21 @@ __device__ __forceinline__ float warp_sum(float v) {
 // latent space per GQA group, q_lat[b,h,:] = RoPE(q[b,h]) . U_K^(g) (the
 // projection is taken after grouping, so U_K^(g) serves the G heads of group g).
 //
-// Grid (Hkv, column blocks of 32 latent columns, row blocks). A row is one
+// Grid (Hkv, column blocks of 16 latent columns, row blocks). A row is one
 // (batch element, head of group g) pair; a CTA holds at most 32 rows: `nbb`
 // whole batch elements when G <= 32, else one 32-head chunk of one element.
 // The rotation angle p * theta_i is reduced modulo one turn exactly with 64-bit
 // fixed-point arithmetic (turn[i] = theta_i / 2pi), then sin/cos of the reduced
 // angle are taken in float32; both outputs are scaled by scale * log2(e).
+//
+// Ordering with neighbouring kernels: only the U_K block (a weight) is read before
+// the grid-dependency wait; q and q_pos, which the preceding kernel may write, are
+// read after it, and dependents are released only after it, so a dependent kernel
+// may read anything the preceding kernels wrote (the caches) without a wait of its own.
 // ---------------------------------------------------------------------------
 constexpr int kQpRows = 32;
-constexpr int kQpCols = 32;
-constexpr int kQpThreads = 128;
+constexpr int kQpCols = 16;
+constexpr int kQpThreads = 256;
 
 // 16-byte vector of storage elements: 8 bf16 or 4 float32.
 template <typename T> struct Vec16;
@@ -88,11 +93,11 @@ template <> struct Vec16<float> {
 
 template <typename T>
 __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant__ QprojArgs a) {
-    __shared__ __align__(16) float qr_s[kQpRows][128];   // query rows, rotated in place (scaled)
-    __shared__ float cs_s[kQpRows][64], sn_s[kQpRows][64];   // per batch element of the block
-    __shared__ __align__(16) float u_s[128][kQpCols];        // U_K^(g) column block
+    // query rows, rotated and scaled (row stride padded by 4 floats: the projection
+    // reads two rows per warp, which then fall in different banks)
+    __shared__ __align__(16) float qr_s[kQpRows][128 + 4];
+    __shared__ __align__(16) float u_s[128][kQpCols];   // U_K^(g) column block
     constexpr int VN = Vec16<T>::N;
-    pdl_trigger();
     const int g = blockIdx.x, cb = blockIdx.y, rb = blockIdx.z;
     const int tid = threadIdx.x;
     const int G = a.Hq / a.Hkv, d = a.d, half = d >> 1;
@@ -111,65 +116,47 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
     }
     const int ni = i1 - i0, rows = nb * ni;
 
-    // issue every global load of the block before using any of them
-    const int qv = d / VN;                                  // vectors per query row
-    const int nq = rows * qv;                               // <= 32 * 32
-    const int nu = a.U_K ? d * (kQpCols / VN) : 0;          // vectors of the U_K block
-    constexpr int kMaxLd = (32 * 32 + 128 * 8) / kQpThreads;   // 16
-    uint4 buf[kMaxLd];
+    // the U_K column block: a weight, read before the dependency wait
+    if (a.U_K != nullptr) {
+        constexpr int upr = kQpCols / VN;   // vectors per row of the block
+        for (int idx = tid; idx < d * upr; idx += kQpThreads) {
+            const int i = idx / upr, e = (idx - i * upr) * VN;
+            const uint4 v = *reinterpret_cast<const uint4*>((const T*)a.U_K + ((size_t)g * d + i) * a.r_k +
+                                                            cb * kQpCols + e);
+            float f[VN];
+            Vec16<T>::to_f(v, f);
 #pragma unroll
-    for (int k = 0; k < kMaxLd; ++k) {
-        const int idx = tid + k * kQpThreads;
-        if (idx < nq) {
-            const int r = idx / qv, e = (idx - r * qv) * VN;
-            const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
-            buf[k] = *reinterpret_cast<const uint4*>((const T*)a.q + ((size_t)(b0 + bl) * a.Hq + h) * d + e);
-        } else if (idx - nq < nu) {
-            const int j = idx - nq, i = j / (kQpCols / VN), e = (j - i * (kQpCols / VN)) * VN;
-            buf[k] = *reinterpret_cast<const uint4*>((const T*)a.U_K + ((size_t)g * d + i) * a.r_k +
-                                                     cb * kQpCols + e);
+            for (int k = 0; k < VN; ++k) u_s[i][e + k] = f[k];
         }
     }
-    // cos / sin of p * theta_i per batch element: the angle reduced to a signed
-    // fraction of a turn (exact 64-bit wrap-around), then sin / cos in float32
-    for (int idx = tid; idx < nb * half; idx += kQpThreads) {
-        const int bl = idx / half, i = idx - bl * half;
+    pdl_wait();       // q, q_pos and this workspace are free to read / write from here
+    pdl_trigger();
+
+    // load, rotate and scale the query rows: item = (row, VN-wide chunk of the first
+    // half); the thread loads both halves of the chunk and rotates them in registers
+    const int cph = half / VN;   // chunks per half row
+    for (int idx = tid; idx < rows * cph; idx += kQpThreads) {
+        const int r = idx / cph, e = (idx - r * cph) * VN;
+        const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
+        const T* src = (const T*)a.q + ((size_t)(b0 + bl) * a.Hq + h) * d;
+        const uint4 v1 = *reinterpret_cast<const uint4*>(src + e);
+        const uint4 v2 = *reinterpret_cast<const uint4*>(src + half + e);
         const unsigned long long pos = (unsigned long long)(long long)a.q_pos[b0 + bl];
-        const long long frac = (long long)(pos * a.turn[i]);
-        float sn, cs;
-        sincospif((float)frac * 1.0842021724855044e-19f, &sn, &cs);   // x 2^-63: half-turns
-        cs_s[bl][i] = cs;
-        sn_s[bl][i] = sn;
-    }
+        float x1[VN], x2[VN];
+        Vec16<T>::to_f(v1, x1);
+        Vec16<T>::to_f(v2, x2);
 #pragma unroll
-    for (int k = 0; k < kMaxLd; ++k) {
-        const int idx = tid + k * kQpThreads;
-        float f[VN];
-        if (idx < nq) {
-            const int r = idx / qv, e = (idx - r * qv) * VN;
-            Vec16<T>::to_f(buf[k], f);
-#pragma unroll
-            for (int v = 0; v < VN; ++v) qr_s[r][e + v] = f[v];
-        } else if (idx - nq < nu) {
-            const int j = idx - nq, i = j / (kQpCols / VN), e = (j - i * (kQpCols / VN)) * VN;
-            Vec16<T>::to_f(buf[k], f);
-#pragma unroll
-            for (int v = 0; v < VN; ++v) u_s[i][e + v] = f[v];
+        for (int k = 0; k < VN; ++k) {
+            // cos / sin of p * theta_i: the angle reduced to a signed fraction of a turn
+            // (exact 64-bit wrap-around), then sin / cos in float32
+            const long long frac = (long long)(pos * a.turn[e + k]);
+            float sn, cs;
+            sincospif((float)frac * 1.0842021724855044e-19f, &sn, &cs);   // x 2^-63: half-turns
+            qr_s[r][e + k] = (x1[k] * cs - x2[k] * sn) * a.scale_log2;
+            qr_s[r][half + e + k] = (x2[k] * cs + x1[k] * sn) * a.scale_log2;
         }
     }
     __syncthreads();
-    for (int idx = tid; idx < rows * half; idx += kQpThreads) {
-        const int r = idx / half, i = idx - r * half;
-        const int bl = r / ni;
-        const float x1 = qr_s[r][i], x2 = qr_s[r][i + half];
-        const float c = cs_s[bl][i], sn = sn_s[bl][i];
-        qr_s[r][i] = (x1 * c - x2 * sn) * a.scale_log2;
-        qr_s[r][i + half] = (x2 * c + x1 * sn) * a.scale_log2;
-    }
-    __syncthreads();
-    // the previous call's kernels may still read this workspace; every CTA waits
-    // (so this grid completes only after its predecessor) before writing it
-    pdl_wait();
     if (cb == 0 && a.q_rot != nullptr) {
         for (int idx = tid; idx < rows * (d / 4); idx += kQpThreads) {
             const int r = idx / (d / 4), e = (idx - r * (d / 4)) * 4;
@@ -179,7 +166,7 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
         }
     }
     if (cb == 0 && a.raw_img != nullptr) {
-        // raw image of (b, g): 32 rows x d, rows [0,16) high parts, [16,32) low parts of the
+        // raw image of (b, g): 32 rows x d, rows [0,16) high, [16,32) low parts of the
         // group's G (<= 16) heads; rows of absent heads are zero
         const size_t ib = raw_img_bytes(d);
         const int units = d / 8;
@@ -215,29 +202,29 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
         }
     }
     if (a.U_K == nullptr) return;
-    // q_lat block: 32 rows x 32 columns; thread = (column, group of 8 rows)
-    const int c = tid & 31, rg = tid >> 5;
-    float acc[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+    // q_lat block: 32 rows x 16 columns; thread = (column c, row pair rp)
+    const int c = tid & (kQpCols - 1), rp = tid / kQpCols;
+    const int r0 = 2 * rp, r1 = 2 * rp + 1;
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 4
     for (int i = 0; i < d; i += 4) {
+        const float4 qa = *reinterpret_cast<const float4*>(&qr_s[r0][i]);
+        const float4 qb = *reinterpret_cast<const float4*>(&qr_s[r1][i]);
         const float u0 = u_s[i][c], u1 = u_s[i + 1][c], u2 = u_s[i + 2][c], u3 = u_s[i + 3][c];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float4 q4 = *reinterpret_cast<const float4*>(&qr_s[rg * 8 + k][i]);
-            acc[k] = fmaf(q4.x, u0, fmaf(q4.y, u1, fmaf(q4.z, u2, fmaf(q4.w, u3, acc[k]))));
-        }
+        acc0 = fmaf(qa.x, u0, fmaf(qa.y, u1, fmaf(qa.z, u2, fmaf(qa.w, u3, acc0))));
+        acc1 = fmaf(qb.x, u0, fmaf(qb.y, u1, fmaf(qb.z, u2, fmaf(qb.w, u3, acc1))));
     }
     const int col = cb * kQpCols + c;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int r = rg * 8 + k;
+    for (int k = 0; k < 2; ++k) {
+        const int r = k ? r1 : r0;
+        const float v = k ? acc1 : acc0;
         if (r < rows) {
             const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
-            if (a.q_lat != nullptr) a.q_lat[((size_t)(b0 + bl) * a.Hq + h) * a.r_k + col] = acc[k];
+            if (a.q_lat != nullptr) a.q_lat[((size_t)(b0 + bl) * a.Hq + h) * a.r_k + col] = v;
             if (a.lat_img != nullptr) {
                 uint8_t* img = a.lat_img + (size_t)(b0 + bl) * lat_img_bytes(a.NP, a.r_k);
-                *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(h, col, a.NP)) = __float2bfloat16_rn(acc[k]);
+                *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(h, col, a.NP)) = __float2bfloat16_rn(v);
             }
         }
     }
@@ -369,28 +356,56 @@ __global__ void __launch_bounds__(128) simt_decode_kernel(SimtDecodeArgs a) {
 // memory round trips, not one per partial.
 // ---------------------------------------------------------------------------
 constexpr int kCombThreads = 256;
-constexpr int kCombBatch = 8;
+constexpr int kCombBatch = 16;
+constexpr int kCombPrefetchCols = 256;   // latent columns of U_V staged before the wait (bf16)
+
+// 16-byte asynchronous global -> shared copy (completion via cp_async_wait_all).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ptx::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+constexpr int kCombRowsPerWarp = 128 / (kCombThreads / 32);   // 16 output rows per warp (d <= 128)
 
 template <typename T>
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(const __grid_constant__ CombineArgs a) {
-    extern __shared__ float dyn[];   // lat: slot, weight; raw: slot, weight (each up to ns)
+    // per covering partial: slot, m, l (later the weight); latent and raw lists; then,
+    // for bf16 storage, U_V^(g)[:, 0:256) staged by asynchronous copies
+    extern __shared__ __align__(16) float dyn[];
     __shared__ __align__(16) float z_s[kMaxRank];
     __shared__ float y_s[128];
     __shared__ int n_lat_s, n_raw_s;
     __shared__ float L_s;
-    pdl_trigger();
     const int h = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = a.Hq / a.Hkv, g = h / G;
     const bool latent = a.U_V != nullptr;
-    pdl_wait();   // partials come from the decode kernel
+    constexpr int VN = Vec16<T>::N;
+    const int nrow = (a.d + (kCombThreads / 32) - 1) / (kCombThreads / 32);
+
     const int s0 = a.slot_begin[b], ns = a.slot_begin[b + 1] - s0;
+    // U_V^(g)[:, 0:256): a weight, copied before the dependency wait
+    const bool prefetch = latent && VN == 8;
+    T* u_stage = reinterpret_cast<T*>(dyn + ((6 * a.ns_max + 3) & ~3));
+    if (prefetch) {
+        const int cpr = min(a.r_v, kCombPrefetchCols) / 8;   // 16-byte chunks per row
+        for (int idx = tid; idx < a.d * cpr; idx += kCombThreads) {
+            const int i = idx / cpr, e = (idx - i * cpr) * 8;
+            cp_async16(u_stage + i * kCombPrefetchCols + e, (const T*)a.U_V + ((size_t)g * a.d + i) * a.r_v + e);
+        }
+        cp_async_commit();
+    }
+    pdl_trigger();
+    pdl_wait();   // partials come from the decode kernel
+
     int* lat_slot = reinterpret_cast<int*>(dyn);
-    float* lat_w = dyn + ns;
-    int* raw_slot = reinterpret_cast<int*>(dyn + 2 * ns);
-    float* raw_w = dyn + 3 * ns;
+    float* lat_m = dyn + ns;
+    float* lat_l = dyn + 2 * ns;
+    int* raw_slot = reinterpret_cast<int*>(dyn + 3 * ns);
+    float* raw_m = dyn + 4 * ns;
+    float* raw_l = dyn + 5 * ns;
     if (warp == 0) {
-        // compact the partials that cover head h, then their weights
+        // compact the partials that cover head h with their (m, l), one load each
         int nl = 0, nr = 0;
         float M = -INFINITY;
         for (int base = 0; base < ns; base += 32) {
@@ -410,28 +425,33 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const __grid_cons
             const unsigned br = __ballot_sync(0xffffffffu, use && is_raw);
             const unsigned below = (1u << lane) - 1u;
             if (use && is_lat) {
-                lat_slot[nl + __popc(bl & below)] = s0 + s;
-                lat_w[nl + __popc(bl & below)] = m;    // the max for now; weight below
+                const int o = nl + __popc(bl & below);
+                lat_slot[o] = s0 + s;
+                lat_m[o] = m;
+                lat_l[o] = l;
             }
             if (use && is_raw) {
-                raw_slot[nr + __popc(br & below)] = s0 + s;
-                raw_w[nr + __popc(br & below)] = m;
+                const int o = nr + __popc(br & below);
+                raw_slot[o] = s0 + s;
+                raw_m[o] = m;
+                raw_l[o] = l;
             }
             nl += __popc(bl);
             nr += __popc(br);
         }
         M = warp_max(M);
         __syncwarp();
+        // weights w = exp2(m - M) (stored over m) and L = sum w l
         float L = 0.f;
         for (int i = lane; i < nl; i += 32) {
-            const float w = exp2f(lat_w[i] - M);
-            L = fmaf(w, a.ml[((size_t)lat_slot[i] * 2 + 1) * a.Hq + h], L);
-            lat_w[i] = w;
+            const float w = exp2f(lat_m[i] - M);
+            L = fmaf(w, lat_l[i], L);
+            lat_m[i] = w;
         }
         for (int i = lane; i < nr; i += 32) {
-            const float w = exp2f(raw_w[i] - M);
-            L = fmaf(w, a.ml[((size_t)raw_slot[i] * 2 + 1) * a.Hq + h], L);
-            raw_w[i] = w;
+            const float w = exp2f(raw_m[i] - M);
+            L = fmaf(w, raw_l[i], L);
+            raw_m[i] = w;
         }
         L = warp_sum(L);
         if (lane == 0) {
@@ -457,8 +477,9 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const __grid_cons
         return acc;
     };
     if (latent)
-        for (int j = tid; j < a.r_v; j += kCombThreads) z_s[j] = accumulate(lat_slot, lat_w, nl, j);
-    for (int i = tid; i < a.d; i += kCombThreads) y_s[i] = accumulate(raw_slot, raw_w, nr, i);
+        for (int j = tid; j < a.r_v; j += kCombThreads) z_s[j] = accumulate(lat_slot, lat_m, nl, j);
+    for (int i = tid; i < a.d; i += kCombThreads) y_s[i] = accumulate(raw_slot, raw_m, nr, i);
+    if (prefetch) cp_async_wait_all();
     __syncthreads();
     const float invL = 1.f / L_s;
     if (!latent) {
@@ -467,38 +488,39 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const __grid_cons
     }
     // out[i] = (z . U_V^(g)[i, :] + y[i]) / L; a warp covers rows i = warp, warp + 8, ...
     // with lane l owning latent columns [8l, 8l + 8) of each 256-column chunk
-    constexpr int VN = Vec16<T>::N;
-    constexpr int kRowsPerWarp = 128 / (kCombThreads / 32);   // 16 (d <= 128)
-    const int nrow = (a.d + (kCombThreads / 32) - 1) / (kCombThreads / 32);
     for (int c0 = 0; c0 < a.r_v; c0 += 256) {
         const int j = c0 + lane * 8;
         float zl[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) zl[e] = (j + e < a.r_v) ? z_s[j + e] : 0.f;
-        float part[kRowsPerWarp];
+        float part[kCombRowsPerWarp];
 #pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) {
+        for (int r = 0; r < kCombRowsPerWarp; ++r) {
             part[r] = 0.f;
             const int i = warp + r * (kCombThreads / 32);
             if (r < nrow && i < a.d && j < a.r_v) {
-                const T* u = (const T*)a.U_V + ((size_t)g * a.d + i) * a.r_v + j;
                 float f[8];
+                if (prefetch && c0 == 0) {
+                    Vec16<T>::to_f(*reinterpret_cast<const uint4*>(u_stage + i * kCombPrefetchCols + j), f);
+                } else {
+                    const T* u = (const T*)a.U_V + ((size_t)g * a.d + i) * a.r_v + j;
 #pragma unroll
-                for (int q = 0; q < 8 / VN; ++q)
-                    Vec16<T>::to_f(*reinterpret_cast<const uint4*>(u + q * VN), f + q * VN);
+                    for (int q = 0; q < 8 / VN; ++q)
+                        Vec16<T>::to_f(*reinterpret_cast<const uint4*>(u + q * VN), f + q * VN);
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) part[r] = fmaf(zl[e], f[e], part[r]);
             }
         }
 #pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) {
+        for (int r = 0; r < kCombRowsPerWarp; ++r) {
             const float v = warp_sum(part[r]);
             const int i = warp + r * (kCombThreads / 32);
             if (lane == 0 && r < nrow && i < a.d) y_s[i] += v;
         }
     }
     __syncwarp();
-    for (int r = 0; r < kRowsPerWarp; ++r) {
+    for (int r = 0; r < kCombRowsPerWarp; ++r) {
         const int i = warp + r * (kCombThreads / 32);
         if (lane == 0 && r < nrow && i < a.d) a.out[((size_t)b * a.Hq + h) * a.d + i] = y_s[i] * invL;
     }
@@ -597,8 +619,16 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl) {
     int ns_max = 0;
     for (int b = 0; b < a.B; ++b) ns_max = std::max(ns_max, a.slot_begin[b + 1] - a.slot_begin[b]);
     if (ns_max > kMaxSlotsPerB) return cudaErrorInvalidValue;
-    const size_t smem = (size_t)ns_max * 4 * sizeof(float);
-    return launch_ex(combine_kernel<T>, dim3(a.Hq, a.B), dim3(kCombThreads), smem, st, pdl, a);
+    CombineArgs b = a;
+    b.ns_max = ns_max;
+    size_t smem = (size_t)((6 * ns_max + 3) & ~3) * sizeof(float);
+    if (a.U_V != nullptr && sizeof(T) == 2) smem += (size_t)a.d * kCombPrefetchCols * sizeof(T);
+    static std::atomic<unsigned long long> attr_done{0};
+    const cudaError_t e = set_max_smem_once(
+        (const void*)combine_kernel<T>,
+        (int)(((6 * kMaxSlotsPerB + 3) & ~3) * sizeof(float) + 128 * kCombPrefetchCols * sizeof(T)), attr_done);
+    if (e != cudaSuccess) return e;
+    return launch_ex(combine_kernel<T>, dim3(a.Hq, a.B), dim3(kCombThreads), smem, st, pdl, b);
 }
 
 template <typename T>

@@ -3,6 +3,8 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stdint.h>
 
 #include "../../include/slimkv.h"
@@ -80,6 +82,7 @@ struct SimtDecodeArgs {
 // Arguments of the split-combine kernel (merges partials, applies U_V^(g)T).
 struct CombineArgs {
     int B, Hq, Hkv, d, r_v, Dmax;
+    int ns_max;                  // most partial slots of one batch element (set by the launcher)
     const void* U_V;             // NULL when no latent partials exist
     const float* acc;
     const float* ml;
@@ -109,6 +112,19 @@ struct QprojArgs {
     float scale_log2;            // score scale * log2(e), folded into both outputs
     unsigned long long turn[64];
 };
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device, once
+// per device (`done` is the caller's bit mask of devices already set).
+inline cudaError_t set_max_smem_once(const void* func, int bytes, std::atomic<unsigned long long>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load() & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit);
+    return e;
+}
 
 // Events requested by slimkv_time_next_decode for the next call of this thread.
 struct DecodeTimer {

@@ -1112,13 +1112,9 @@ const WorkPlan& cached_plan(int B, const SegList& sl, int max_ctas) {
 
 template <int NP>
 cudaError_t launch_decode(const TcParams& prm, int grid, uint32_t smem, cudaStream_t st) {
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemMax);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::atomic<unsigned long long> attr_done{0};
+    const cudaError_t ea = set_max_smem_once((const void*)tc_decode_kernel<NP>, kSmemMax, attr_done);
+    if (ea != cudaSuccess) return ea;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
