@@ -33,6 +33,28 @@ METRIC = "decode-attn µs/step & HBM GB/s (frac of 8 TB/s), 128K ctx @16x, 1 B30
 NOMINAL_HBM_GBS = 8000.0
 
 
+def _measured_traffic(w, mode):
+    """DRAM bytes per decode launch from the committed ncu capture, or None.
+
+    The capture is only used while the decode kernel's sources are unchanged
+    since it was taken (hashes recorded beside it) and for the workload it was
+    taken on."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "tc_decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        for rel, digest in rec["source_sha256"].items():
+            with open(os.path.join(ROOT, rel), "rb") as src:
+                if hashlib.sha256(src.read()).hexdigest() != digest:
+                    return None
+    except (OSError, KeyError, ValueError):
+        return None
+    if mode != "latent" or not rec["workload"].startswith(w.name + ","):
+        return None
+    return rec["dram_bytes_read_per_launch"] + rec["dram_bytes_write_per_launch"]
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -327,7 +349,7 @@ def run_slimkv(args):
         "frac_of_measured_copy": cache_b / (ms * 1e-3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "kernel": "tc_decode_kernel", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": _measured_traffic(w, mode),
                      "launch_us": kern_avg_ms * 1e3, "bytes_per_launch": layer_bytes},
         "clocks": clk.summary(),
         "e2e": {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d,
