@@ -1009,6 +1009,12 @@ struct SegList {
     std::vector<std::pair<int, int>> segs;
 };
 
+// Fixed cost of a piece in tile-cost units (about 1.6 tiles): its first tile waits for
+// a query image and takes the rescale path, and its end waits for the last value MMAs
+// and writes a partial. The planner avoids splitting a segment across CTAs unless
+// that pays for itself.
+constexpr int kPieceCost = 8;
+
 WorkPlan make_plan(int B, const SegList& sl, int max_ctas) {
     // runs of equal-cost units in unit order (batch-major, then segment)
     int64_t total = 0, units = 0;
@@ -1020,65 +1026,65 @@ WorkPlan make_plan(int B, const SegList& sl, int max_ctas) {
             cmax = std::max(cmax, r.second);
         }
     const int G = (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, units));
-    // number of CTAs greedy packing needs with per-CTA budget T
-    auto count = [&](int64_t T) {
+    // Greedy packing with per-CTA budget T: a CTA takes units in order until the next
+    // one would exceed T; every piece (a CTA's run inside one segment) costs
+    // kPieceCost on top of its units. `visit(u, new_cta, new_piece, b)` sees every
+    // unit boundary where a CTA or a piece starts; returns the number of CTAs.
+    auto pack = [&](int64_t T, auto&& visit) {
         int ctas = 1;
-        int64_t cur = 0;
+        int64_t cur = 0, u = 0;
         for (int b = 0; b < B; ++b)
             for (auto& r : sl.segs) {
                 int n = r.first;
+                bool open = false;   // a piece of this segment is open in the current CTA
                 while (n > 0) {
+                    if (!open) {
+                        if (cur > 0 && cur + kPieceCost + r.second > T) {
+                            ++ctas;
+                            cur = 0;
+                            visit(u, true, b);
+                        } else {
+                            visit(u, false, b);
+                        }
+                        cur += kPieceCost;
+                        open = true;
+                    }
                     int64_t room = (T - cur) / r.second;
                     if (room == 0) {
                         ++ctas;
-                        cur = 0;
-                        room = T / r.second;
+                        cur = kPieceCost;
+                        visit(u, true, b);
+                        room = (T - cur) / r.second;
                     }
                     const int take = (int)std::min<int64_t>(n, room);
                     cur += (int64_t)take * r.second;
+                    u += take;
                     n -= take;
                 }
             }
         return ctas;
     };
-    int64_t lo = std::max<int64_t>(cmax, (total + G - 1) / G), hi = std::max<int64_t>(lo, total);
+    auto no_visit = [](int64_t, bool, int) {};
+    int64_t lo = std::max<int64_t>(cmax + kPieceCost, (total + G - 1) / G),
+            hi = std::max<int64_t>(lo, total + (int64_t)kPieceCost * B * (int64_t)sl.segs.size());
     while (lo < hi) {
         const int64_t mid = (lo + hi) / 2;
-        if (count(mid) <= G) hi = mid;
+        if (pack(mid, no_visit) <= G) hi = mid;
         else lo = mid + 1;
     }
     const int64_t T = lo;
     WorkPlan w;
-    w.u_begin.push_back(0);
-    // pieces: a CTA boundary or a segment boundary starts a new one
     std::vector<int> piece_cta;   // CTA of each piece, in unit order
     std::vector<int> piece_b;
-    int64_t cur = 0, u = 0;
-    bool fresh = true;
-    for (int b = 0; b < B; ++b)
-        for (auto& r : sl.segs) {
-            int n = r.first;
-            fresh = true;
-            while (n > 0) {
-                int64_t room = (T - cur) / r.second;
-                if (room == 0) {
-                    w.u_begin.push_back((int)u);
-                    cur = 0;
-                    room = T / r.second;
-                    fresh = true;
-                }
-                const int take = (int)std::min<int64_t>(n, room);
-                if (fresh) {
-                    piece_cta.push_back((int)w.u_begin.size() - 1);
-                    piece_b.push_back(b);
-                    fresh = false;
-                }
-                cur += (int64_t)take * r.second;
-                u += take;
-                n -= take;
-            }
-        }
-    w.u_begin.push_back((int)u);
+    w.u_begin.push_back(0);
+    bool first = true;
+    pack(T, [&](int64_t u, bool new_cta, int b) {
+        if (new_cta && !first) w.u_begin.push_back((int)u);
+        first = false;
+        piece_cta.push_back((int)w.u_begin.size() - 1);
+        piece_b.push_back(b);
+    });
+    w.u_begin.push_back((int)units);
     w.n_ctas = (int)w.u_begin.size() - 1;
     // slots in piece order: CTA i's pieces are consecutive, and batch b owns a
     // contiguous slot range because units are batch-major
