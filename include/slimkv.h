@@ -174,6 +174,23 @@ slimkv_status slimkv_decode_attn_noalloc(const slimkv_shape* shape, const void* 
                                          const void* U_K, const void* U_V,
                                          const int32_t* q_pos, float* out, void* stream);
 
+/* Multi-step decode: append the current token to the raw window before the
+ * layer's decode call. The decode rule keeps raw-window keys after RoPE ("RoPE ...
+ * on raw keys only", section "Latent-space attention removes the rebuild step"),
+ * so each new key is rotated once, here, at its own absolute position. The window
+ * is a ring of W slots: the token at position pos[b] goes to slot pos[b] mod W,
+ * replacing token pos[b] - W (the pages condense old raw tokens into beacons with
+ * trained projections; that step is outside this library). Attention does not
+ * depend on the order of window rows, so a later slimkv_decode_attn with
+ * q_pos = pos sees the last W tokens including the new one.
+ *   k_new, v_new  [B, Hkv, d]      the new token's key (before RoPE) and value
+ *   K_raw, V_raw  [B, W, Hkv, d]   the window (keys after RoPE), updated in place
+ *   pos           [B] int32        absolute positions, >= 0 (device)
+ * Uses shape->B, Hkv, d, W (>= 1), rope_base and dtype; the other fields are
+ * ignored. Pointers 16-byte aligned (pos 4-byte). Asynchronous on `stream`. */
+slimkv_status slimkv_append_kv(const slimkv_shape* shape, const void* k_new, const void* v_new,
+                               void* K_raw, void* V_raw, const int32_t* pos, void* stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char* slimkv_status_str(slimkv_status status);
 

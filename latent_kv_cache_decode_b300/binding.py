@@ -28,7 +28,7 @@ NOALLOC_SCRATCH_BYTES = 64 << 20   # SLIMKV_NOALLOC_SCRATCH_BYTES
 EXPORTS = ("slimkv_workspace_bytes", "slimkv_decode_attn", "slimkv_decode_attn_reconstruct",
            "slimkv_decode_attn_full_kv", "slimkv_status_str", "slimkv_abi_version",
            "slimkv_kernel_path", "slimkv_force_simt", "slimkv_time_next_decode",
-           "slimkv_decode_attn_noalloc")
+           "slimkv_decode_attn_noalloc", "slimkv_append_kv")
 
 
 class SlimkvError(RuntimeError):
@@ -68,6 +68,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.slimkv_decode_attn_full_kv.restype = ctypes.c_int
     lib.slimkv_decode_attn_noalloc.argtypes = [sp] + [vp] * 7 + [i32p, vp, vp]
     lib.slimkv_decode_attn_noalloc.restype = ctypes.c_int
+    lib.slimkv_append_kv.argtypes = [sp, vp, vp, vp, vp, i32p, vp]
+    lib.slimkv_append_kv.restype = ctypes.c_int
     lib.slimkv_status_str.argtypes = [ctypes.c_int]
     lib.slimkv_status_str.restype = ctypes.c_char_p
     lib.slimkv_abi_version.argtypes = []
@@ -95,6 +97,23 @@ def make_shape(B, Hq, Hkv, d, N_b, r_k, r_v, W, dtype, scale=None, rope_base=100
         scale = 1.0 / math.sqrt(d)
     code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
     return Shape(B, Hq, Hkv, d, N_b, r_k, r_v, W, scale, rope_base, code)
+
+
+_SHAPES: dict = {}
+
+
+def _shape_and_bytes(which: int, B, Hq, Hkv, d, N_b, r_k, r_v, W, dtype, scale, rope_base):
+    """(Shape, workspace bytes) for one argument signature, built once and reused:
+    a decode step calls the library once per layer with the same few signatures."""
+    key = (which, B, Hq, Hkv, d, N_b, r_k, r_v, W, dtype, scale, rope_base)
+    hit = _SHAPES.get(key)
+    if hit is None:
+        sh = make_shape(B, Hq, Hkv, d, N_b, r_k, r_v, W, dtype, scale, rope_base)
+        nb = int(load().slimkv_workspace_bytes(ctypes.byref(sh), which))
+        if len(_SHAPES) > 1024:
+            _SHAPES.clear()
+        hit = _SHAPES[key] = (sh, nb)
+    return hit
 
 
 def workspace_bytes(shape: Shape, which: int) -> int:
@@ -152,10 +171,13 @@ def decode_attn(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, *, scale=None, rope_
     Hkv = U_K.shape[0] // d if U_K is not None else K_raw.shape[2]
     r_k = C_K.shape[2] if C_K is not None else 0
     r_v = C_V.shape[2] if C_V is not None else 0
-    sh = shape or make_shape(B, Hq, Hkv, d, N_b, r_k, r_v, W, q.dtype, scale, rope_base)
+    if shape is not None:
+        sh = shape
+        nb = lib.slimkv_workspace_bytes(ctypes.byref(sh), SLIMKV_LATENT)
+    else:
+        sh, nb = _shape_and_bytes(SLIMKV_LATENT, B, Hq, Hkv, d, N_b, r_k, r_v, W, q.dtype, scale, rope_base)
     if out is None:
         out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
-    nb = lib.slimkv_workspace_bytes(ctypes.byref(sh), SLIMKV_LATENT)
     if nb == 0:
         _check(2, "slimkv_decode_attn")
     ws = (workspace or Workspace(q.device)).get(nb)
@@ -173,11 +195,10 @@ def decode_attn_reconstruct(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, *, scale
     lib = load()
     B, Hq, d = q.shape
     W = K_raw.shape[1] if K_raw is not None else 0
-    sh = make_shape(B, Hq, U_K.shape[0] // d, d, C_K.shape[1], C_K.shape[2], C_V.shape[2], W,
-                    q.dtype, scale, rope_base)
+    sh, nb = _shape_and_bytes(SLIMKV_RECONSTRUCT, B, Hq, U_K.shape[0] // d, d, C_K.shape[1], C_K.shape[2],
+                              C_V.shape[2], W, q.dtype, scale, rope_base)
     if out is None:
         out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
-    nb = lib.slimkv_workspace_bytes(ctypes.byref(sh), SLIMKV_RECONSTRUCT)
     if nb == 0:
         _check(2, "slimkv_decode_attn_reconstruct")
     ws = (workspace or Workspace(q.device)).get(nb)
@@ -194,10 +215,10 @@ def decode_attn_full_kv(q, K, V, q_pos, *, scale=None, rope_base=10000.0, out=No
     """slimkv_decode_attn_full_kv on torch CUDA tensors."""
     lib = load()
     B, Hq, d = q.shape
-    sh = make_shape(B, Hq, K.shape[2], d, 0, 0, 0, K.shape[1], q.dtype, scale, rope_base)
+    sh, nb = _shape_and_bytes(SLIMKV_FULL_KV, B, Hq, K.shape[2], d, 0, 0, 0, K.shape[1], q.dtype, scale,
+                              rope_base)
     if out is None:
         out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
-    nb = lib.slimkv_workspace_bytes(ctypes.byref(sh), SLIMKV_FULL_KV)
     if nb == 0:
         _check(2, "slimkv_decode_attn_full_kv")
     ws = (workspace or Workspace(q.device)).get(nb)
@@ -231,3 +252,15 @@ def decode_attn_noalloc(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, *, scale=Non
 
 def status_str(status: int) -> str:
     return load().slimkv_status_str(status).decode()
+
+
+def append_kv(k_new, v_new, K_raw, V_raw, pos, *, rope_base=10000.0, stream=None):
+    """slimkv_append_kv: the current token into the window ring (slot pos mod W),
+    its key rotated at pos. K_raw / V_raw [B, W, Hkv, d] are updated in place."""
+    lib = load()
+    B, W, Hkv, d = K_raw.shape
+    sh = make_shape(B, 1, 1, d, 0, 0, 0, W, K_raw.dtype, 1.0, rope_base)
+    sh.Hkv = Hkv
+    st = lib.slimkv_append_kv(ctypes.byref(sh), _ptr(k_new), _ptr(v_new), _ptr(K_raw), _ptr(V_raw), _ptr(pos),
+                              _stream(stream))
+    _check(st, "slimkv_append_kv")

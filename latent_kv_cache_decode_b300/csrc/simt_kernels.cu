@@ -564,6 +564,18 @@ __global__ void __launch_bounds__(256) simt_reconstruct_kernel(const T* __restri
 
 }  // namespace
 
+void rope_turns(double base, int d, unsigned long long (&turn)[64]) {
+    const long double two_pi = 6.283185307179586476925286766559L;
+    for (int i = 0; i < 64; ++i) {
+        turn[i] = 0;
+        if (i < d / 2) {
+            long double t = powl((long double)base, -2.0L * i / d) / two_pi;
+            t -= floorl(t);
+            turn[i] = (unsigned long long)(t * 18446744073709551616.0L + 0.5L);
+        }
+    }
+}
+
 template <typename T>
 cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* q_rot,
                          float* q_lat, int B, int Hq, int Hkv, int d, int r_k, double base,
@@ -592,16 +604,7 @@ cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* 
         a.nbb = 1;
         a.hcn = (G + kQpRows - 1) / kQpRows;
     }
-    // theta_i / (2 pi) as a fraction of a turn in 64-bit fixed point
-    const long double two_pi = 6.283185307179586476925286766559L;
-    for (int i = 0; i < 64; ++i) {
-        a.turn[i] = 0;
-        if (i < d / 2) {
-            long double t = powl((long double)base, -2.0L * i / d) / two_pi;
-            t -= floorl(t);
-            a.turn[i] = (unsigned long long)(t * 18446744073709551616.0L + 0.5L);
-        }
-    }
+    rope_turns(base, d, a.turn);
     const int row_blocks = (G <= kQpRows) ? (B + a.nbb - 1) / a.nbb : B * a.hcn;
     const int col_blocks = U_K ? r_k / kQpCols : 1;
     return launch_ex(qproj_kernel<T>, dim3(Hkv, col_blocks, row_blocks), dim3(kQpThreads), 0, st, pdl, a);

@@ -319,6 +319,30 @@ const char* slimkv_status_str(slimkv_status status) {
     return "unknown status";
 }
 
+slimkv_status slimkv_append_kv(const slimkv_shape* s, const void* k_new, const void* v_new, void* K_raw,
+                               void* V_raw, const int32_t* pos, void* stream) {
+    if (s == nullptr || k_new == nullptr || v_new == nullptr || K_raw == nullptr || V_raw == nullptr ||
+        pos == nullptr)
+        return SLIMKV_ERR_NULL;
+    if (s->dtype != SLIMKV_F32 && s->dtype != SLIMKV_BF16) return SLIMKV_ERR_DTYPE;
+    if (s->B < 1 || s->B > kMaxB || s->Hkv < 1 || s->Hkv > kMaxHq) return SLIMKV_ERR_SHAPE;
+    if (s->d != 64 && s->d != 128) return SLIMKV_ERR_SHAPE;
+    if (s->W < 1 || s->W > (1 << 24) || (int64_t)s->W * s->Hkv > (int64_t(1) << 28)) return SLIMKV_ERR_SHAPE;
+    if (!(s->rope_base > 0.0) || !isfinite(s->rope_base)) return SLIMKV_ERR_SHAPE;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(K_raw) || !aligned16(V_raw)) return SLIMKV_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(pos) & 3u) != 0) return SLIMKV_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (s->dtype == SLIMKV_F32)
+        e = launch_append_kv<float>((const float*)k_new, (const float*)v_new, (float*)K_raw, (float*)V_raw, pos,
+                                    s->B, s->Hkv, s->d, s->W, s->rope_base, st);
+    else
+        e = launch_append_kv<__nv_bfloat16>((const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new,
+                                            (__nv_bfloat16*)K_raw, (__nv_bfloat16*)V_raw, pos, s->B, s->Hkv,
+                                            s->d, s->W, s->rope_base, st);
+    return e == cudaSuccess ? SLIMKV_OK : SLIMKV_ERR_CUDA;
+}
+
 int slimkv_abi_version(void) { return SLIMKV_ABI_VERSION; }
 
 int slimkv_kernel_path(const slimkv_shape* shape, int which) { return select_path(shape, which); }

@@ -126,6 +126,15 @@ inline cudaError_t set_max_smem_once(const void* func, int bytes, std::atomic<un
     return e;
 }
 
+// theta_i / (2 pi) for i < d / 2 as a 64-bit fixed-point fraction of a turn
+// (theta_i = base^(-2i/d)); entries past d / 2 are zero.
+void rope_turns(double base, int d, unsigned long long (&turn)[64]);
+
+// Append the current token to the raw window ring (slot pos[b] mod W), key rotated at pos[b].
+template <typename T>
+cudaError_t launch_append_kv(const T* k_new, const T* v_new, T* K, T* V, const int32_t* pos, int B, int Hkv,
+                             int d, int W, double base, cudaStream_t st);
+
 // Events requested by slimkv_time_next_decode for the next call of this thread.
 struct DecodeTimer {
     cudaEvent_t start = nullptr, stop = nullptr;

@@ -33,7 +33,8 @@ import torch
 
 # tensor ids used as part of the per-tensor seed
 _TID = {"U_K": 0, "U_V": 1, "C_K": 2, "C_V": 3, "K_raw": 4, "V_raw": 5, "q": 6,
-        "peaks": 7, "ranks": 8, "K_full": 9, "V_full": 10}
+        "peaks": 7, "ranks": 8, "K_full": 9, "V_full": 10, "k_new": 11, "v_new": 12,
+        "q_step": 13}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -192,6 +193,24 @@ def layer_tensors(w: Workload, layer: int, batch: Optional[List[int]] = None,
         out["K_full"] = _store(np.stack(kf), w)
         out["V_full"] = _store(np.stack(vf), w)
     return out
+
+
+def decode_steps(w: Workload, layer: int, steps: int,
+                 batch: Optional[List[int]] = None) -> Dict[str, torch.Tensor]:
+    """CPU tensors (storage dtype) for ``steps`` generated tokens of one layer.
+
+    Keys: k_new, v_new [S,B,Hkv,d] (the new tokens' keys before RoPE and values),
+    q [S,B,Hq,d] and pos [S,B] int32. Token s sits at position q_pos + s, right
+    after the prompt window, whose tokens q_pos - W .. q_pos - 1 are taken to be
+    stored in slots (position mod W)."""
+    bs = list(range(w.B)) if batch is None else list(batch)
+    s = w.seed
+    kn = np.stack([_normal(_rng(s, layer, b, _TID["k_new"]), (steps, w.Hkv, w.d)) for b in bs], axis=1)
+    vn = np.stack([_normal(_rng(s, layer, b, _TID["v_new"]), (steps, w.Hkv, w.d)) for b in bs], axis=1)
+    qq = np.stack([_normal(_rng(s, layer, b, _TID["q_step"]), (steps, w.Hq, w.d)) for b in bs], axis=1)
+    pos = w.q_pos + np.arange(steps, dtype=np.int64)[:, None] + np.zeros((1, len(bs)), dtype=np.int64)
+    return {"k_new": _store(kn, w), "v_new": _store(vn, w), "q": _store(qq, w),
+            "pos": torch.from_numpy(pos.astype(np.int32))}
 
 
 def as_f64(t: torch.Tensor) -> np.ndarray:

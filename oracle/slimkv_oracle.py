@@ -156,3 +156,43 @@ def decode_attn_reconstruct(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, scale,
 def decode_attn_full_kv(q, K, V, q_pos, scale, rope_base, pairs=None):
     """Uncompressed GQA decode over a full RoPE'd cache (the speed baseline)."""
     return gqa_attn(q, K, V, q_pos, scale, rope_base, pairs=pairs)
+
+
+# ---------------------------------------------------------------------------
+# Multi-step decode: appending the current token to the raw window.
+#
+# The decode rule above keeps raw-window keys after RoPE. A generation loop
+# therefore rotates each new key once, at its own absolute position, when it is
+# appended. Reading taken here (the pages condense old raw tokens into beacons,
+# which needs trained projections and is out of scope): the window is a ring of W
+# slots, the token at absolute position p lives in slot p mod W, so appending
+# token p replaces token p - W. Attention is invariant to the order of the window
+# rows, so the ring order needs no bookkeeping.
+# ---------------------------------------------------------------------------
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 value, ties to even (the
+    storage rounding of a bf16 cache), returned as float64. bfloat16 keeps 8
+    significant bits: x = m 2^e with 0.5 <= |m| < 1 is rounded to a multiple of
+    2^(e-8); numpy's round is round-half-to-even."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.round(m * 256.0), e - 8)
+
+
+def append_kv(K_raw, V_raw, k_new, v_new, pos, rope_base, storage: str = "bf16"):
+    """Append the current token of every batch element to the raw window.
+
+    K_raw, V_raw [B, W, Hkv, d] (keys after RoPE); k_new, v_new [B, Hkv, d];
+    pos [B] absolute positions. Slot pos[b] mod W of batch element b receives
+    RoPE(k_new[b], pos[b]) and v_new[b], both rounded to the storage type
+    ("bf16" or "f32"). Returns new arrays; the inputs are not modified."""
+    K = np.array(K_raw, dtype=np.float64, copy=True)
+    V = np.array(V_raw, dtype=np.float64, copy=True)
+    W = K.shape[1]
+    rnd = round_bf16 if storage == "bf16" else (lambda a: np.asarray(a, np.float32).astype(np.float64))
+    for b in range(K.shape[0]):
+        slot = int(pos[b]) % W
+        K[b, slot] = rnd(rope(np.asarray(k_new[b], np.float64), float(pos[b]), rope_base))
+        V[b, slot] = rnd(np.asarray(v_new[b], np.float64))
+    return K, V

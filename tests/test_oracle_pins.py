@@ -320,3 +320,59 @@ def test_pins_catch_transposed_projection():
     out_bad = O.decode_attn(**c_bad)
     np.testing.assert_allclose(out_good, ref, rtol=1e-11, atol=1e-12)
     assert np.abs(out_bad - ref).max() > 1e-6
+
+
+# ---------------------------------------------------------------------------
+# Multi-step decode: bf16 storage rounding and the raw-window append
+# ---------------------------------------------------------------------------
+
+def test_round_bf16_matches_torch_on_float32_values():
+    # an independent implementation (torch's float32 -> bfloat16 conversion,
+    # round to nearest even) agrees on every float32 value, ties included
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(50000) * np.logspace(-4, 4, 50000)).astype(np.float32)
+    ties = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 3 * 2 ** -9 + 2 ** -17], np.float32)
+    x = np.concatenate([x, ties])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.round_bf16(x.astype(np.float64)), ref)
+    # ties go to the even neighbour
+    assert O.round_bf16(np.array([1 + 2 ** -8]))[0] == 1.0
+    assert O.round_bf16(np.array([1 + 3 * 2 ** -8]))[0] == 1 + 2 ** -6
+
+
+def test_append_writes_the_ring_slot_and_nothing_else():
+    rng = np.random.default_rng(12)
+    B, W, Hkv, d = 2, 5, 2, 8
+    K = rng.standard_normal((B, W, Hkv, d))
+    V = rng.standard_normal((B, W, Hkv, d))
+    kn = rng.standard_normal((B, Hkv, d))
+    vn = rng.standard_normal((B, Hkv, d))
+    pos = np.array([7, 10])   # slots 2 and 0
+    K2, V2 = O.append_kv(K, V, kn, vn, pos, 10000.0, storage="f32")
+    for b, slot in ((0, 2), (1, 0)):
+        other = [t for t in range(W) if t != slot]
+        assert np.array_equal(K2[b, other], K[b, other]) and np.array_equal(V2[b, other], V[b, other])
+        assert np.allclose(V2[b, slot], vn[b].astype(np.float32))
+    # W + 1 appends visit every slot once and then overwrite the first one
+    seen = [int(p) % W for p in range(13, 13 + W + 1)]
+    assert sorted(seen[:W]) == list(range(W)) and seen[W] == seen[0]
+
+
+def test_appended_key_scores_like_the_unrotated_pair():
+    # a query and a key at the same position: <R(p) q, R(p) k> = <q, k> for
+    # any p (rotations are orthogonal), so the score against the appended key is
+    # scale * q.k whatever the position; checked through the decode oracle with
+    # a single-token window, where the output must be that token's value
+    rng = np.random.default_rng(13)
+    B, Hq, Hkv, d = 1, 2, 1, 16
+    K = np.zeros((B, 1, Hkv, d))
+    V = np.zeros((B, 1, Hkv, d))
+    kn = rng.standard_normal((B, Hkv, d))
+    vn = rng.standard_normal((B, Hkv, d))
+    q = rng.standard_normal((B, Hq, d))
+    for p in (0, 1, 4097, 131072 + 2048):
+        K2, V2 = O.append_kv(K, V, kn, vn, np.array([p]), 500000.0, storage="f32")
+        qr = O.rope(q[0, 0], float(p), 500000.0)
+        assert abs(qr @ K2[0, 0, 0] - q[0, 0] @ kn[0, 0]) < 1e-5 * (1 + abs(q[0, 0] @ kn[0, 0]))
+        out = O.decode_attn(q, None, None, K2, V2, None, None, np.array([p]), 0.25, 500000.0)
+        assert np.allclose(out[0, 0], V2[0, 0, 0]) and np.allclose(out[0, 1], V2[0, 0, 0])
