@@ -607,6 +607,9 @@ cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* 
     rope_turns(base, d, a.turn);
     const int row_blocks = (G <= kQpRows) ? (B + a.nbb - 1) / a.nbb : B * a.hcn;
     const int col_blocks = U_K ? r_k / kQpCols : 1;
+    static std::atomic<unsigned long long> attr_done{0};
+    const cudaError_t e = set_max_smem_once((const void*)qproj_kernel<T>, 0, attr_done);
+    if (e != cudaSuccess) return e;
     return launch_ex(qproj_kernel<T>, dim3(Hkv, col_blocks, row_blocks), dim3(kQpThreads), 0, st, pdl, a);
 }
 

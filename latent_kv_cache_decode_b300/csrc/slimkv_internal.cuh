@@ -113,15 +113,19 @@ struct QprojArgs {
     unsigned long long turn[64];
 };
 
-// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device, once
-// per device (`done` is the caller's bit mask of devices already set).
+// Raise a kernel's dynamic shared-memory limit to `bytes` (0: leave it) on the current
+// device, once per device (`done` is the caller's bit mask of devices already set).
 inline cudaError_t set_max_smem_once(const void* func, int bytes, std::atomic<unsigned long long>& done) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (done.load() & bit) return cudaSuccess;
-    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (bytes > 0) e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    // every kernel of a call prefers the largest shared-memory carveout, so an SM
+    // need not change its L1 / shared split between the call's kernels
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess) done.fetch_or(bit);
     return e;
 }

@@ -328,26 +328,32 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
     ptx::tc_fence_after();
     const uint32_t tS0 = c.t_S + c.lane_off + (j & 1) * SW;
 
-    // pass 1: does a score of this thread's rows exceed its head's reference by more than kLazy?
-    float dmax = -INFINITY;
+    // pass 1: does a score of this thread's rows exceed its head's reference by more
+    // than kLazy? (The first tile of a piece has no reference yet: it always takes
+    // the rare path, without the vote.)
+    bool slow = !has_prev;
+    if (has_prev) {
+        float dmax = -INFINITY;
 #pragma unroll
-    for (int rb = 0; rb < RB; ++rb) {
-        const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
-        float dm = -INFINITY;
+        for (int rb = 0; rb < RB; ++rb) {
+            const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
+            float dm = -INFINITY;
 #pragma unroll
-        for (int hc = 0; hc < NS / 16; ++hc) {
-            float sc[16];
-            load_scores<LO, NS>(tS + hc * 16, sc);
+            for (int hc = 0; hc < NS / 16; ++hc) {
+                float sc[16];
+                load_scores<LO, NS>(tS + hc * 16, sc);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) dm = fmaxf(dm, sc[i] - mref[hc * 16 + i]);
+                for (int i = 0; i < 16; ++i) dm = fmaxf(dm, sc[i] - mref[hc * 16 + i]);
+            }
+            dmax = (row0 + rb * 128 < rows) ? fmaxf(dmax, dm) : dmax;
         }
-        dmax = (row0 + rb * 128 < rows) ? fmaxf(dmax, dm) : dmax;
+        const bool any = __any_sync(0xffffffffu, dmax > kLazy);
+        volatile int* fl = c.flags + (j & 1) * 4;
+        if (c.lane == 0) fl[c.wq] = any ? 1 : 0;
+        ptx::named_bar(1, 128);
+        slow = (fl[0] | fl[1] | fl[2] | fl[3]) != 0;
     }
-    const bool any = __any_sync(0xffffffffu, dmax > kLazy);
-    volatile int* fl = c.flags + (j & 1) * 4;
-    if (c.lane == 0) fl[c.wq] = any ? 1 : 0;
-    ptx::named_bar(1, 128);
-    if (fl[0] | fl[1] | fl[2] | fl[3]) {
+    if (slow) {
         softmax_new_ref<NS, NP, RB, LO>(c.red, c.m_ref_s, c.alpha_s, c.bar.vfree, c.abort, tS0, c.t_accp + c.lane_off,
                                         row0, rows, j, has_prev ? c.nMB : 0, c.aw, c.tid, c.lane, c.wq);
 #pragma unroll
