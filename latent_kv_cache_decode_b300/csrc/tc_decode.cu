@@ -939,7 +939,11 @@ SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], con
     const int misc_bytes = (6 * s.NP + 32) * 4;
     const int avail = kSmemMax - q_bytes - p_bytes - round_up(nbars * 8, 16) - misc_bytes - 1024;
     s.nslot = std::min(kMaxSlots, avail / kSlot);
-    if (s.nslot < maxK + maxV) return s;
+    // One tile part (keys or values) must fit the ring. The loads run in consumption
+    // order and each waits only for earlier parts to be consumed, so a ring smaller
+    // than a key plus a value tile (latent ranks above 256) still drains: it only
+    // serialises those tiles' loads behind their consumers.
+    if (s.nslot < std::max(maxK, maxV)) return s;
     s.off_q = s.nslot * kSlot;
     s.off_p = s.off_q + q_bytes;
     s.off_bar = s.off_p + p_bytes;

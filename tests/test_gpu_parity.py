@@ -107,7 +107,19 @@ EDGE = [
     dict(name="mqa", Hq=16, Hkv=1, N_b=256, W=128),
     dict(name="d64-bf16", d=64, Hq=8, Hkv=2, N_b=130, W=70, rank=64),
     dict(name="big-heads", Hq=64, Hkv=8, N_b=200, W=100),
+    # latent ranks above 256: a key or value tile part fills the whole ring
+    dict(name="rank320", Hq=32, Hkv=8, N_b=300, W=90, rank=320),
+    dict(name="rank512-g5", Hq=40, Hkv=8, N_b=300, W=100, rank=512),
+    dict(name="rank512-64heads", Hq=64, Hkv=8, N_b=200, W=60, rank=512),
 ]
+
+
+@pytest.mark.parametrize("Hq,rank", [(32, 320), (40, 384), (40, 512), (48, 512)])
+def test_large_ranks_take_the_tensor_core_path(Hq, rank):
+    # (64 heads with rank 512 needs a 64 KB query image and stays on the SIMT path)
+    w = wl.custom(Hq=Hq, Hkv=8, N_b=256, W=128, rank=rank)
+    sh = bd.make_shape(w.B, w.Hq, w.Hkv, w.d, w.N_b, rank, rank, w.W, torch.bfloat16)
+    assert bd.kernel_path(sh, bd.SLIMKV_LATENT) == 1
 
 
 @pytest.mark.parametrize("case", EDGE, ids=[c["name"] for c in EDGE])
