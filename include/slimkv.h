@@ -125,7 +125,10 @@ slimkv_status slimkv_decode_attn(const slimkv_shape* shape, const void* q, const
  * storage dtype, then standard GQA attention runs over [K_b ; K_raw] with RoPE on
  * the query only (beacon keys get none, so the result equals slimkv_decode_attn
  * up to rounding). Same arguments as slimkv_decode_attn; workspace >=
- * slimkv_workspace_bytes(shape, SLIMKV_RECONSTRUCT). Requires N_b > 0. */
+ * slimkv_workspace_bytes(shape, SLIMKV_RECONSTRUCT). Requires N_b > 0. With bf16
+ * storage the materialisation is a plain cuBLAS GEMM (bf16 in, float32 accumulate);
+ * its cuBLAS handle is created on the device's first reconstruction call (outside
+ * any graph capture), the one allocation this library makes. */
 slimkv_status slimkv_decode_attn_reconstruct(const slimkv_shape* shape, const void* q,
                                              const void* C_K, const void* C_V,
                                              const void* K_raw, const void* V_raw,
