@@ -1,0 +1,22 @@
+"""Host logic: the split-decode work planner, compiled from its header with g++ and
+checked on the headline shape and on random segment lists (no GPU)."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(os.path.dirname(HERE), "latent_kv_cache_decode_b300", "csrc")
+
+
+def test_work_planner_invariants(tmp_path):
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("g++ not available")
+    exe = tmp_path / "plan_check"
+    subprocess.run([gxx, "-O2", "-std=c++17", "-I", CSRC, os.path.join(HERE, "native", "plan_check.cpp"),
+                    "-o", str(exe)], check=True, capture_output=True, text=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "headline: 128 CTAs, max 1 pieces, 8..8 tiles" in r.stdout
