@@ -54,7 +54,8 @@
 extern "C" {
 #endif
 
-#define SLIMKV_ABI_VERSION 1
+/* 2: adds slimkv_append_kv (version 1 calls are unchanged) */
+#define SLIMKV_ABI_VERSION 2
 
 typedef enum {
     SLIMKV_OK = 0,

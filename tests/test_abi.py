@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.slimkv_abi_version() == 1
+    assert lib.slimkv_abi_version() == 2
     for code, name in bd.STATUS.items():
         s = lib.slimkv_status_str(code)
         assert isinstance(s, bytes) and len(s) > 0
@@ -133,3 +133,24 @@ def test_unused_operands_may_be_null(lib):
     s = _shape(N_b=0)
     p = [256, None, None, 768, 1024, None, None, 4096, 8192, 1 << 20]
     assert _call(lib, s, p, 256) == 5
+
+
+def test_append_kv_host_checks(lib):
+    # slimkv_append_kv rejects NULL, bad shapes and misaligned pointers before any launch
+    s = _shape(W=64)
+    good = [256, 512, 1024, 2048, 4096]                   # k_new, v_new, K_raw, V_raw, pos
+    for i in range(5):
+        p = list(good)
+        p[i] = None
+        assert lib.slimkv_append_kv(ctypes.byref(s), *p, None) == 1
+    assert lib.slimkv_append_kv(None, *good, None) == 1
+    for bad in (dict(W=0), dict(d=96), dict(B=0), dict(Hkv=0), dict(rope_base=-1.0), dict(W=1 << 25)):
+        assert lib.slimkv_append_kv(ctypes.byref(_shape(**bad)), *good, None) == 2, bad
+    assert lib.slimkv_append_kv(ctypes.byref(_shape(dtype=5)), *good, None) == 3
+    for i in range(4):                                    # tensors 8-byte aligned only
+        p = list(good)
+        p[i] += 8
+        assert lib.slimkv_append_kv(ctypes.byref(s), *p, None) == 4
+    p = list(good)
+    p[4] += 2                                             # positions not 4-byte aligned
+    assert lib.slimkv_append_kv(ctypes.byref(s), *p, None) == 4
