@@ -67,9 +67,9 @@ constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory we may use per CT
 constexpr int kNumKinds = 3;          // latent, raw source 0, raw source 1
 constexpr int kNG = 16;               // heads of a raw tile's query operand (the group's heads, padded)
 // m_ref moves only when a score exceeds it by more than this (log2 units). P values up
-// to 2^20 are exact enough in bf16 high + low parts and far from fp32 overflow, so a
-// generous margin keeps the rescale path (which waits for the previous value MMAs)
-// off the common path even for peaked score distributions.
+// to 2^20 keep bf16's relative precision and stay far from fp32 overflow in the
+// accumulator and row sums, so a generous margin keeps the rescale path (which waits
+// for the previous value MMAs) off the common path even for peaked score distributions.
 constexpr float kLazy = 20.f;
 constexpr int kPAtom = 128 * 32;      // bytes of one 16-head column block of P per 128 rows (x 32 B)
 constexpr int kRBRaw = 2;             // 128-row blocks per raw tile: a raw tile is 256 tokens of one KV head
@@ -85,7 +85,7 @@ struct TcParams {
     int dk[kNumKinds], dv[kNumKinds]; // key / value width
     int rb[kNumKinds];                // 128-row blocks per tile (1 latent, kRBRaw raw)
     int tiles_per_b;
-    const uint8_t* lat_img;           // query images (bf16 hi / lo, operand layout)
+    const uint8_t* lat_img;           // query images (operand layout: latent bf16, raw bf16 hi / lo)
     const uint8_t* raw_img;
     uint32_t lat_img_bytes, raw_img_bytes;
     float* acc;                       // [slots, Hq, Dmax]
@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
     uint8_t* qbuf = smem + p.off_q;          // query operand of the current piece (image copy)
-    uint8_t* pbuf = smem + p.off_p;          // [2][hi, lo][NP/16 blocks][128 rows x 32 B]
+    uint8_t* pbuf = smem + p.off_p;          // [2][NP/16 blocks][128 * RB rows x 32 B] bf16
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     float* red = reinterpret_cast<float*>(smem + p.off_red);   // [4][NP]
     float* m_ref_s = red + 4 * NP;                             // [NP]
@@ -922,8 +922,8 @@ SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], con
     s.q_cols = round_up(qc, 64);
     s.ok = false;
     if (s.NP > 64) return s;
-    // TMEM: two score buffers of 2*NP columns, then one or two accumulator buffers;
-    // prefer hi / lo accumulator parts side by side and two buffers
+    // TMEM: two score buffers of sbuf_w(NP) columns, then one or two accumulator
+    // buffers (two when they fit, so a piece's write-out overlaps the next piece)
     s.accstride = nmb * s.NP;
     int tmem = 0;
     for (s.accbuf = 2; s.accbuf >= 1; --s.accbuf) {
