@@ -50,12 +50,15 @@ slimkv_status check_shape(const slimkv_shape* s, int which) {
     return SLIMKV_OK;
 }
 
-// Number of segments (runs of rows of one kind for one batch element).
+// Number of segments (runs of rows of one kind for one batch element): the latent
+// beacons form one segment, raw rows one per KV head (the tensor-core path's split),
+// so one partial slot per segment plus kSlotCap covers every plan.
 int n_segments(const slimkv_shape* s, int which) {
+    const int raw = s->W > 0 ? s->Hkv : 0;
     int per_b = 0;
-    if (which == SLIMKV_LATENT) per_b = (s->N_b > 0) + (s->W > 0);
-    if (which == SLIMKV_RECONSTRUCT) per_b = 1 + (s->W > 0);
-    if (which == SLIMKV_FULL_KV) per_b = 1;
+    if (which == SLIMKV_LATENT) per_b = (s->N_b > 0) + raw;
+    if (which == SLIMKV_RECONSTRUCT) per_b = s->Hkv + raw;   // materialised beacons are raw rows too
+    if (which == SLIMKV_FULL_KV) per_b = raw;
     return per_b * s->B;
 }
 

@@ -33,6 +33,9 @@ static int check(int B, const SegList& sl, int G, int* n_ctas, int* max_pieces, 
         maxu = std::max(maxu, w.u_begin[c + 1] - w.u_begin[c]);
     }
     if (pieces != w.slots || (int)w.batch_slot.size() != B + 1 || w.batch_slot[B] != pieces) return 5;
+    // every piece starts at a CTA start or a segment start: the workspace reserves one
+    // partial slot per segment plus a fixed margin above the largest grid
+    if (w.slots > w.n_ctas + (int)seg_start.size()) return 7;
     // batch element b's slots are contiguous and hold exactly its pieces
     for (int b = 0; b < B; ++b)
         if (w.batch_slot[b + 1] < w.batch_slot[b]) return 6;
