@@ -154,3 +154,21 @@ def test_append_kv_host_checks(lib):
     p = list(good)
     p[4] += 2                                             # positions not 4-byte aligned
     assert lib.slimkv_append_kv(ctypes.byref(s), *p, None) == 4
+
+
+def test_plain_c_consumer(lib, tmp_path):
+    # the header is plain C: a C99 program compiles against it, links the library and
+    # runs the host-side checks
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    so_dir = os.path.join(ROOT, "latent_kv_cache_decode_b300")
+    exe = tmp_path / "abi_c_check"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "native", "abi_c_check.c"), "-L", so_dir, "-lslimkv",
+                    "-Wl,-rpath," + so_dir, "-o", str(exe)], check=True, capture_output=True, text=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "c abi ok" in r.stdout
