@@ -9,7 +9,16 @@ with its own cache buffers in HBM (4 GiB of cache per step, far larger than L2,
 so no flush is needed between steps).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl slimkv|reference]
-                  [--config 2] [--mode latent|reconstruct|full]
+                  [--config 2] [--mode latent|reconstruct|full] [--loop 128] [--layers N]
+
+Besides the device-timed step (`value`), the line carries the split-decode
+kernel's roofline (CUDA events around its launch; DRAM traffic from the committed
+ncu capture while the kernel sources match it), the end-to-end time through the
+public API with one packed host copy of every layer's inputs in and of every
+output out per step (`e2e`), the CPU oracle's time on a sample of the step
+(`cpu_baseline`), the SM clocks sampled during the timed region, and a
+multi-step decode of `--loop` generated tokens (window append + decode per layer,
+`decode_loop`). Under torchrun each rank decodes its own share of the batch.
 
 --impl reference times the float64 CPU oracle on the host cores on a bounded
 sample of the same workload (the pages describe a method, not a program).
