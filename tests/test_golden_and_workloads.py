@@ -2,6 +2,7 @@
 import os
 
 import numpy as np
+import torch
 
 from latent_kv_cache_decode_b300 import workloads as wl
 
@@ -56,3 +57,36 @@ def test_peaked_keys_fraction():
     norms = np.linalg.norm(k.reshape(2000, -1), axis=1)
     big = norms > 4 * np.median(norms)
     assert big.sum() == 20
+
+
+def test_decode_steps_are_seeded_per_batch_element():
+    w = wl.custom(B=3, Hq=8, Hkv=2, d=128, N_b=64, W=32, rank=64, ratio=4)
+    a = wl.decode_steps(w, 1, 4)
+    b = wl.decode_steps(w, 1, 4)
+    assert a["k_new"].shape == (4, 3, 2, 128) and a["q"].shape == (4, 3, 8, 128)
+    assert all(torch.equal(a[k], b[k]) for k in a)                   # deterministic
+    sub = wl.decode_steps(w, 1, 4, batch=[2])                         # a batch element alone
+    assert torch.equal(sub["k_new"][:, 0], a["k_new"][:, 2]) and torch.equal(sub["q"][:, 0], a["q"][:, 2])
+    assert not torch.equal(wl.decode_steps(w, 2, 4)["k_new"], a["k_new"])   # layers differ
+    assert a["pos"].dtype == torch.int32
+    assert a["pos"][:, 0].tolist() == [w.q_pos + s for s in range(4)]
+
+
+def test_bench_traffic_guard(tmp_path, monkeypatch):
+    # the recorded DRAM traffic is used only for its workload and while the kernel
+    # sources hash as recorded
+    import json
+    import bench
+    w = wl.config(2)
+    assert bench._measured_traffic(w, "latent") is not None
+    assert bench._measured_traffic(w, "full") is None
+    assert bench._measured_traffic(wl.config(1), "latent") is None
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "tc_decode_traffic.json")))
+    rel = next(iter(rec["source_sha256"]))
+    rec["source_sha256"][rel] = "0" * 64
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "tc_decode_traffic.json").write_text(json.dumps(rec))
+    os.makedirs(os.path.dirname(tmp_path / rel), exist_ok=True)
+    (tmp_path / rel).write_bytes(open(os.path.join(bench.ROOT, rel), "rb").read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._measured_traffic(w, "latent") is None
