@@ -74,19 +74,25 @@ def test_decode_steps_are_seeded_per_batch_element():
 
 def test_bench_traffic_guard(tmp_path, monkeypatch):
     # the recorded DRAM traffic is used only for its workload and while the kernel
-    # sources hash as recorded
+    # sources hash as recorded (checked on a record written here, so that the test
+    # does not depend on the committed capture being current)
+    import hashlib
     import json
+    import shutil
     import bench
+    rels = ["latent_kv_cache_decode_b300/csrc/tc_decode.cu", "latent_kv_cache_decode_b300/csrc/tc_ptx.cuh"]
+    for rel in rels:
+        os.makedirs(os.path.dirname(tmp_path / rel), exist_ok=True)
+        shutil.copy(os.path.join(bench.ROOT, rel), tmp_path / rel)
     w = wl.config(2)
-    assert bench._measured_traffic(w, "latent") is not None
-    assert bench._measured_traffic(w, "full") is None
-    assert bench._measured_traffic(wl.config(1), "latent") is None
-    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "tc_decode_traffic.json")))
-    rel = next(iter(rec["source_sha256"]))
-    rec["source_sha256"][rel] = "0" * 64
+    rec = {"workload": w.name + ", one layer", "dram_bytes_read_per_launch": 100,
+           "dram_bytes_write_per_launch": 20,
+           "source_sha256": {rel: hashlib.sha256(open(tmp_path / rel, "rb").read()).hexdigest() for rel in rels}}
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "tc_decode_traffic.json").write_text(json.dumps(rec))
-    os.makedirs(os.path.dirname(tmp_path / rel), exist_ok=True)
-    (tmp_path / rel).write_bytes(open(os.path.join(bench.ROOT, rel), "rb").read())
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._measured_traffic(w, "latent") == 120
+    assert bench._measured_traffic(w, "full") is None
+    assert bench._measured_traffic(wl.config(1), "latent") is None
+    (tmp_path / rels[0]).write_bytes(open(tmp_path / rels[0], "rb").read() + b"// changed\n")
     assert bench._measured_traffic(w, "latent") is None
