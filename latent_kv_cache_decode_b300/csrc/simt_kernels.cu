@@ -45,16 +45,27 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// 16-byte asynchronous global -> shared copy (completion via cp_async_wait_all).
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ptx::smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-// Pull `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
+// ---------------------------------------------------------------------------
+// Query RoPE and latent projection, "Latent-space attention removes the rebuild
+// step": RoPE stays on every query, and the beacon query is projected into the
+// latent space per GQA group, q_lat[b,h,:] = RoPE(q[b,h]) . U_K^(g) (the
+// projection is taken after grouping, so U_K^(g) serves the G heads of group g).
+//
+// Grid (Hkv, column blocks of 16 latent columns, row blocks). A row is one
+// (batch element, head of group g) pair; a CTA holds at most 32 rows: `nbb`
+// whole batch elements when G <= 32, else one 32-head chunk of one element.
+// The rotation angle p * theta_i is reduced modulo one turn exactly with 64-bit
+// fixed-point arithmetic (turn[i] = theta_i / 2pi), then sin/cos of the reduced
+// angle are taken in float32; both outputs are scaled by scale * log2(e).
+//
+// Ordering with neighbouring kernels: only the U_K block (a weight) is read before
+// the grid-dependency wait; q and q_pos, which the preceding kernel may write, are
+// read after it, and dependents are released only after it, so a dependent kernel
+// may read anything the preceding kernels wrote (the caches) without a wait of its own.
+// ---------------------------------------------------------------------------
+constexpr int kQpRows = 32;
+constexpr int kQpCols = 16;
+constexpr int kQpThreads = 256;
 
 // 16-byte vector of storage elements: 8 bf16 or 4 float32.
 template <typename T> struct Vec16;
@@ -80,66 +91,57 @@ template <> struct Vec16<float> {
     }
 };
 
-// ---------------------------------------------------------------------------
-// Query RoPE and latent projection, "Latent-space attention removes the rebuild
-// step": RoPE stays on every query, and the beacon query is projected into the
-// latent space per GQA group, q_lat[b,h,:] = RoPE(q[b,h]) . U_K^(g) (the
-// projection is taken after grouping, so U_K^(g) serves the G heads of group g).
-//
-// Grid (Hkv, blocks of 32 latent columns, row blocks). A row is one (batch
-// element, head of group g) pair; a CTA holds at most 16 rows. The rotation angle
-// p * theta_i is reduced modulo one turn exactly with 64-bit fixed-point arithmetic
-// (turn[i] = theta_i / 2pi), then sin/cos of the reduced angle are taken in float32;
-// every output is scaled by scale * log2(e).
-//
-// The kernel is small (128 threads, at most 25 KB of shared memory for float32
-// storage, 16 KB for bf16) so that its CTAs fit on an SM next to a decode CTA.
-//
-// Ordering with neighbouring kernels: only the U_K block (a weight) is read before
-// the grid-dependency wait; q and q_pos, which the preceding kernel may write, are
-// read after it. Dependents are released at once: the decode kernel reads only its
-// cache operands before its own wait (and a call's cache operands are never written
-// by the kernels of the call before it).
-// ---------------------------------------------------------------------------
-constexpr int kQpRows = 16;
-constexpr int kQpCols = 32;
-constexpr int kQpThreads = 128;
-
 template <typename T>
 __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant__ QprojArgs a) {
-    // query rows, rotated and scaled (row stride padded by 4 floats)
+    // query rows, rotated and scaled (row stride padded by 4 floats: the projection
+    // reads two rows per warp, which then fall in different banks)
     __shared__ __align__(16) float qr_s[kQpRows][128 + 4];
-    __shared__ __align__(16) T u_s[128][kQpCols];   // U_K^(g) column block
+    __shared__ __align__(16) float u_s[128][kQpCols];   // U_K^(g) column block
     constexpr int VN = Vec16<T>::N;
     const int g = blockIdx.x, cb = blockIdx.y, rb = blockIdx.z;
     const int tid = threadIdx.x;
     const int G = a.Hq / a.Hkv, d = a.d, half = d >> 1;
-    // rows of this block: r = r0 + rl (rl < nr), batch element r / G, head g * G + r % G
-    const int r0 = rb * kQpRows, nr = min(kQpRows, a.B * G - r0);
-    const bool proj = a.U_K != nullptr;
-
-    // the U_K column block: a weight, copied before the dependency wait
-    if (proj) {
-        constexpr int cpr = kQpCols / VN;   // 16-byte chunks per row of the block
-        for (int idx = tid; idx < d * cpr; idx += kQpThreads) {
-            const int i = idx / cpr, e = (idx - i * cpr) * VN;
-            cp_async16(&u_s[i][e], (const T*)a.U_K + ((size_t)g * d + i) * a.r_k + cb * kQpCols + e);
-        }
-        cp_async_commit();
+    // rows of this block: batch elements [b0, b0 + nb) x heads-in-group [i0, i1)
+    int b0, nb, i0, i1;
+    if (a.hcn == 1) {
+        b0 = rb * a.nbb;
+        nb = min(a.nbb, a.B - b0);
+        i0 = 0;
+        i1 = G;
+    } else {
+        b0 = rb / a.hcn;
+        nb = 1;
+        i0 = (rb % a.hcn) * 32;
+        i1 = min(G, i0 + 32);
     }
-    pdl_trigger();
+    const int ni = i1 - i0, rows = nb * ni;
+
+    // the U_K column block: a weight, read before the dependency wait
+    if (a.U_K != nullptr) {
+        constexpr int upr = kQpCols / VN;   // vectors per row of the block
+        for (int idx = tid; idx < d * upr; idx += kQpThreads) {
+            const int i = idx / upr, e = (idx - i * upr) * VN;
+            const uint4 v = *reinterpret_cast<const uint4*>((const T*)a.U_K + ((size_t)g * d + i) * a.r_k +
+                                                            cb * kQpCols + e);
+            float f[VN];
+            Vec16<T>::to_f(v, f);
+#pragma unroll
+            for (int k = 0; k < VN; ++k) u_s[i][e + k] = f[k];
+        }
+    }
     pdl_wait();       // q, q_pos and this workspace are free to read / write from here
+    pdl_trigger();
 
     // load, rotate and scale the query rows: item = (row, VN-wide chunk of the first
     // half); the thread loads both halves of the chunk and rotates them in registers
     const int cph = half / VN;   // chunks per half row
-    for (int idx = tid; idx < nr * cph; idx += kQpThreads) {
-        const int rl = idx / cph, e = (idx - rl * cph) * VN;
-        const int r = r0 + rl, b = r / G, h = g * G + (r - b * G);
-        const T* src = (const T*)a.q + ((size_t)b * a.Hq + h) * d;
+    for (int idx = tid; idx < rows * cph; idx += kQpThreads) {
+        const int r = idx / cph, e = (idx - r * cph) * VN;
+        const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
+        const T* src = (const T*)a.q + ((size_t)(b0 + bl) * a.Hq + h) * d;
         const uint4 v1 = *reinterpret_cast<const uint4*>(src + e);
         const uint4 v2 = *reinterpret_cast<const uint4*>(src + half + e);
-        const unsigned long long pos = (unsigned long long)(long long)a.q_pos[b];
+        const unsigned long long pos = (unsigned long long)(long long)a.q_pos[b0 + bl];
         float x1[VN], x2[VN];
         Vec16<T>::to_f(v1, x1);
         Vec16<T>::to_f(v2, x2);
@@ -150,36 +152,31 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
             const long long frac = (long long)(pos * a.turn[e + k]);
             float sn, cs;
             sincospif((float)frac * 1.0842021724855044e-19f, &sn, &cs);   // x 2^-63: half-turns
-            qr_s[rl][e + k] = (x1[k] * cs - x2[k] * sn) * a.scale_log2;
-            qr_s[rl][half + e + k] = (x2[k] * cs + x1[k] * sn) * a.scale_log2;
+            qr_s[r][e + k] = (x1[k] * cs - x2[k] * sn) * a.scale_log2;
+            qr_s[r][half + e + k] = (x2[k] * cs + x1[k] * sn) * a.scale_log2;
         }
     }
-    if (proj) cp_async_wait_all();
     __syncthreads();
-
-    // batch elements whose head 0 is a row of this block write the zero rows of the
-    // absent heads (Hq <= h < NP) of their images (raw image: by the first column block)
-    const int b_first = (r0 + G - 1) / G, b_end = (r0 + nr + G - 1) / G;
-    const int npad = a.NP - a.Hq;
-    if (cb == 0) {
-        if (a.q_rot != nullptr) {
-            for (int idx = tid; idx < nr * (d / 4); idx += kQpThreads) {
-                const int rl = idx / (d / 4), e = (idx - rl * (d / 4)) * 4;
-                const int r = r0 + rl, b = r / G, h = g * G + (r - b * G);
-                *reinterpret_cast<float4*>(a.q_rot + ((size_t)b * a.Hq + h) * d + e) =
-                    *reinterpret_cast<const float4*>(&qr_s[rl][e]);
-            }
+    if (cb == 0 && a.q_rot != nullptr) {
+        for (int idx = tid; idx < rows * (d / 4); idx += kQpThreads) {
+            const int r = idx / (d / 4), e = (idx - r * (d / 4)) * 4;
+            const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
+            *reinterpret_cast<float4*>(a.q_rot + ((size_t)(b0 + bl) * a.Hq + h) * d + e) =
+                *reinterpret_cast<const float4*>(&qr_s[r][e]);
         }
-        if (a.raw_img != nullptr) {
-            // raw image of b: rows [0, NP) high, [NP, 2 NP) low parts of every head
-            const size_t ib = raw_img_bytes(a.NP, d);
-            const int units = d / 8;
-            for (int idx = tid; idx < nr * units; idx += kQpThreads) {
-                const int rl = idx / units, u = idx - rl * units;
-                const int r = r0 + rl, b = r / G, h = g * G + (r - b * G);
-                uint8_t* img = a.raw_img + (size_t)b * ib;
-                const float* src = &qr_s[rl][u * 8];
-                uint32_t hi[4], lo[4];
+    }
+    if (cb == 0 && a.raw_img != nullptr) {
+        // raw image of (b, g): 32 rows x d, rows [0,16) high, [16,32) low parts of the
+        // group's G (<= 16) heads; rows of absent heads are zero
+        const size_t ib = raw_img_bytes(d);
+        const int units = d / 8;
+        for (int idx = tid; idx < nb * 16 * units; idx += kQpThreads) {
+            const int bl = idx / (16 * units), rem = idx - bl * 16 * units;
+            const int i = rem / units, u = rem - i * units;
+            uint8_t* img = a.raw_img + ((size_t)(b0 + bl) * a.Hkv + g) * ib;
+            uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+            if (i < G) {
+                const float* src = &qr_s[bl * ni + i][u * 8];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(src[2 * k], src[2 * k + 1]);
@@ -188,55 +185,46 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
                     hi[k] = *reinterpret_cast<const uint32_t*>(&h2);
                     lo[k] = *reinterpret_cast<const uint32_t*>(&l2);
                 }
-                *reinterpret_cast<uint4*>(img + ptx::sw128_offset(h, u * 8, 2 * a.NP)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(img + ptx::sw128_offset(a.NP + h, u * 8, 2 * a.NP)) =
-                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
-            if (g == 0 && npad > 0) {
-                const int n = (b_end - b_first) * 2 * npad * units;
-                for (int idx = tid; idx < n; idx += kQpThreads) {
-                    const int bl = idx / (2 * npad * units), rem = idx - bl * 2 * npad * units;
-                    const int pr = rem / units, u = rem - pr * units;
-                    const int row = pr < npad ? a.Hq + pr : a.NP + a.Hq + (pr - npad);
-                    uint8_t* img = a.raw_img + (size_t)(b_first + bl) * ib;
-                    *reinterpret_cast<uint4*>(img + ptx::sw128_offset(row, u * 8, 2 * a.NP)) = make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
+            *reinterpret_cast<uint4*>(img + ptx::sw128_offset(i, u * 8, 32)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(img + ptx::sw128_offset(16 + i, u * 8, 32)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
     }
-    if (!proj) return;
-    if (a.lat_img != nullptr && g == 0 && npad > 0) {
-        const int n = (b_end - b_first) * npad * kQpCols;
-        for (int idx = tid; idx < n; idx += kQpThreads) {
+    if (a.lat_img != nullptr && g == 0 && (a.hcn == 1 || rb % a.hcn == 0) && a.NP > a.Hq) {
+        // rows of absent heads (Hq <= h < NP) of the latent image are zero, so that the
+        // tensor-core path may treat every head column alike
+        const int npad = a.NP - a.Hq;
+        for (int idx = tid; idx < nb * npad * kQpCols; idx += kQpThreads) {
             const int bl = idx / (npad * kQpCols), rem = idx - bl * npad * kQpCols;
             const int h = a.Hq + rem / kQpCols, col = cb * kQpCols + rem % kQpCols;
-            uint8_t* img = a.lat_img + (size_t)(b_first + bl) * lat_img_bytes(a.NP, a.r_k);
+            uint8_t* img = a.lat_img + (size_t)(b0 + bl) * lat_img_bytes(a.NP, a.r_k);
             *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(h, col, a.NP)) = __float2bfloat16_rn(0.f);
         }
     }
-    // q_lat block: 16 rows x 32 columns; thread = (column c, rows 4 rg .. 4 rg + 3)
-    const int c = tid & (kQpCols - 1), rg = tid / kQpCols;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (a.U_K == nullptr) return;
+    // q_lat block: 32 rows x 16 columns; thread = (column c, row pair rp)
+    const int c = tid & (kQpCols - 1), rp = tid / kQpCols;
+    const int r0 = 2 * rp, r1 = 2 * rp + 1;
+    float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll 4
     for (int i = 0; i < d; i += 4) {
-        const float u0 = to_f(u_s[i][c]), u1 = to_f(u_s[i + 1][c]), u2 = to_f(u_s[i + 2][c]),
-                    u3 = to_f(u_s[i + 3][c]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 qv = *reinterpret_cast<const float4*>(&qr_s[rg * 4 + k][i]);
-            acc[k] = fmaf(qv.x, u0, fmaf(qv.y, u1, fmaf(qv.z, u2, fmaf(qv.w, u3, acc[k]))));
-        }
+        const float4 qa = *reinterpret_cast<const float4*>(&qr_s[r0][i]);
+        const float4 qb = *reinterpret_cast<const float4*>(&qr_s[r1][i]);
+        const float u0 = u_s[i][c], u1 = u_s[i + 1][c], u2 = u_s[i + 2][c], u3 = u_s[i + 3][c];
+        acc0 = fmaf(qa.x, u0, fmaf(qa.y, u1, fmaf(qa.z, u2, fmaf(qa.w, u3, acc0))));
+        acc1 = fmaf(qb.x, u0, fmaf(qb.y, u1, fmaf(qb.z, u2, fmaf(qb.w, u3, acc1))));
     }
     const int col = cb * kQpCols + c;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int rl = rg * 4 + k;
-        if (rl < nr) {
-            const int r = r0 + rl, b = r / G, h = g * G + (r - b * G);
-            if (a.q_lat != nullptr) a.q_lat[((size_t)b * a.Hq + h) * a.r_k + col] = acc[k];
+    for (int k = 0; k < 2; ++k) {
+        const int r = k ? r1 : r0;
+        const float v = k ? acc1 : acc0;
+        if (r < rows) {
+            const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
+            if (a.q_lat != nullptr) a.q_lat[((size_t)(b0 + bl) * a.Hq + h) * a.r_k + col] = v;
             if (a.lat_img != nullptr) {
-                uint8_t* img = a.lat_img + (size_t)b * lat_img_bytes(a.NP, a.r_k);
-                *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(h, col, a.NP)) = __float2bfloat16_rn(acc[k]);
+                uint8_t* img = a.lat_img + (size_t)(b0 + bl) * lat_img_bytes(a.NP, a.r_k);
+                *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(h, col, a.NP)) = __float2bfloat16_rn(v);
             }
         }
     }
@@ -265,8 +253,9 @@ __global__ void __launch_bounds__(128) simt_decode_kernel(SimtDecodeArgs a) {
     const T* Vp;
     const float* qv;
     size_t ks, vs;
-    int Dk, Dv, n_rows, rpi;
+    int Dk, Dv, n_rows, rpi, kind;
     if (k < a.nit_L) {
+        kind = 0;
         Kp = (const T*)a.C_K + (size_t)b * a.N_b * a.r_k;
         Vp = (const T*)a.C_V + (size_t)b * a.N_b * a.r_v;
         ks = a.r_k;
@@ -287,6 +276,7 @@ __global__ void __launch_bounds__(128) simt_decode_kernel(SimtDecodeArgs a) {
             K = (const T*)a.K1;
             V = (const T*)a.V1;
         }
+        kind = 1;
         Kp = K + ((size_t)b * W * a.Hkv + g) * a.d;
         Vp = V + ((size_t)b * W * a.Hkv + g) * a.d;
         ks = vs = (size_t)a.Hkv * a.d;
@@ -345,6 +335,7 @@ __global__ void __launch_bounds__(128) simt_decode_kernel(SimtDecodeArgs a) {
     if (tid == 0) {
         a.ml[((size_t)slot * 2 + 0) * a.Hq + h] = m;
         a.ml[((size_t)slot * 2 + 1) * a.Hq + h] = l;
+        if (h == 0) a.kind[slot] = kind;
     }
 #pragma unroll
     for (int e = 0; e < kMaxRank / 128; ++e) {
@@ -355,176 +346,183 @@ __global__ void __launch_bounds__(128) simt_decode_kernel(SimtDecodeArgs a) {
 
 // ---------------------------------------------------------------------------
 // Split combine fused with the value up-projection ("(A C_V) U_V^T": the latent
-// aggregate is up-projected once, after all beacon splits are merged). One CTA per
-// (batch element b, KV group g and chunk of at most 4 of its heads). The partials of
-// b cover every head; latent ones (r_v wide) occupy slots [slot_begin[b],
-// slot_mid[b]), raw ones (d wide) [slot_mid[b], slot_begin[b+1]). They are merged by
-// their log2-domain maxima:
+// aggregate is up-projected once, after all beacon splits are merged). One CTA
+// per (query head h, batch element b), g its KV group. The partials of batch b
+// that cover head h (SlotKind) are merged by their log2-domain maxima:
 //   M = max_s m_s, w_s = exp2(m_s - M), L = sum_s w_s l_s,
 //   z = sum_{latent s} w_s acc_s (r_v wide), y = sum_{raw s} w_s acc_s (d wide),
-//   out[b,h,i] = (z . U_V^(g)[i, :] + y[i]) / L.
-// A partial with l = 0 covered no key of that head and is skipped; a NaN l (a decode
-// CTA that gave up on a wait) propagates into the output.
-//
-// The kernel is latency-bound: it is laid out as three rounds of independent loads
-// (the (m, l) pairs, then every partial value the merge needs, then U_V^(g), whose
-// rows are pulled into L2 before the dependency wait), so that each round costs one
-// memory round trip. It is small (256 threads, a few KB of shared memory) so that
-// its CTAs fit on an SM next to a decode CTA.
+//   out[b,h,:] = (z . U_V^(g)T + y) / L.
+// Global loads are issued in independent batches so that the kernel costs a few
+// memory round trips, not one per partial.
 // ---------------------------------------------------------------------------
 constexpr int kCombThreads = 256;
-constexpr int kCombHeads = 4;    // heads per CTA
-constexpr int kCombBatch = 8;    // slots whose loads are in flight together
-constexpr int kCombWeightRegs = 2;   // slots per lane whose (m, l) stay in registers
+constexpr int kCombBatch = 16;
+constexpr int kCombPrefetchCols = 256;   // latent columns of U_V staged before the wait (bf16)
+
+// 16-byte asynchronous global -> shared copy (completion via cp_async_wait_all).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ptx::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+constexpr int kCombRowsPerWarp = 128 / (kCombThreads / 32);   // 16 output rows per warp (d <= 128)
 
 template <typename T>
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(const __grid_constant__ CombineArgs a) {
+    // per covering partial: slot, m, l (later the weight); latent and raw lists; then,
+    // for bf16 storage, U_V^(g)[:, 0:256) staged by asynchronous copies
     extern __shared__ __align__(16) float dyn[];
-    __shared__ float L_s[kCombHeads];
-    const int b = blockIdx.x;
-    const int G = a.Hq / a.Hkv, nhc = (G + kCombHeads - 1) / kCombHeads;
-    const int g = blockIdx.y / nhc, hc = blockIdx.y - g * nhc;
-    const int h0 = g * G + hc * kCombHeads, nh = min(kCombHeads, G - hc * kCombHeads);
+    __shared__ __align__(16) float z_s[kMaxRank];
+    __shared__ float y_s[128];
+    __shared__ int n_lat_s, n_raw_s;
+    __shared__ float L_s;
+    const int h = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d = a.d;
-    const int s0 = a.slot_begin[b], sm = a.slot_mid[b], s1 = a.slot_begin[b + 1];
-    const int ns = s1 - s0, nl = sm - s0, nr = s1 - sm;
+    const int G = a.Hq / a.Hkv, g = h / G;
     const bool latent = a.U_V != nullptr;
-    float* w_s = dyn;                                          // [ns][4] merge weights
-    float* z_s = dyn + a.ns_max * kCombHeads;                  // [r_v][4] latent aggregate
-    float* y_s = z_s + (latent ? a.r_v * kCombHeads : 0);      // [d][4] raw aggregate
-    if (latent && tid < 2) {
-        // U_V^(g): a weight, pulled into L2 before the dependency wait (two halves)
-        const size_t half = (size_t)d * a.r_v * sizeof(T) / 2;
-        prefetch_l2(reinterpret_cast<const char*>(a.U_V) + (size_t)g * d * a.r_v * sizeof(T) + tid * half,
-                    (uint32_t)half);
+    constexpr int VN = Vec16<T>::N;
+    const int nrow = (a.d + (kCombThreads / 32) - 1) / (kCombThreads / 32);
+
+    const int s0 = a.slot_begin[b], ns = a.slot_begin[b + 1] - s0;
+    // U_V^(g)[:, 0:256): a weight, copied before the dependency wait
+    const bool prefetch = latent && VN == 8;
+    T* u_stage = reinterpret_cast<T*>(dyn + ((6 * a.ns_max + 3) & ~3));
+    if (prefetch) {
+        const int cpr = min(a.r_v, kCombPrefetchCols) / 8;   // 16-byte chunks per row
+        for (int idx = tid; idx < a.d * cpr; idx += kCombThreads) {
+            const int i = idx / cpr, e = (idx - i * cpr) * 8;
+            cp_async16(u_stage + i * kCombPrefetchCols + e, (const T*)a.U_V + ((size_t)g * a.d + i) * a.r_v + e);
+        }
+        cp_async_commit();
     }
     pdl_trigger();
     pdl_wait();   // partials come from the decode kernel
 
-    // round 1: merge weights of head h0 + warp over the slots of b; every lane loads its
-    // (m, l) pairs once (up to kCombWeightRegs slots per lane stay in registers)
-    if (warp < nh) {
-        const int h = h0 + warp;
-        constexpr int R = kCombWeightRegs;
-        float mr[R], lr[R];
-#pragma unroll
-        for (int k = 0; k < R; ++k) {
-            const int s = lane + 32 * k;
-            mr[k] = s < ns ? a.ml[((size_t)(s0 + s) * 2) * a.Hq + h] : -INFINITY;
-            lr[k] = s < ns ? a.ml[((size_t)(s0 + s) * 2 + 1) * a.Hq + h] : 0.f;
-        }
+    int* lat_slot = reinterpret_cast<int*>(dyn);
+    float* lat_m = dyn + ns;
+    float* lat_l = dyn + 2 * ns;
+    int* raw_slot = reinterpret_cast<int*>(dyn + 3 * ns);
+    float* raw_m = dyn + 4 * ns;
+    float* raw_l = dyn + 5 * ns;
+    if (warp == 0) {
+        // compact the partials that cover head h with their (m, l), one load each
+        int nl = 0, nr = 0;
         float M = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < R; ++k)
-            if (lr[k] != 0.f) M = fmaxf(M, mr[k]);   // a NaN (poisoned) l is kept
-        for (int s = lane + 32 * R; s < ns; s += 32) {
-            const float l = a.ml[((size_t)(s0 + s) * 2 + 1) * a.Hq + h];
-            if (l != 0.f) M = fmaxf(M, a.ml[((size_t)(s0 + s) * 2) * a.Hq + h]);
+        for (int base = 0; base < ns; base += 32) {
+            const int s = base + lane;
+            int kd = -1;
+            float m = -INFINITY, l = 0.f;
+            if (s < ns) {
+                kd = a.kind[s0 + s];
+                m = a.ml[((size_t)(s0 + s) * 2) * a.Hq + h];
+                l = a.ml[((size_t)(s0 + s) * 2 + 1) * a.Hq + h];
+            }
+            const bool is_lat = latent && kd == kSlotLatent;
+            const bool is_raw = kd == kSlotRawAll || kd == kSlotRawGroup + g;
+            const bool use = (is_lat || is_raw) && l != 0.f;   // a NaN (poisoned) l is kept
+            if (use) M = fmaxf(M, m);
+            const unsigned bl = __ballot_sync(0xffffffffu, use && is_lat);
+            const unsigned br = __ballot_sync(0xffffffffu, use && is_raw);
+            const unsigned below = (1u << lane) - 1u;
+            if (use && is_lat) {
+                const int o = nl + __popc(bl & below);
+                lat_slot[o] = s0 + s;
+                lat_m[o] = m;
+                lat_l[o] = l;
+            }
+            if (use && is_raw) {
+                const int o = nr + __popc(br & below);
+                raw_slot[o] = s0 + s;
+                raw_m[o] = m;
+                raw_l[o] = l;
+            }
+            nl += __popc(bl);
+            nr += __popc(br);
         }
         M = warp_max(M);
+        __syncwarp();
+        // weights w = exp2(m - M) (stored over m) and L = sum w l
         float L = 0.f;
-#pragma unroll
-        for (int k = 0; k < R; ++k) {
-            const int s = lane + 32 * k;
-            if (s < ns) {
-                const float w = (lr[k] != 0.f) ? exp2f(mr[k] - M) : 0.f;
-                w_s[s * kCombHeads + warp] = w;
-                L = fmaf(w, lr[k], L);
-            }
+        for (int i = lane; i < nl; i += 32) {
+            const float w = exp2f(lat_m[i] - M);
+            L = fmaf(w, lat_l[i], L);
+            lat_m[i] = w;
         }
-        for (int s = lane + 32 * R; s < ns; s += 32) {
-            const float m = a.ml[((size_t)(s0 + s) * 2) * a.Hq + h];
-            const float l = a.ml[((size_t)(s0 + s) * 2 + 1) * a.Hq + h];
-            const float w = (l != 0.f) ? exp2f(m - M) : 0.f;
-            w_s[s * kCombHeads + warp] = w;
-            L = fmaf(w, l, L);
+        for (int i = lane; i < nr; i += 32) {
+            const float w = exp2f(raw_m[i] - M);
+            L = fmaf(w, raw_l[i], L);
+            raw_m[i] = w;
         }
         L = warp_sum(L);
-        if (lane == 0) L_s[warp] = L;
+        if (lane == 0) {
+            n_lat_s = nl;
+            n_raw_s = nr;
+            L_s = L;
+        }
     }
     __syncthreads();
-    // round 2: z (items of 4 latent columns x one head) and y (4 rows x one head);
-    // every thread takes at most one item of each, loads batched over kCombBatch slots
-    const size_t sstride = (size_t)a.Hq * a.Dmax;   // floats between consecutive slots
-    auto merge = [&](int item, int first_slot, int nslot, int wbase) {
-        const int col = (item >> 2) * 4, hh = item & 3;
-        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (hh < nh) {
-            const float* src = a.acc + ((size_t)first_slot * a.Hq + h0 + hh) * a.Dmax + col;
-            for (int s = 0; s < nslot; s += kCombBatch) {
-                float4 v[kCombBatch];
+    const int nl = n_lat_s, nr = n_raw_s;
+    // z[j] and y[i]: batches of independent loads over the covering partials
+    auto accumulate = [&](const int* slot, const float* w, int n, int col) {
+        float acc = 0.f;
+        for (int i0 = 0; i0 < n; i0 += kCombBatch) {
+            float v[kCombBatch];
 #pragma unroll
-                for (int k = 0; k < kCombBatch; ++k)
-                    v[k] = s + k < nslot ? *reinterpret_cast<const float4*>(src + (s + k) * sstride)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < kCombBatch; ++k)
+                v[k] = (i0 + k < n) ? a.acc[((size_t)slot[i0 + k] * a.Hq + h) * a.Dmax + col] : 0.f;
 #pragma unroll
-                for (int k = 0; k < kCombBatch; ++k) {
-                    const float w = s + k < nslot ? w_s[(wbase + s + k) * kCombHeads + hh] : 0.f;
-                    z.x = fmaf(w, v[k].x, z.x);
-                    z.y = fmaf(w, v[k].y, z.y);
-                    z.z = fmaf(w, v[k].z, z.z);
-                    z.w = fmaf(w, v[k].w, z.w);
-                }
-            }
+            for (int k = 0; k < kCombBatch; ++k)
+                if (i0 + k < n) acc = fmaf(w[i0 + k], v[k], acc);
         }
-        return z;
+        return acc;
     };
-    const int nz = latent ? a.r_v : 0;    // (r_v / 4) column quads x 4 heads
-    const int ny = d;                     // (d / 4) row quads x 4 heads
-    for (int it = tid; it < nz + ny; it += kCombThreads) {
-        const bool zi = it < nz;
-        const int item = zi ? it : it - nz;
-        const float4 v = zi ? merge(item, s0, nl, 0) : merge(item, sm, nr, nl);
-        float* dst = zi ? z_s : y_s;
-        const int col = (item >> 2) * 4, hh = item & 3;
-        dst[(col + 0) * kCombHeads + hh] = v.x;
-        dst[(col + 1) * kCombHeads + hh] = v.y;
-        dst[(col + 2) * kCombHeads + hh] = v.z;
-        dst[(col + 3) * kCombHeads + hh] = v.w;
-    }
+    if (latent)
+        for (int j = tid; j < a.r_v; j += kCombThreads) z_s[j] = accumulate(lat_slot, lat_m, nl, j);
+    for (int i = tid; i < a.d; i += kCombThreads) y_s[i] = accumulate(raw_slot, raw_m, nr, i);
+    if (prefetch) cp_async_wait_all();
     __syncthreads();
-    // round 3: out[i] = (z . U_V^(g)[i, :] + y[i]) / L; thread = (row i, half jh of the
-    // latent columns), the half row's U_V loads issued together
-    for (int i2 = tid; i2 < 2 * d; i2 += kCombThreads) {
-        const int i = i2 >> 1, jh = i2 & 1;
-        float part[kCombHeads] = {0.f, 0.f, 0.f, 0.f};
-        if (latent) {
-            const int jn = a.r_v >> 1, j0 = jh * jn;
-            const T* u = (const T*)a.U_V + ((size_t)g * d + i) * a.r_v + j0;
-            const float4* z4 = reinterpret_cast<const float4*>(z_s) + j0;
-            for (int jj = 0; jj < jn; jj += 64) {
-                constexpr int VN = Vec16<T>::N;
-                uint4 uv[64 / VN];
+    const float invL = 1.f / L_s;
+    if (!latent) {
+        for (int i = tid; i < a.d; i += kCombThreads) a.out[((size_t)b * a.Hq + h) * a.d + i] = y_s[i] * invL;
+        return;
+    }
+    // out[i] = (z . U_V^(g)[i, :] + y[i]) / L; a warp covers rows i = warp, warp + 8, ...
+    // with lane l owning latent columns [8l, 8l + 8) of each 256-column chunk
+    for (int c0 = 0; c0 < a.r_v; c0 += 256) {
+        const int j = c0 + lane * 8;
+        float zl[8];
 #pragma unroll
-                for (int q = 0; q < 64 / VN; ++q)
-                    uv[q] = jj + q * VN < jn ? *reinterpret_cast<const uint4*>(u + jj + q * VN) : make_uint4(0, 0, 0, 0);
+        for (int e = 0; e < 8; ++e) zl[e] = (j + e < a.r_v) ? z_s[j + e] : 0.f;
+        float part[kCombRowsPerWarp];
 #pragma unroll
-                for (int q = 0; q < 64 / VN; ++q) {
-                    float f[VN];
-                    Vec16<T>::to_f(uv[q], f);
+        for (int r = 0; r < kCombRowsPerWarp; ++r) {
+            part[r] = 0.f;
+            const int i = warp + r * (kCombThreads / 32);
+            if (r < nrow && i < a.d && j < a.r_v) {
+                float f[8];
+                if (prefetch && c0 == 0) {
+                    Vec16<T>::to_f(*reinterpret_cast<const uint4*>(u_stage + i * kCombPrefetchCols + j), f);
+                } else {
+                    const T* u = (const T*)a.U_V + ((size_t)g * a.d + i) * a.r_v + j;
 #pragma unroll
-                    for (int e = 0; e < VN; ++e) {
-                        if (jj + q * VN + e < jn) {
-                            const float4 zz = z4[jj + q * VN + e];
-                            part[0] = fmaf(zz.x, f[e], part[0]);
-                            part[1] = fmaf(zz.y, f[e], part[1]);
-                            part[2] = fmaf(zz.z, f[e], part[2]);
-                            part[3] = fmaf(zz.w, f[e], part[3]);
-                        }
-                    }
+                    for (int q = 0; q < 8 / VN; ++q)
+                        Vec16<T>::to_f(*reinterpret_cast<const uint4*>(u + q * VN), f + q * VN);
                 }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) part[r] = fmaf(zl[e], f[e], part[r]);
             }
         }
 #pragma unroll
-        for (int hh = 0; hh < kCombHeads; ++hh) part[hh] += __shfl_xor_sync(0xffffffffu, part[hh], 1);
-        // the two threads of a row write two heads each
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int hh = 2 * jh + k;
-            if (hh < nh)
-                a.out[((size_t)b * a.Hq + h0 + hh) * d + i] = (part[hh] + y_s[i * kCombHeads + hh]) / L_s[hh];
+        for (int r = 0; r < kCombRowsPerWarp; ++r) {
+            const float v = warp_sum(part[r]);
+            const int i = warp + r * (kCombThreads / 32);
+            if (lane == 0 && r < nrow && i < a.d) y_s[i] += v;
         }
+    }
+    __syncwarp();
+    for (int r = 0; r < kCombRowsPerWarp; ++r) {
+        const int i = warp + r * (kCombThreads / 32);
+        if (lane == 0 && r < nrow && i < a.d) a.out[((size_t)b * a.Hq + h) * a.d + i] = y_s[i] * invL;
     }
 }
 
@@ -597,11 +595,17 @@ cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* 
     a.Hkv = Hkv;
     a.d = d;
     a.r_k = r_k;
-    a.rows = kQpRows;
     a.scale_log2 = scale_log2;
-    rope_turns(base, d, a.turn);
     const int G = Hq / Hkv;
-    const int row_blocks = (B * G + kQpRows - 1) / kQpRows;
+    if (G <= kQpRows) {
+        a.nbb = kQpRows / G;
+        a.hcn = 1;
+    } else {
+        a.nbb = 1;
+        a.hcn = (G + kQpRows - 1) / kQpRows;
+    }
+    rope_turns(base, d, a.turn);
+    const int row_blocks = (G <= kQpRows) ? (B + a.nbb - 1) / a.nbb : B * a.hcn;
     const int col_blocks = U_K ? r_k / kQpCols : 1;
     static std::atomic<unsigned long long> attr_done{0};
     const cudaError_t e = set_max_smem_once((const void*)qproj_kernel<T>, 0, attr_done);
@@ -623,14 +627,14 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl) {
     if (ns_max > kMaxSlotsPerB) return cudaErrorInvalidValue;
     CombineArgs b = a;
     b.ns_max = ns_max;
-    const size_t smem = sizeof(float) * kCombHeads * ((size_t)ns_max + (a.U_V ? a.r_v : 0) + a.d);
+    size_t smem = (size_t)((6 * ns_max + 3) & ~3) * sizeof(float);
+    if (a.U_V != nullptr && sizeof(T) == 2) smem += (size_t)a.d * kCombPrefetchCols * sizeof(T);
     static std::atomic<unsigned long long> attr_done{0};
     const cudaError_t e = set_max_smem_once(
-        (const void*)combine_kernel<T>, (int)(sizeof(float) * kCombHeads * (kMaxSlotsPerB + kMaxRank + 128)),
-        attr_done);
+        (const void*)combine_kernel<T>,
+        (int)(((6 * kMaxSlotsPerB + 3) & ~3) * sizeof(float) + 128 * kCombPrefetchCols * sizeof(T)), attr_done);
     if (e != cudaSuccess) return e;
-    const int G = a.Hq / a.Hkv, nhc = (G + kCombHeads - 1) / kCombHeads;
-    return launch_ex(combine_kernel<T>, dim3(a.B, a.Hkv * nhc), dim3(kCombThreads), smem, st, pdl, b);
+    return launch_ex(combine_kernel<T>, dim3(a.Hq, a.B), dim3(kCombThreads), smem, st, pdl, b);
 }
 
 template <typename T>

@@ -51,13 +51,13 @@ slimkv_status check_shape(const slimkv_shape* s, int which) {
 }
 
 // Number of segments (runs of rows of one kind for one batch element): the latent
-// beacons and each raw source form one segment per batch element, so one partial slot
-// per segment plus kSlotCap covers every plan of the tensor-core path.
+// beacons form one segment, raw rows one per KV head (the tensor-core path's split),
+// so one partial slot per segment plus kSlotCap covers every plan.
 int n_segments(const slimkv_shape* s, int which) {
-    const int raw = s->W > 0 ? 1 : 0;
+    const int raw = s->W > 0 ? s->Hkv : 0;
     int per_b = 0;
     if (which == SLIMKV_LATENT) per_b = (s->N_b > 0) + raw;
-    if (which == SLIMKV_RECONSTRUCT) per_b = 1 + raw;   // materialised beacons are raw rows too
+    if (which == SLIMKV_RECONSTRUCT) per_b = s->Hkv + raw;   // materialised beacons are raw rows too
     if (which == SLIMKV_FULL_KV) per_b = raw;
     return per_b * s->B;
 }
@@ -76,13 +76,13 @@ WsLayout layout(const slimkv_shape* s, int which) {
     L.lat_img = off;
     if (lat) off = align_up(off + (size_t)s->B * lat_img_bytes(NP, s->r_k));
     L.raw_img = off;
-    off = align_up(off + (size_t)s->B * raw_img_bytes(NP, s->d));
-    L.flags = off;
-    off = align_up(off + sizeof(unsigned long long) * kMaxCtas);
+    off = align_up(off + (size_t)s->B * s->Hkv * raw_img_bytes(s->d));
     L.acc = off;
     off = align_up(off + sizeof(float) * (size_t)L.slots * s->Hq * L.Dmax);
     L.ml = off;
     off = align_up(off + sizeof(float) * (size_t)L.slots * 2 * s->Hq);
+    L.kind = off;
+    off = align_up(off + sizeof(int) * (size_t)L.slots);
     if (which == SLIMKV_RECONSTRUCT) {
         const size_t kv = (size_t)s->B * s->N_b * s->Hkv * s->d * elem_size(s->dtype);
         L.kb = off;
@@ -168,6 +168,7 @@ slimkv_status run_simt(const slimkv_shape* s, int which, const Ptrs& p, cudaStre
     a.q_lat = q_lat;
     a.acc = reinterpret_cast<float*>(ws + L.acc);
     a.ml = reinterpret_cast<float*>(ws + L.ml);
+    a.kind = reinterpret_cast<int*>(ws + L.kind);
     a.Dmax = L.Dmax;
     if (which == SLIMKV_RECONSTRUCT) {
         T* kb = reinterpret_cast<T*>(ws + L.kb);
@@ -218,11 +219,10 @@ slimkv_status run_simt(const slimkv_shape* s, int which, const Ptrs& p, cudaStre
     c.U_V = lat ? p.U_V : nullptr;
     c.acc = a.acc;
     c.ml = a.ml;
+    c.kind = a.kind;
     c.out = p.out;
-    // items of a batch element: latent first, then the raw sources
     const int per_b = a.nit_L + a.nit_R0 + a.nit_R1;
     for (int b = 0; b <= s->B; ++b) c.slot_begin[b] = b * per_b;
-    for (int b = 0; b < s->B; ++b) c.slot_mid[b] = b * per_b + a.nit_L;
     if (launch_combine<T>(c, st, false) != cudaSuccess) return SLIMKV_ERR_CUDA;
     return SLIMKV_OK;
 }
@@ -261,9 +261,9 @@ slimkv_status run(const slimkv_shape* s, int which, const Ptrs& p, void* stream)
         c.q_lat = reinterpret_cast<float*>(ws + L.q_lat);
         c.lat_img = reinterpret_cast<uint8_t*>(ws + L.lat_img);
         c.raw_img = reinterpret_cast<uint8_t*>(ws + L.raw_img);
-        c.flags = reinterpret_cast<unsigned long long*>(ws + L.flags);
         c.acc = reinterpret_cast<float*>(ws + L.acc);
         c.ml = reinterpret_cast<float*>(ws + L.ml);
+        c.kind = reinterpret_cast<int*>(ws + L.kind);
         c.kb = ws + L.kb;
         c.vb = ws + L.vb;
         c.slots = L.slots;

@@ -36,13 +36,13 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 // Workspace partition (byte offsets from the workspace base, 256-byte aligned).
 struct WsLayout {
-    size_t q_rot = 0;    // float [B, Hq, d]          rotated queries (SIMT path)
-    size_t q_lat = 0;    // float [B, Hq, r_k]        latent queries q . U_K^(g) (SIMT path)
+    size_t q_rot = 0;    // float [B, Hq, d]          rotated queries
+    size_t q_lat = 0;    // float [B, Hq, r_k]        latent queries q . U_K^(g)
     size_t acc = 0;      // float [slots, Hq, Dmax]   per-split value accumulators
     size_t ml = 0;       // float [slots, 2, Hq]      per-split running max (log2) and sum
+    size_t kind = 0;     // int   [slots]             what a partial covers (SlotKind)
     size_t lat_img = 0;  // bf16  [B][NP x r_k]       latent query image (tensor-core path)
-    size_t raw_img = 0;  // bf16  [B][2 NP x d]       raw query image, hi and lo parts (tensor-core path)
-    size_t flags = 0;    // u64   [kMaxCtas]          per-CTA flags of the tensor-core decode
+    size_t raw_img = 0;  // bf16  [B][Hkv][32 x d]    raw query images (tensor-core path)
     size_t kb = 0;       // T     [B, N_b, Hkv, d]    materialised beacon keys (reconstruct)
     size_t vb = 0;       // T     [B, N_b, Hkv, d]    materialised beacon values (reconstruct)
     size_t total = 0;
@@ -50,8 +50,15 @@ struct WsLayout {
     int Dmax = 0;        // accumulator width
 };
 
-// Partial slots of a batch element: the latent partials (acc r_v wide) come first,
-// then the raw partials (acc d wide); every partial covers all heads.
+// One "segment" is a run of key rows of one kind for one batch element. Rows of
+// a latent segment are beacons; rows of a raw segment are (token, KV head) pairs
+// flattened as token * Hkv + g, so one row is one d-vector of the cache.
+enum SegKind { kSegLatent = 0, kSegRaw0 = 1, kSegRaw1 = 2 };
+
+// What one partial slot holds: a latent accumulator (r_v wide) for every head, a
+// raw accumulator (d wide) for every head, or a raw accumulator for the heads of
+// one KV group g only (kSlotRawGroup + g; the other heads' rows are not written).
+enum SlotKind { kSlotLatent = 0, kSlotRawAll = 1, kSlotRawGroup = 2 };
 // Arguments of the SIMT split-decode kernel.
 struct SimtDecodeArgs {
     int B, Hq, Hkv, d, N_b, r_k, r_v;
@@ -66,6 +73,7 @@ struct SimtDecodeArgs {
     const float* q_lat;
     float* acc;
     float* ml;
+    int* kind;
     int Dmax;
     int rpi_L, rpi_R;            // rows (beacons / tokens) per item
     int nit_L, nit_R0, nit_R1;   // items per batch element
@@ -78,11 +86,9 @@ struct CombineArgs {
     const void* U_V;             // NULL when no latent partials exist
     const float* acc;
     const float* ml;
+    const int* kind;
     float* out;
-    // partial slots of batch element b: latent [slot_begin[b], slot_mid[b]),
-    // raw [slot_mid[b], slot_begin[b+1])
-    int slot_begin[kMaxB + 1];
-    int slot_mid[kMaxB];
+    int slot_begin[kMaxB + 1];   // partial slots of batch element b: [slot_begin[b], slot_begin[b+1])
 };
 
 // Arguments of the query kernel (RoPE + latent projection). The RoPE angle of pair
@@ -95,15 +101,15 @@ struct QprojArgs {
     const int32_t* q_pos;
     float* q_rot;                // [B, Hq, d]   RoPE(q) * scale_log2 (NULL: not written)
     float* q_lat;                // [B, Hq, r_k] RoPE(q) . U_K^(g) * scale_log2 (NULL: not written)
-    // Query operands of the tensor-core decode kernel, bf16, laid out exactly as that
-    // kernel's shared-memory operand (128-byte swizzled rows of 64 columns, for a
-    // 1024-byte aligned destination), so it can copy them in bulk:
-    uint8_t* lat_img;            // per b: NP rows, bf16 of q_lat[b] (rows of absent heads zero)
-    uint8_t* raw_img;            // per b: rows [0, NP) high, [NP, 2 NP) low parts of q_rot[b]
-    int NP;                      // heads of the images, rounded up to 16
+    // Query operands of the tensor-core decode kernel, as bf16 high / low parts laid
+    // out exactly as that kernel's shared-memory operand (128-byte swizzled rows of
+    // 64 columns, for a 1024-byte aligned destination), so it can copy them in bulk:
+    uint8_t* lat_img;            // per b: NP rows, bf16 of q_lat[b] (heads past Hq unused)
+    uint8_t* raw_img;            // per (b, g): rows [0, 16) high, [16, 32) low parts of q_rot of group g
+    int NP;                      // heads of the latent image, rounded up to 16
     int B, Hq, Hkv, d, r_k;
-    int rows;                    // (batch element, head of the group) rows per CTA
-    float scale_log2;            // score scale * log2(e), folded into every output
+    int nbb, hcn;                // batch elements and 32-head chunks per CTA row block
+    float scale_log2;            // score scale * log2(e), folded into both outputs
     unsigned long long turn[64];
 };
 
@@ -158,10 +164,9 @@ cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* 
                          float scale_log2, cudaStream_t st, bool pdl, uint8_t* lat_img = nullptr,
                          uint8_t* raw_img = nullptr, int NP = 0);
 
-// Bytes of the query images of one batch element (latent: NP rows of r_k rounded to 64;
-// raw: hi and lo parts, 2 NP rows of d).
+// Bytes of the query images (latent: per batch element; raw: per (batch element, KV group)).
 __host__ __device__ inline size_t lat_img_bytes(int NP, int r_k) { return (size_t)NP * ((r_k + 63) / 64 * 64) * 2; }
-__host__ __device__ inline size_t raw_img_bytes(int NP, int d) { return (size_t)2 * NP * d * 2; }
+__host__ __device__ inline size_t raw_img_bytes(int d) { return (size_t)2 * 16 * d * 2; }
 template <typename T>
 cudaError_t launch_simt_decode(const SimtDecodeArgs& a, cudaStream_t st);
 template <typename T>

@@ -6,31 +6,29 @@
 // RoPE(q) K_raw^T against the raw window, in one softmax; values aggregate as
 // (A C_V) U_V^(g)T + A V_raw, the latent aggregate taken before the up-projection.
 //
-// Work layout. A "segment" is all key rows of one kind for one batch element,
-// read as a 2-D [rows, width] bf16 matrix:
+// Work layout. A "segment" is all key rows of one kind for one batch element:
 //   latent: the N_b beacons of C_K[b] / C_V[b] (widths r_k / r_v), shared by
 //           every query head (one latent cache per layer for all KV heads);
-//   raw:    the W x Hkv rows of K[b] / V[b] (row = token * Hkv + KV head, width d).
-//           A raw row is scored by every head, and the softmax keeps only the
-//           heads of the row's own KV group, so one query image serves the whole
-//           window and raw tiles need no per-group split.
+//   raw:    the tokens of KV head g in K[b] / V[b] (width d), read by the G
+//           query heads of group g only; there is one raw segment per group.
 // A "tile" (unit of work) is 128 rows of a segment. A host planner gives every
 // CTA a contiguous, byte-balanced run of tiles (flash-decoding split of the
 // context); a run's part inside one segment is a "piece", which produces one
 // partial (m, l, acc) in the workspace, merged later by the combine kernel.
 //
-// Per tile, with the query operand Q (float32 query carrying scale * log2(e)):
-//   scores  S^T[row, col] = tile[row, :] . Q[col, :]   (M = 128 rows; one
-//           tcgen05.mma per 16-wide k-step). Latent tiles: Q = bf16 of the latent
-//           query, N = heads (latent scores are not peaked, so one bf16 part stays
-//           far inside the error bar). Raw tiles: Q = [q_hi ; q_lo], the bf16 high
-//           and low parts of the rotated query (raw keys can be large), N = 2 x
-//           heads, and the softmax adds the two parts;
-//   softmax P[row, head] = exp2(S^T - m_ref[head]) for the heads the row belongs
-//           to (all heads for a latent row, the row's KV group for a raw row),
-//           else 0; rounded to bf16 (relative error at most 2^-9 per weight,
-//           averaging out in the sums);
+// Per tile, with the query operand Q = [q_hi ; q_lo] (bf16 high and low parts of
+// the float32 query, which already carries scale * log2(e)), stacked along N:
+//   scores  S^T[row, (part, head)] = tile[row, :] . Q[(part, head), :]
+//           (one tcgen05.mma per 16-wide k-step, M = 128 rows, N = 2 x heads); the
+//           softmax adds the two parts. The latent query is rounded to bf16 in one
+//           part: latent scores are not peaked, so its rounding stays far inside the
+//           error bar, while the raw window (whose keys can be large) keeps both;
+//   softmax P[row, head] = exp2(S^T - m_ref[head]), rounded to bf16 (the rounding
+//           of P, unlike that of the query, stays far inside the error bar: the
+//           relative error of a weight is at most 2^-9 and averages out);
 //   values  acc^T[value dim, head] += tile_V[:, value dim]^T . P (M = 128 value dims).
+// Issuing few, wide MMAs matters: the issuing thread, not the tensor core, is the
+// limit for narrow ones.
 // m_ref is a lazy running maximum: it moves (and the TMEM accumulator is rescaled)
 // only when some score exceeds it by more than kLazy (log2 units), which one warp
 // vote per tile detects; so most tiles need no cross-row reduction at all.
@@ -42,30 +40,11 @@
 // the instruction cache, not the arithmetic, limits a kernel whose loops the
 // compiler unrolls freely, so runtime-trip loops stay rolled and rare paths are
 // out of line.
-//
-// Query images. The kernel makes its own query operands ("RoPE ... on all queries";
-// the projection is taken after GQA grouping): the rotated query of every head as bf16
-// high and low parts (raw image) and its projection q . U_K^(g) (latent image), one
-// pair of images per batch element in the workspace. The CTAs that work on a batch
-// element share the work: units of (KV group, 64 latent columns) and (KV group, raw
-// rows) are dealt out round-robin; each CTA publishes its units with a release flag,
-// and a CTA copies an image into shared memory once every CTA of that batch element
-// has flagged. The flags carry a token unique to the launch: a per-channel epoch in
-// library-owned device memory (zero when the library loads) that the launch's CTAs
-// read after the grid-dependency wait, the last of them advancing it; the host gives
-// every workspace its own channel. So no workspace word needs a known initial value.
-// While the first images are made, the producer already streams key and value tiles.
-//
-// Shared memory is kept below what one SM holds by about 30 KB whenever the shape
-// allows, so that a combine CTA can sit on the same SM: with programmatic dependent
-// launch, the next layer's decode CTAs take over an SM as soon as this layer's CTA
-// leaves it and stream their first tiles while the combine runs.
 #include <cuda.h>
 #include <string.h>
 
 #include <algorithm>
 #include <map>
-#include <memory>
 #include <mutex>
 #include <tuple>
 #include <vector>
@@ -84,64 +63,47 @@ constexpr int kTile = 128;            // rows per tile (MMA M)
 constexpr int kBox = 16384;           // one TMA box: 128 rows x 64 bf16 columns, 128B-swizzled
 constexpr int kSlot = 2 * kBox;       // ring slot: 128 rows x 128 columns
 constexpr int kThreads = 224;
-constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory one CTA may use
-// Preferred budget: leaves room on the SM for one query-projection and one combine CTA.
-constexpr int kSmemShared = 196 * 1024;
+constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory we may use per CTA
 constexpr int kNumKinds = 3;          // latent, raw source 0, raw source 1
+constexpr int kNG = 16;               // heads of a raw tile's query operand (the group's heads, padded)
 // m_ref moves only when a score exceeds it by more than this (log2 units). P values up
 // to 2^20 keep bf16's relative precision and stay far from fp32 overflow in the
 // accumulator and row sums, so a generous margin keeps the rescale path (which waits
 // for the previous value MMAs) off the common path even for peaked score distributions.
 constexpr float kLazy = 20.f;
 constexpr int kPAtom = 128 * 32;      // bytes of one 16-head column block of P per 128 rows (x 32 B)
+constexpr int kRBRaw = 2;             // 128-row blocks per raw tile: a raw tile is 256 tokens of one KV head
 constexpr int kR = 16;                // depth of the per-tile barrier rings
 constexpr int kMaxSlots = 16;
-constexpr int kChannels = 1024;       // launch-token channels (one per workspace in use)
-// Bytes each CTA pulls into L2 beyond its first two tiles when it starts (see the producer).
-constexpr int kPrefetchBytes = 384 * 1024;
-
-// Per-channel launch epochs and check-in counts (zero when the module loads).
-__device__ unsigned int g_chan_epoch[kChannels];
-__device__ unsigned int g_chan_count[kChannels];
 
 struct TcParams {
-    CUtensorMap tm[2 * kNumKinds];    // per kind: keys, values (3-D [B][rows][width])
+    CUtensorMap tm[2 * kNumKinds];    // per kind: keys, values (latent 3-D, raw 4-D)
     int B, Hq, Hkv, G;
     int rows[kNumKinds];              // rows of one segment (0 = kind absent)
     int tiles[kNumKinds];             // tiles of one segment
+    int ngroups[kNumKinds];           // segments of this kind per batch element
     int dk[kNumKinds], dv[kNumKinds]; // key / value width
+    int rb[kNumKinds];                // 128-row blocks per tile (1 latent, kRBRaw raw)
     int tiles_per_b;
-    uint8_t* lat_img;                 // query images (operand layout: latent bf16, raw bf16 hi / lo)
-    uint8_t* raw_img;
+    const uint8_t* lat_img;           // query images (operand layout: latent bf16, raw bf16 hi / lo)
+    const uint8_t* raw_img;
     uint32_t lat_img_bytes, raw_img_bytes;
     float* acc;                       // [slots, Hq, Dmax]
     float* ml;                        // [slots, 2, Hq]
+    int* kind;                        // [slots]
     int Dmax;
     int nslot;                        // ring slots of 32 KB
     int accbuf;                       // TMEM accumulator buffers (1 or 2)
     int accstride;                    // TMEM columns of one accumulator buffer
     uint32_t off_q, off_p, off_bar, off_red;
     uint32_t tmem_cols;
-    // query images, made by the kernel
-    const __nv_bfloat16* q;           // [B, Hq, d] queries before RoPE
-    const __nv_bfloat16* U_K;         // [Hkv * d, r_k] (latent images only)
-    const int32_t* q_pos;             // [B]
-    unsigned long long* flags;        // [gridDim.x] per-CTA "images published" flags (workspace)
-    int ch;                           // launch-token channel
-    int r_k;
-    int ncb;                          // latent image units per KV group (64 columns each; 0: no latent image)
-    int pf_tiles;                     // tiles after the first two whose boxes are pulled into L2 at the start
-    int img_raw;                      // 1: raw images are needed
-    float scale_log2;                 // score scale * log2(e), folded into both images
-    unsigned long long turn[64];      // RoPE angles per pair as 64-bit fractions of a turn
-    short cta_first[kMaxB], cta_last[kMaxB];   // CTAs whose runs touch batch element b
     int u_begin[kMaxCtas + 1];        // CTA i owns units (tiles) [u_begin[i], u_begin[i+1])
     int slot_base[kMaxCtas];          // first partial slot of CTA i
 };
 
 // The run of a CTA's units that starts at u and stays inside one segment.
 struct Piece {
-    int b, k, t0, n;
+    int b, k, g, t0, n;
 };
 __device__ __forceinline__ Piece piece_at(const TcParams& p, int u, int u1) {
     Piece r;
@@ -149,12 +111,14 @@ __device__ __forceinline__ Piece piece_at(const TcParams& p, int u, int u1) {
     int t = u - r.b * p.tiles_per_b;
     int k = 0;
     for (; k < kNumKinds - 1; ++k) {
-        if (t < p.tiles[k]) break;
-        t -= p.tiles[k];
+        const int span = p.ngroups[k] * p.tiles[k];
+        if (t < span) break;
+        t -= span;
     }
     r.k = k;
-    r.t0 = t;
-    r.n = min(u1 - u, p.tiles[k] - t);
+    r.g = t / p.tiles[k];
+    r.t0 = t - r.g * p.tiles[k];
+    r.n = min(u1 - u, p.tiles[k] - r.t0);
     return r;
 }
 
@@ -194,14 +158,15 @@ struct TileIter {
 // Ring position s (< 2 n) modulo n.
 __device__ __forceinline__ int ring_wrap(int s, int n) { return s >= n ? s - n : s; }
 
-// Query operand image of a piece: the latent or the raw image of its batch element.
+// Query operand image of a piece: the latent image of its batch element, or the raw
+// image of its (batch element, KV group).
 __device__ __forceinline__ void query_image(const TcParams& p, const Piece& pc, const uint8_t*& src,
                                             uint32_t& bytes) {
     if (pc.k == 0) {
         src = p.lat_img + (size_t)pc.b * p.lat_img_bytes;
         bytes = p.lat_img_bytes;
     } else {
-        src = p.raw_img + (size_t)pc.b * p.raw_img_bytes;
+        src = p.raw_img + ((size_t)pc.b * p.Hkv + pc.g) * p.raw_img_bytes;
         bytes = p.raw_img_bytes;
     }
 }
@@ -220,7 +185,6 @@ struct Bars {
     uint64_t* accfree;
     uint64_t* drain;
     uint64_t* qready;   // the CTA's first query image landed                       [TMA tx]
-    uint64_t* tok;      // the launch token is in shared memory                     [1 arrival]
 };
 __device__ __forceinline__ uint32_t ph_of(int j) { return ((uint32_t)j / kR) & 1u; }
 
@@ -238,11 +202,14 @@ struct SoftCtx {
     int aw;               // TMEM columns per 128 value rows of the accumulator
 };
 
-// TMEM columns of one score buffer (hi and lo columns of every head for raw tiles)
-// and bytes of one P buffer (NP heads x 128 rows, bf16).
+
+// TMEM columns of one score buffer: hi and lo scores (2 x NS columns) for each of
+// the tile's row blocks; at least 64.
 template <int NP> struct SBuf {
-    static constexpr int W = 2 * NP;
-    static constexpr int PB = NP * 256;
+    // latent tiles: NP score columns; raw tiles: hi and lo columns of kNG heads per row block
+    static constexpr int W = NP > 2 * kNG * kRBRaw ? NP : 2 * kNG * kRBRaw;
+    // bytes of one P buffer: NP heads x 128 rows (latent) or kNG heads x 256 rows (raw), bf16
+    static constexpr int PB = (NP > kNG * kRBRaw ? NP : kNG * kRBRaw) * 256;
 };
 
 // Scores of 16 heads of this thread's row: hi + lo parts (raw tiles) or one part.
@@ -256,13 +223,6 @@ __device__ __forceinline__ void load_scores(uint32_t tS, float (&x)[16]) {
     } else {
         ptx::tmem_ld16(tS, x);
     }
-}
-
-// Whether head h is scored by this thread's row: every head for a latent row, the
-// heads [hlo, hlo + hn) of the row's KV group for a raw row (LO).
-template <bool LO>
-__device__ __forceinline__ bool head_on(int h, int hlo, int hn) {
-    return !LO || (unsigned)(h - hlo) < (unsigned)hn;
 }
 
 // Reduction across the 32 lanes of 16 values per lane, one result per value:
@@ -297,28 +257,34 @@ __device__ __forceinline__ float warp_reduce16(float* v, int lane) {
 // the rescale factors alpha = exp2(m_old - m_new), and, when the accumulator already
 // holds earlier tiles of the piece (nMB > 0), the rescale of its columns once the
 // previous value MMAs are done. All 128 softmax threads call it together.
-template <int NP, bool LO>
+template <int NS, int NP, int RB, bool LO>
 __device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* alpha_s, uint64_t* vfree,
-                                             volatile int* abort, uint32_t tS, uint32_t t_acc_lane, bool row_ok,
-                                             int hlo, int hn, int j, int nMB, int aw, int tid, int lane, int wq) {
-    // per-head maximum over this warp's scored rows, then over the four warps
-    // (the TMEM loads are warp-collective: every lane loads, unscored entries are masked after)
-    float x[NP];
+                                             volatile int* abort, uint32_t tS0, uint32_t t_acc_lane, int row0,
+                                             int rows, int j, int nMB, int aw, int tid, int lane, int wq) {
+    // per-head maximum over this warp's valid rows, then over the four warps
+    float x[NS];
 #pragma unroll
-    for (int hc = 0; hc < NP / 16; ++hc) {
-        float sc[16];
-        load_scores<LO, NP>(tS + hc * 16, sc);
+    for (int h = 0; h < NS; ++h) x[h] = -INFINITY;
+    // (the TMEM loads are warp-collective: every lane loads, invalid rows are masked after)
+#pragma unroll 1
+    for (int rb = 0; rb < RB; ++rb) {
+        const bool valid = row0 + rb * 128 < rows;
+        const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            x[hc * 16 + i] = (row_ok && head_on<LO>(hc * 16 + i, hlo, hn)) ? sc[i] : -INFINITY;
+        for (int hc = 0; hc < NS / 16; ++hc) {
+            float sc[16];
+            load_scores<LO, NS>(tS + hc * 16, sc);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[hc * 16 + i] = valid ? fmaxf(x[hc * 16 + i], sc[i]) : x[hc * 16 + i];
+        }
     }
 #pragma unroll
-    for (int hc = 0; hc < NP / 16; ++hc) {
+    for (int hc = 0; hc < NS / 16; ++hc) {
         const float wmax = warp_reduce16<true>(x + hc * 16, lane);
         if (lane < 16) red[wq * NP + hc * 16 + lane] = wmax;
     }
     ptx::named_bar(1, 128);
-    if (tid < NP) {
+    if (tid < NS) {
         const float M = fmaxf(fmaxf(red[tid], red[NP + tid]), fmaxf(red[2 * NP + tid], red[3 * NP + tid]));
         const float mo = m_ref_s[tid];
         float a = 1.f;
@@ -335,7 +301,7 @@ __device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* 
 #pragma unroll 1
         for (int cc = 0; cc < nMB; ++cc) {
 #pragma unroll 1
-            for (int hc = 0; hc < NP / 16; ++hc) {
+            for (int hc = 0; hc < NS / 16; ++hc) {
                 float v[16];
                 const uint32_t ta = t_acc_lane + cc * aw + hc * 16;
                 ptx::tmem_ld16(ta, v);
@@ -347,363 +313,156 @@ __device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* 
     }
 }
 
-// Softmax of tile j of the current piece (128 rows, NP heads). row_ok: this thread's
-// row lies inside the segment; [hlo, hlo + hn): the heads a raw row belongs to. Reads
-// S^T from TMEM (hi at +0 and lo at +NP for raw tiles), writes P as the MN-major B
-// operand of the value MMA (16-head column blocks of 128 rows x 32 bytes, 32-byte
-// swizzle), then signals vready[j]. Every head column is processed alike, without
-// per-head branches: the query rows of absent heads are zero, so their scores are
-// finite, and their columns are never written out.
-template <int NP, bool LO>
-__device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, bool row_ok, int hlo, int hn, bool has_prev,
-                                             float (&l_part)[NP]) {
-    const float* mref = c.m_ref_s;   // reference maxima (shared; every thread reads the same words)
+// Softmax of tile j of the current piece: RB row blocks of 128 rows, NS heads wide;
+// row0 is this thread's row index (segment-wide) in block 0. Reads S^T from TMEM
+// (block rb at +rb*NS, or hi at +rb*2NS and lo at +rb*2NS+NS for raw tiles), writes P
+// as the MN-major B operand of the value MMA (16-head column blocks of 128*RB rows x
+// 32 bytes, 32-byte swizzle), then signals vready[j]. Every head column is processed
+// alike: the query rows of absent heads are zero, so their scores are finite and
+// their columns, which are never written out, cost no branches.
+template <int NS, int NP, int RB, bool LO>
+__device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, int rows, bool has_prev,
+                                             float (&l_part)[NP], float (&mref)[NP]) {
     constexpr int SW = SBuf<NP>::W;
     const int jr = j % kR;
     ptx::mbar_wait(&c.bar.kfree[jr], ph_of(j), c.abort);   // S(j) complete
     ptx::tc_fence_after();
-    const uint32_t tS = c.t_S + c.lane_off + (j & 1) * SW;
+    const uint32_t tS0 = c.t_S + c.lane_off + (j & 1) * SW;
 
-    // pass 1: does a score of this thread's row exceed its head's reference by more
+    // pass 1: does a score of this thread's rows exceed its head's reference by more
     // than kLazy? (The first tile of a piece has no reference yet: it always takes
     // the rare path, without the vote.)
     bool slow = !has_prev;
     if (has_prev) {
-        float dm = -INFINITY;
+        float dmax = -INFINITY;
 #pragma unroll
-        for (int hc = 0; hc < NP / 16; ++hc) {
-            float sc[16];
-            load_scores<LO, NP>(tS + hc * 16, sc);
+        for (int rb = 0; rb < RB; ++rb) {
+            const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
+            float dm = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float dd = sc[i] - mref[hc * 16 + i];
-                dm = head_on<LO>(hc * 16 + i, hlo, hn) ? fmaxf(dm, dd) : dm;
+            for (int hc = 0; hc < NS / 16; ++hc) {
+                float sc[16];
+                load_scores<LO, NS>(tS + hc * 16, sc);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) dm = fmaxf(dm, sc[i] - mref[hc * 16 + i]);
             }
+            dmax = (row0 + rb * 128 < rows) ? fmaxf(dmax, dm) : dmax;
         }
-        const bool any = __any_sync(0xffffffffu, row_ok && dm > kLazy);
+        const bool any = __any_sync(0xffffffffu, dmax > kLazy);
         volatile int* fl = c.flags + (j & 1) * 4;
         if (c.lane == 0) fl[c.wq] = any ? 1 : 0;
         ptx::named_bar(1, 128);
         slow = (fl[0] | fl[1] | fl[2] | fl[3]) != 0;
     }
     if (slow) {
-        softmax_new_ref<NP, LO>(c.red, c.m_ref_s, c.alpha_s, c.bar.vfree, c.abort, tS, c.t_accp + c.lane_off,
-                                row_ok, hlo, hn, j, has_prev ? c.nMB : 0, c.aw, c.tid, c.lane, c.wq);
+        softmax_new_ref<NS, NP, RB, LO>(c.red, c.m_ref_s, c.alpha_s, c.bar.vfree, c.abort, tS0, c.t_accp + c.lane_off,
+                                        row0, rows, j, has_prev ? c.nMB : 0, c.aw, c.tid, c.lane, c.wq);
 #pragma unroll
-        for (int h = 0; h < NP; ++h) l_part[h] *= c.alpha_s[h];
+        for (int h = 0; h < NS; ++h) {
+            mref[h] = c.m_ref_s[h];
+            l_part[h] *= c.alpha_s[h];
+        }
     }
 
     // pass 2: probabilities against the reference, rounded to bf16; the P buffer
     // (j & 1) is free once the value MMAs of tile j - 2 are done
     if (j >= 2) ptx::mbar_wait(&c.bar.vfree[(j - 2) % kR], ph_of(j - 2), c.abort);
     uint8_t* phi = c.pbuf + (j & 1) * SBuf<NP>::PB;
-    const int row = c.myrow;
-    const uint32_t row_off = row * 32;
-    const uint32_t sw = ((row >> 2) & 1) << 4;
 #pragma unroll
-    for (int hc = 0; hc < NP / 16; ++hc) {
-        float sc[16];
-        load_scores<LO, NP>(tS + hc * 16, sc);
-        uint32_t pk[8];
+    for (int rb = 0; rb < RB; ++rb) {
+        const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
+        const bool valid = row0 + rb * 128 < rows;
+        const int row = rb * 128 + c.myrow;
+        const uint32_t row_off = row * 32;
+        const uint32_t sw = ((row >> 2) & 1) << 4;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int h = hc * 16 + 2 * i;
-            const float e0 = exp2f(sc[2 * i] - mref[h]);
-            const float e1 = exp2f(sc[2 * i + 1] - mref[h + 1]);
-            const float p0 = (row_ok && head_on<LO>(h, hlo, hn)) ? e0 : 0.f;
-            const float p1 = (row_ok && head_on<LO>(h + 1, hlo, hn)) ? e1 : 0.f;
-            l_part[h] += p0;
-            l_part[h + 1] += p1;
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        for (int hc = 0; hc < NS / 16; ++hc) {
+            float sc[16];
+            load_scores<LO, NS>(tS + hc * 16, sc);
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int h = hc * 16 + 2 * i;
+                const float p0 = valid ? exp2f(sc[2 * i] - mref[h]) : 0.f;
+                const float p1 = valid ? exp2f(sc[2 * i + 1] - mref[h + 1]) : 0.f;
+                l_part[h] += p0;
+                l_part[h + 1] += p1;
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            const uint32_t o0 = hc * (kPAtom * RB) + row_off + (0u ^ sw);
+            const uint32_t o1 = hc * (kPAtom * RB) + row_off + (16u ^ sw);
+            *reinterpret_cast<uint4*>(phi + o0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(phi + o1) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
-        const uint32_t o0 = hc * kPAtom + row_off + (0u ^ sw);
-        const uint32_t o1 = hc * kPAtom + row_off + (16u ^ sw);
-        *reinterpret_cast<uint4*>(phi + o0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(phi + o1) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
     ptx::tc_fence_before();          // TMEM reads / writes of this tile before the signal
     ptx::fence_proxy_async_smem();   // P stores visible to the tensor core
     ptx::mbar_arrive(&c.bar.vready[jr]);
 }
 
-// Partial write-out of a piece, out of line (once per piece): (m, l) of the real
-// heads from the per-warp row-sum reductions in `red`, and the accumulator columns
-// read from TMEM.
-template <int NP>
-__device__ __noinline__ void write_partial_acc(float* ml, float* acc, const float* red, const float* m_ref_s,
-                                               int Hq, int Dmax, int slot, int dv, int nMB, int aw,
-                                               uint32_t t_acc_lane, int tid, int myrow) {
-    if (tid < Hq) {
+// Partial write-out of a piece, out of line (once per piece): (m, l) of the piece's
+// real heads from the per-warp row-sum reductions in `red`, and the accumulator
+// columns read from TMEM.
+template <int NS, int NP>
+__device__ __noinline__ void write_partial_acc(float* ml, float* acc, int* kindp, const float* red,
+                                               const float* m_ref_s, int Hq, int Dmax, int slot, int kind, int h0,
+                                               int nvalid, int dv, int nMB, int aw, uint32_t t_acc_lane,
+                                               int tid, int myrow) {
+    if (tid < nvalid) {
         const float L = red[tid] + red[NP + tid] + red[2 * NP + tid] + red[3 * NP + tid];
-        ml[((size_t)slot * 2) * Hq + tid] = m_ref_s[tid];
-        ml[((size_t)slot * 2 + 1) * Hq + tid] = L;
+        ml[((size_t)slot * 2) * Hq + h0 + tid] = m_ref_s[tid];
+        ml[((size_t)slot * 2 + 1) * Hq + h0 + tid] = L;
     }
+    if (tid == 0) kindp[slot] = kind;
 #pragma unroll 1
     for (int cc = 0; cc < nMB; ++cc) {
         const int r = cc * 128 + myrow;
 #pragma unroll 1
-        for (int hc = 0; hc < NP / 16; ++hc) {
+        for (int hc = 0; hc < NS / 16; ++hc) {
             float v[16];
             const uint32_t ta = t_acc_lane + cc * aw + hc * 16;
             ptx::tmem_ld16(ta, v);
             if (r < dv) {
-                float* dst = acc + ((size_t)slot * Hq + hc * 16) * Dmax + r;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (hc * 16 + i < Hq) dst[(size_t)i * Dmax] = v[i];
+                for (int i = 0; i < 16; ++i) {
+                    const int h = hc * 16 + i;
+                    if (h < nvalid) acc[((size_t)slot * Hq + h0 + h) * Dmax + r] = v[i];
+                }
             }
         }
     }
 }
 
 // End of a piece: reduce the row sums, write (m, l) and the accumulator columns of
-// the real heads to partial slot `slot`.
-template <int NP>
-__device__ __forceinline__ void write_partial(const TcParams& p, const SoftCtx& c, int slot, int dv,
-                                              float (&l_part)[NP]) {
-    float v[NP];
+// the piece's real heads to partial slot `slot`.
+template <int NS, int NP>
+__device__ __forceinline__ void write_partial(const TcParams& p, const SoftCtx& c, int slot, int kind,
+                                              int h0, int nvalid, int dv, float (&l_part)[NP]) {
+    float v[NS];
 #pragma unroll
-    for (int h = 0; h < NP; ++h) v[h] = l_part[h];
+    for (int h = 0; h < NS; ++h) v[h] = l_part[h];
 #pragma unroll
-    for (int hc = 0; hc < NP / 16; ++hc) {
+    for (int hc = 0; hc < NS / 16; ++hc) {
         const float wsum = warp_reduce16<false>(v + hc * 16, c.lane);
         if (c.lane < 16) c.red[c.wq * NP + hc * 16 + c.lane] = wsum;
     }
     ptx::named_bar(1, 128);
-    write_partial_acc<NP>(p.ml, p.acc, c.red, c.m_ref_s, p.Hq, p.Dmax, slot, dv, c.nMB, c.aw,
-                          c.t_accp + c.lane_off, c.tid, c.myrow);
-}
-
-
-// ------------------------------------------------------------------ query images
-
-// splitmix64 finaliser: spreads (channel, epoch) over 64 bits.
-__device__ __forceinline__ unsigned long long mix64(unsigned long long x) {
-    x += 0x9E3779B97F4A7C15ull;
-    x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
-    x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
-    return x ^ (x >> 31);
-}
-
-// The launch's token (one thread per CTA, after the grid-dependency wait, when the
-// previous launch on this channel has completed): every CTA reads the channel's epoch
-// and then checks in; the last to check in resets the count and advances the epoch for
-// the next launch. The check-in is acquire-release, so no CTA can read an epoch that
-// the last one already advanced. The token is never 0.
-__device__ __forceinline__ unsigned long long launch_token(int ch) {
-    const unsigned int e = *reinterpret_cast<volatile unsigned int*>(&g_chan_epoch[ch]);
-    unsigned int old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(&g_chan_count[ch]) : "memory");
-    if (old == gridDim.x - 1) {
-        *reinterpret_cast<volatile unsigned int*>(&g_chan_count[ch]) = 0u;
-        *reinterpret_cast<volatile unsigned int*>(&g_chan_epoch[ch]) = e + 1u;
-    }
-    return mix64(((unsigned long long)(unsigned)ch << 32) | e) | 1ull;
-}
-
-__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-// Order this thread's generic-proxy global writes (or reads' visibility) with later
-// async-proxy (bulk copy) accesses.
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Whole warp: wait until the flags of CTAs [lo, hi] all hold `tok` (bounded; false
-// and *abort raised if the wait runs out or *abort is raised elsewhere).
-__device__ __noinline__ bool poll_flags_warp(const unsigned long long* flags, int lo, int hi, unsigned long long tok,
-                                             volatile int* abort) {
-    const int lane = threadIdx.x & 31;
-    const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t it = 0;; ++it) {
-        bool ok = true;
-        for (int c = lo + lane; c <= hi; c += 32) ok = ok && ld_acquire(flags + c) == tok;
-        if (__all_sync(0xffffffffu, ok)) return true;
-        __nanosleep(64);   // leave issue slots and memory bandwidth to the working warps
-        if (*abort) return false;
-        if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
-            *abort = 1;
-            return false;
-        }
-    }
-}
-// One thread: the same wait, eight flags at a time.
-__device__ __noinline__ bool poll_flags_thread(const unsigned long long* flags, int lo, int hi, unsigned long long tok,
-                                               volatile int* abort) {
-    const uint64_t t0 = ptx::globaltimer();
-    int c = lo;
-    while (c <= hi) {
-        unsigned long long v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = c + k <= hi ? ld_acquire(flags + c + k) : tok;
-        int k = 0;
-        while (k < 8 && v[k] == tok) ++k;
-        c += k;
-        if (k < 8 && c <= hi) {
-            __nanosleep(64);
-            if (*abort) return false;
-            if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
-                *abort = 1;
-                return false;
-            }
-        }
-    }
-    return true;
-}
-
-// 16-byte asynchronous global -> shared copy (completion via cp_async_wait_all).
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ptx::smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-// Stage the 64-latent-column block cb of U_K^(g) (rows k < 128, 128 bytes each; columns
-// past r_k are left alone) into `dst`, by the 128 softmax threads (tid).
-__device__ __forceinline__ void stage_ublock(const TcParams& p, int g, int cb, uint8_t* dst, int tid) {
-    const __nv_bfloat16* base = p.U_K + (size_t)g * 128 * p.r_k + cb * 64;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int ch = tid + i * 128, row = ch >> 3, part = ch & 7;
-        if (cb * 64 + part * 8 < p.r_k) cp_async16(dst + row * 128 + part * 16, base + (size_t)row * p.r_k + part * 8);
-    }
-    cp_async_commit();
-}
-
-// Image units of batch element b, round-robin over the CTAs that work on b: per KV
-// group g, ncb latent units (64 columns of q . U_K^(g) for the group's heads) and, if
-// raw images are needed, one raw unit (the group's rows of the hi / lo image). Run by
-// the 128 softmax threads (tid); qr is shared scratch for G x d floats, ub for one
-// 64-column block of U_K^(g) (128 rows x 128 bytes). `staged` (g * ncb + cb, or -1)
-// names a block already being copied into ub.
-__device__ __noinline__ void make_image_units(const TcParams& p, int cta, int b, float* qr, uint8_t* ub, int& staged,
-                                              int tid) {
-    const int G = p.G, NP = (p.Hq + 15) / 16 * 16;
-    const int per_g = p.ncb + p.img_raw;
-    const int nunits = p.Hkv * per_g;
-    const int n_b = p.cta_last[b] - p.cta_first[b] + 1;
-    const unsigned long long pos = (unsigned long long)(long long)p.q_pos[b];
-#pragma unroll 1
-    for (int u = cta - p.cta_first[b]; u < nunits; u += n_b) {
-        const int g = u / per_g, kind = u - g * per_g;
-        ptx::named_bar(1, 128);   // the previous unit is done with qr and ub
-        if (kind < p.ncb) {
-            if (staged != g * p.ncb + kind) stage_ublock(p, g, kind, ub, tid);
-            staged = -1;
-        }
-        // rotated, scaled query rows of the group's heads (pair i = item % 64)
-#pragma unroll 1
-        for (int it = tid; it < G * 64; it += 128) {
-            const int hh = it >> 6, i = it & 63;
-            const __nv_bfloat16* src = p.q + ((size_t)b * p.Hq + g * G + hh) * 128;
-            const float x1 = __bfloat162float(src[i]), x2 = __bfloat162float(src[i + 64]);
-            // the angle reduced to a signed fraction of a turn (exact 64-bit wrap-around)
-            const long long frac = (long long)(pos * p.turn[i]);
-            float sn, cs;
-            sincospif((float)frac * 1.0842021724855044e-19f, &sn, &cs);   // x 2^-63: half-turns
-            qr[hh * 128 + i] = (x1 * cs - x2 * sn) * p.scale_log2;
-            qr[hh * 128 + i + 64] = (x2 * cs + x1 * sn) * p.scale_log2;
-        }
-        cp_async_wait_all();
-        ptx::named_bar(1, 128);
-        if (kind < p.ncb) {
-            // latent unit: column kind * 64 + (tid % 64) of q . U_K^(g), heads tid / 64, + 2, ...
-            const int cl = tid & 63, col = kind * 64 + cl;
-            uint8_t* img = p.lat_img + (size_t)b * p.lat_img_bytes;
-            if (col < p.r_k) {
-                const __nv_bfloat16* uc = reinterpret_cast<const __nv_bfloat16*>(ub) + cl;
-#pragma unroll 1
-                for (int hh = tid >> 6; hh < G; hh += 2) {
-                    const float4* q4 = reinterpret_cast<const float4*>(qr + hh * 128);
-                    float acc = 0.f;
-#pragma unroll 8
-                    for (int k4 = 0; k4 < 32; ++k4) {
-                        const float4 qv = q4[k4];
-                        acc = fmaf(qv.x, __bfloat162float(uc[(4 * k4 + 0) * 64]), acc);
-                        acc = fmaf(qv.y, __bfloat162float(uc[(4 * k4 + 1) * 64]), acc);
-                        acc = fmaf(qv.z, __bfloat162float(uc[(4 * k4 + 2) * 64]), acc);
-                        acc = fmaf(qv.w, __bfloat162float(uc[(4 * k4 + 3) * 64]), acc);
-                    }
-                    *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(g * G + hh, col, NP)) =
-                        __float2bfloat16_rn(acc);
-                }
-                if (g == 0)   // rows of absent heads are zero
-                    for (int h = p.Hq + (tid >> 6); h < NP; h += 2)
-                        *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(h, col, NP)) = __float2bfloat16_rn(0.f);
-            }
-        } else {
-            // raw unit: the group's rows of the raw image, bf16 high part and the bf16 of the rest
-            uint8_t* img = p.raw_img + (size_t)b * p.raw_img_bytes;
-#pragma unroll 1
-            for (int it = tid; it < G * 16; it += 128) {
-                const int hh = it >> 4, un = it & 15;
-                const float* src = qr + hh * 128 + un * 8;
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(src[2 * k], src[2 * k + 1]);
-                    const float2 hf = __bfloat1622float2(h2);
-                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(src[2 * k] - hf.x, src[2 * k + 1] - hf.y);
-                    hi[k] = *reinterpret_cast<const uint32_t*>(&h2);
-                    lo[k] = *reinterpret_cast<const uint32_t*>(&l2);
-                }
-                const int h = g * G + hh;
-                *reinterpret_cast<uint4*>(img + ptx::sw128_offset(h, un * 8, 2 * NP)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(img + ptx::sw128_offset(NP + h, un * 8, 2 * NP)) =
-                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-            if (g == 0) {
-                const int npad = NP - p.Hq;
-#pragma unroll 1
-                for (int it = tid; it < 2 * npad * 16; it += 128) {
-                    const int pr = it >> 4, un = it & 15;
-                    const int row = pr < npad ? p.Hq + pr : NP + p.Hq + (pr - npad);
-                    *reinterpret_cast<uint4*>(img + ptx::sw128_offset(row, un * 8, 2 * NP)) = make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-        }
-    }
-}
-
-// The first latent unit this CTA makes (batch element and unit), or false if none.
-__device__ __forceinline__ bool first_latent_unit(const TcParams& p, int cta, int b_lo, int b_hi, int& g, int& cb) {
-    const int per_g = p.ncb + p.img_raw;
-    if (p.ncb == 0) return false;
-    for (int b = b_lo; b <= b_hi; ++b) {
-        const int n_b = p.cta_last[b] - p.cta_first[b] + 1;
-        for (int u = cta - p.cta_first[b]; u < p.Hkv * per_g; u += n_b) {
-            const int kind = u % per_g;
-            if (kind < p.ncb) {
-                g = u / per_g;
-                cb = kind;
-                return true;
-            }
-        }
-    }
-    return false;
+    write_partial_acc<NS, NP>(p.ml, p.acc, p.kind, c.red, c.m_ref_s, p.Hq, p.Dmax, slot, kind, h0, nvalid, dv, c.nMB,
+                              c.aw, c.t_accp + c.lane_off, c.tid, c.myrow);
 }
 
 // NP: query heads rounded up to 16 (a template parameter, so the MMA issue sequences
 // are straight-line code: a conditional branch between two tcgen05.mma instructions
 // costs the issuing thread tens of cycles per MMA).
-// At most 200 registers per thread: registers are allocated to warps in groups of four,
-// so the 7 warps of a CTA hold 8 warps' worth, and a combine CTA (8 warps of 48) must
-// still fit beside it on the SM.
 template <int NP>
-__global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
     uint8_t* qbuf = smem + p.off_q;          // query operand of the current piece (image copy)
-    uint8_t* pbuf = smem + p.off_p;          // [2][NP/16 blocks][128 rows x 32 B] bf16
+    uint8_t* pbuf = smem + p.off_p;          // [2][NP/16 blocks][128 * RB rows x 32 B] bf16
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     float* red = reinterpret_cast<float*>(smem + p.off_red);   // [4][NP]
     float* m_ref_s = red + 4 * NP;                             // [NP]
@@ -713,7 +472,6 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
     volatile int* flag = reinterpret_cast<volatile int*>(alpha_s + NP);
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(alpha_s + NP) + 12;
     int* owner = reinterpret_cast<int*>(alpha_s + NP) + 16;    // [kMaxSlots] producer's slot owners
-    volatile unsigned long long* tok_s = reinterpret_cast<volatile unsigned long long*>(alpha_s + NP) + 16;
 
     Bars bar;
     bar.kready = bars;
@@ -723,7 +481,6 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
     bar.accfree = bars + 4 * kR;
     bar.drain = bars + 4 * kR + 2;      // [0] score issuer, [1] value issuer
     bar.qready = bars + 4 * kR + 4;
-    bar.tok = bars + 4 * kR + 5;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
@@ -742,7 +499,6 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
         ptx::mbar_init(&bar.drain[0], 1);
         ptx::mbar_init(&bar.drain[1], 1);
         ptx::mbar_init(bar.qready, 1);
-        ptx::mbar_init(bar.tok, 1);
         #pragma unroll 1
         for (int i = 0; i < 9; ++i) flag[i] = 0;
         #pragma unroll 1
@@ -775,13 +531,10 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
                 if (p.rows[i >> 1] > 0) ptx::tma_prefetch_desc(&p.tm[i]);
             int pos = 0;                     // ring position of the next slot
             const uint64_t pol = ptx::policy_evict_first();   // the cache is streamed once
-            // the first piece's images were checked by the score issuer before its first MMA
-            int flags_b = u0 < u1 ? u0 / p.tiles_per_b : -1;
-            unsigned long long tok = 0;
+            bool pdl_done = false;
             // pending query-image copy (pieces after the first)
             bool q_pend = false;
             int q_tile = 0, q_after = 0;     // kready tile; tile whose score MMAs must finish first
-            int q_b = 0;                     // batch element of the pending image
             const uint8_t* q_src = nullptr;
             uint32_t q_bytes = 0;
             auto try_q = [&](bool block) {
@@ -791,16 +544,10 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
                 } else if (!ptx::mbar_test(&bar.kfree[q_after % kR], ph_of(q_after))) {
                     return;
                 }
-                if (q_b != flags_b) {
-                    // another batch element: wait until its images are published
-                    if (tok == 0) {
-                        ptx::mbar_wait(bar.tok, 0, abort_flag);
-                        tok = *tok_s;
-                    }
-                    poll_flags_thread(p.flags, p.cta_first[q_b], p.cta_last[q_b], tok, abort_flag);
-                    flags_b = q_b;
+                if (!pdl_done) {
+                    pdl_wait();              // the images come from the preceding kernel
+                    pdl_done = true;
                 }
-                fence_proxy_async_global();
                 ptx::bulk_load(qbuf, q_src, q_bytes, &bar.kready[q_tile % kR]);
                 q_pend = false;
             };
@@ -829,37 +576,16 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
             kit.init(p, u0, u1);
             vit.init(p, u0, u1);
             int kiss = 0, viss = 0;   // tiles whose K / V loads were issued
-            // Once the first two key tiles are on their way, pull the next pf_tiles tiles into
-            // L2: they stream from HBM while the query images are made (the ring alone
-            // would fill and stall), and their ring loads later hit L2.
-            bool pf_done = p.pf_tiles == 0;
-            auto prefetch_l2 = [&]() {
-                TileIter pf;
-                pf.init(p, u0, u1);
-                if (pf.valid()) pf.next();
-                if (pf.valid()) pf.next();
-#pragma unroll 1
-                for (int n = 0; n < p.pf_tiles && pf.valid(); ++n, pf.next()) {
-                    const int k = pf.pc.k;
-#pragma unroll 1
-                    for (int part = 0; part < 2; ++part) {
-                        const int w = part ? p.dv[k] : p.dk[k];
-#pragma unroll 1
-                        for (int col = 0; col < w; col += 64)
-                            ptx::tma_prefetch_3d(&p.tm[2 * k + part], col, pf.t * kTile, pf.pc.b);
-                    }
-                }
-                pf_done = true;
-            };
 #pragma unroll 1
             while (vit.valid() && !*abort_flag) {
-                if (!pf_done && kiss >= 2) prefetch_l2();
                 const bool isK = kit.valid() && kit.j <= vit.j + 1;
                 TileIter ti = isK ? kit : vit;
                 const int part = isK ? 0 : 1;
                 const int k = ti.pc.k;
                 const CUtensorMap* tm = &p.tm[2 * k + part];
-                const int nc = ((part ? p.dv[k] : p.dk[k]) + 127) >> 7;   // slots: 128-column chunks
+                const int ncols = ((part ? p.dv[k] : p.dk[k]) + 127) >> 7;
+                const int RBk = p.rb[k];
+                const int nc = ncols * RBk;   // slots: column chunks x row blocks
 #pragma unroll 1
                 for (int c = 0; c < nc; ++c) slot_free(ring_wrap(pos + c, p.nslot));
                 const int jr = ti.j % kR;
@@ -868,7 +594,6 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
                         if (q_pend) try_q(true);   // the previous piece's image goes first
                         query_image(p, ti.pc, q_src, q_bytes);
                         ptx::mbar_expect_tx_only(&bar.kready[jr], q_bytes);
-                        q_b = ti.pc.b;
                         q_pend = true;
                         q_tile = ti.j;
                         q_after = ti.j - 1;
@@ -878,13 +603,19 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
                     ptx::mbar_expect_tx(&bar.vready[jr], nc * kSlot);
                 }
                 uint64_t* rb = part ? &bar.vready[jr] : &bar.kready[jr];
-                const int row = ti.t * kTile;
 #pragma unroll 1
                 for (int c = 0; c < nc; ++c) {
                     const int s = ring_wrap(pos + c, p.nslot);
                     uint8_t* dst = ring + (size_t)s * kSlot;
-                    ptx::tma_load_3d_hint(dst, tm, c * 128, row, ti.pc.b, rb, pol);
-                    ptx::tma_load_3d_hint(dst + kBox, tm, c * 128 + 64, row, ti.pc.b, rb, pol);
+                    const int col = (c % ncols) * 128;
+                    const int row = (ti.t * RBk + c / ncols) * kTile;
+                    if (k == 0) {
+                        ptx::tma_load_3d_hint(dst, tm, col, row, ti.pc.b, rb, pol);
+                        ptx::tma_load_3d_hint(dst + kBox, tm, col + 64, row, ti.pc.b, rb, pol);
+                    } else {
+                        ptx::tma_load_4d_hint(dst, tm, col, ti.pc.g, row, ti.pc.b, rb, pol);
+                        ptx::tma_load_4d_hint(dst + kBox, tm, col + 64, ti.pc.g, row, ti.pc.b, rb, pol);
+                    }
                     owner[s] = (ti.j << 1) | part;
                 }
                 pos = ring_wrap(pos + nc, p.nslot);
@@ -914,24 +645,18 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
         // behind the tensor core's in-flight operand reads, so they are kept few. Both
         // walk the producer's sequence of tile parts to track ring positions.
         const bool s_issuer = warp == 1;
-        bool first_ok = true;
-        if (s_issuer && u0 < u1) {
-            // the CTA's first query image: published by the CTAs of its batch element in
-            // this launch (the whole warp polls their flags)
-            const int b = u0 / p.tiles_per_b;
-            ptx::mbar_wait(bar.tok, 0, abort_flag);
-            first_ok = poll_flags_warp(p.flags, p.cta_first[b], p.cta_last[b], *tok_s, abort_flag);
-        }
         if (lane == 0) {
             const uint32_t idS_lat = ptx::idesc_bf16(128, NP, false, false);
-            const uint32_t idS_raw = ptx::idesc_bf16(128, 2 * NP, false, false);
-            const uint32_t idV = ptx::idesc_bf16(128, NP, true, true);
+            const uint32_t idS_raw = ptx::idesc_bf16(128, 2 * kNG, false, false);
+            const uint32_t idV_lat = ptx::idesc_bf16(128, NP, true, true);
+            const uint32_t idV_raw = ptx::idesc_bf16(128, kNG, true, true);
             // base descriptors; a k-step or ring slot only adds (byte offset >> 4) to
             // the start-address field, which stays below 2^14 for shared memory
             const uint64_t dA_S = ptx::sdesc_sw128(ptx::smem_u32(ring), 16, 1024);      // K tile, K-major
             const uint64_t dA_V = ptx::sdesc_sw128(ptx::smem_u32(ring), kBox, 1024);    // V tile, MN-major
             const uint64_t dB_Q = ptx::sdesc_sw128(ptx::smem_u32(qbuf), 16, 1024);      // Q, K-major
-            const uint64_t dB_P = ptx::sdesc_sw32(ptx::smem_u32(pbuf), kPAtom, 256);    // P, MN-major
+            const uint64_t dB_P = ptx::sdesc_sw32(ptx::smem_u32(pbuf), kPAtom, 256);    // P (latent), MN-major
+            const uint64_t dB_Pr = ptx::sdesc_sw32(ptx::smem_u32(pbuf), kPAtom * kRBRaw, 256);  // P (raw)
             int pos = 0;   // ring position, same sequence as the producer
 
             auto issue_S = [&](const TileIter& ti) {
@@ -943,37 +668,52 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
                 }
                 ptx::mbar_wait(&bar.kready[jr], ph_of(ti.j), abort_flag);
                 const uint32_t dS = t_S + (ti.j & 1) * SW;
-                // latent tiles: N = heads (one bf16 part of the latent query); raw tiles:
-                // N = 2 x heads (hi and lo parts). Q is stored in 64-column chunks of N rows.
-                const bool lat = ti.pc.k == 0;
-                const uint32_t idS = lat ? idS_lat : idS_raw;
-                const uint32_t qstride = (lat ? NP : 2 * NP) * 128 >> 4;
-                const int ksteps = p.dk[ti.pc.k] >> 4;
-                const int nK = (p.dk[ti.pc.k] + 127) >> 7;
-                const int nfull = ksteps >> 3;   // whole 128-column chunks
+                if (ti.pc.k == 0) {
+                    // latent tile: 128 beacons, key width r_k in 128-column chunks
+                    const uint32_t qstride = NP * 128 >> 4;   // 64-column chunk of Q
+                    const int ksteps = p.dk[0] >> 4;
+                    const int nK = (p.dk[0] + 127) >> 7;
+                    const int nfull = ksteps >> 3;   // whole 128-column chunks
 #pragma unroll 1
-                for (int c = 0; c < nfull; ++c) {
-                    const int s = ring_wrap(pos + c, p.nslot);
-                    const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
-                    const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
-                    const uint32_t acc0 = c != 0 ? 1u : 0u;
+                    for (int c = 0; c < nfull; ++c) {
+                        const int s = ring_wrap(pos + c, p.nslot);
+                        const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
+                        const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
+                        const uint32_t acc0 = c != 0 ? 1u : 0u;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
-                                      b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS, kk == 0 ? acc0 : 1u);
-                }
-                if (nfull < nK) {
-                    // a last, partial chunk (key width not a multiple of 128)
-                    const int c = nfull;
-                    const int s = ring_wrap(pos + c, p.nslot);
-                    const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
-                    const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
+                        for (int kk = 0; kk < 8; ++kk)
+                            ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
+                                          b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS_lat,
+                                          kk == 0 ? acc0 : 1u);
+                    }
+                    if (nfull < nK) {
+                        // a last, partial chunk (key width not a multiple of 128)
+                        const int c = nfull;
+                        const int s = ring_wrap(pos + c, p.nslot);
+                        const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
+                        const uint64_t b0 = dB_Q + (uint64_t)(2 * c * qstride);
 #pragma unroll 1
-                    for (int kk = 0; kk < ksteps - 8 * c; ++kk)
-                        ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
-                                      b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS, (c | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < ksteps - 8 * c; ++kk)
+                            ptx::mma_bf16(dS, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
+                                          b0 + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS_lat,
+                                          (c | kk) != 0 ? 1u : 0u);
+                    }
+                    pos = ring_wrap(pos + nK, p.nslot);
+                } else {
+                    // raw tile: kRBRaw blocks of 128 tokens of one KV head, key width d = 128
+                    const uint32_t qstride = 2 * kNG * 128 >> 4;
+#pragma unroll
+                    for (int rb = 0; rb < kRBRaw; ++rb) {
+                        const int s = ring_wrap(pos + rb, p.nslot);
+                        const uint64_t a0 = dA_S + (uint64_t)((s * kSlot) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            ptx::mma_bf16(dS + rb * 2 * kNG, a0 + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2),
+                                          dB_Q + (uint64_t)((kk >> 2) * qstride + (kk & 3) * 2), idS_raw,
+                                          kk == 0 ? 0u : 1u);
+                    }
+                    pos = ring_wrap(pos + kRBRaw, p.nslot);
                 }
-                pos = ring_wrap(pos + nK, p.nslot);
                 ptx::mma_commit(&bar.kfree[jr]);
             };
             auto issue_V = [&](const TileIter& ti) {
@@ -991,21 +731,40 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
                 ptx::tc_fence_after();
                 const uint32_t abase = t_acc + (uint32_t)((p.accbuf == 2 ? (pc & 1) : 0) * p.accstride);
                 const uint32_t acc0 = ti.first() ? 0u : 1u;
-                const uint64_t pd = dB_P + (uint64_t)(((ti.j & 1) * SBuf<NP>::PB) >> 4);
-                const int nV = (p.dv[ti.pc.k] + 127) >> 7;
+                const uint32_t pboff = (uint32_t)(((ti.j & 1) * SBuf<NP>::PB) >> 4);
+                if (ti.pc.k == 0) {
+                    const uint64_t pd = dB_P + (uint64_t)pboff;
+                    const int nV = (p.dv[0] + 127) >> 7;
 #pragma unroll 1
-                for (int c = 0; c < nV; ++c) {
-                    const int s = ring_wrap(pos + c, p.nslot);
-                    const uint64_t vd = dA_V + (uint64_t)((s * kSlot) >> 4);
-                    const uint32_t d0 = abase + c * aw;
+                    for (int c = 0; c < nV; ++c) {
+                        const int s = ring_wrap(pos + c, p.nslot);
+                        const uint64_t vd = dA_V + (uint64_t)((s * kSlot) >> 4);
+                        const uint32_t d0 = abase + c * aw;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t a = vd + (uint64_t)(kk * (2048 >> 4));
-                        const uint64_t b = pd + (uint64_t)(kk * (512 >> 4));
-                        ptx::mma_bf16(d0, a, b, idV, kk == 0 ? acc0 : 1u);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t a = vd + (uint64_t)(kk * (2048 >> 4));
+                            const uint64_t b = pd + (uint64_t)(kk * (512 >> 4));
+                            ptx::mma_bf16(d0, a, b, idV_lat, kk == 0 ? acc0 : 1u);
+                        }
                     }
+                    pos = ring_wrap(pos + nV, p.nslot);
+                } else {
+                    // 256 tokens: k-steps 0-7 from block 0's slot, 8-15 from block 1's
+                    const uint64_t pd = dB_Pr + (uint64_t)pboff;
+#pragma unroll
+                    for (int rb = 0; rb < kRBRaw; ++rb) {
+                        const int s = ring_wrap(pos + rb, p.nslot);
+                        const uint64_t vd = dA_V + (uint64_t)((s * kSlot) >> 4);
+                        const uint32_t accr = rb == 0 ? acc0 : 1u;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t a = vd + (uint64_t)(kk * (2048 >> 4));
+                            const uint64_t b = pd + (uint64_t)((rb * 8 + kk) * (512 >> 4));
+                            ptx::mma_bf16(abase, a, b, idV_raw, kk == 0 ? accr : 1u);
+                        }
+                    }
+                    pos = ring_wrap(pos + kRBRaw, p.nslot);
                 }
-                pos = ring_wrap(pos + nV, p.nslot);
                 ptx::mma_commit(&bar.vfree[jr]);
             };
 
@@ -1013,19 +772,15 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
             kit.init(p, u0, u1);
             vit.init(p, u0, u1);
             if (s_issuer && kit.valid()) {
-                // the CTA's first query image (its own barrier: the key and value loads
-                // never wait for it)
+                // the CTA's first query image, once the preceding kernel has written it
+                // (its own barrier: the key and value loads never wait for it)
                 const uint8_t* q_src;
                 uint32_t q_bytes;
                 query_image(p, kit.pc, q_src, q_bytes);
-                if (first_ok) {
-                    fence_proxy_async_global();
-                    ptx::mbar_expect_tx(bar.qready, q_bytes);
-                    ptx::bulk_load(qbuf, q_src, q_bytes, bar.qready);
-                    ptx::mbar_wait(bar.qready, 0, abort_flag);
-                } else {
-                    ptx::mbar_arrive(bar.qready);   // nothing to copy: the kernel is winding down
-                }
+                pdl_wait();
+                ptx::mbar_expect_tx(bar.qready, q_bytes);
+                ptx::bulk_load(qbuf, q_src, q_bytes, bar.qready);
+                ptx::mbar_wait(bar.qready, 0, abort_flag);
             }
 #pragma unroll 1
             while (vit.valid()) {
@@ -1036,7 +791,7 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
                     else issue_V(ti);
                 } else {
                     const int k = ti.pc.k;
-                    pos = ring_wrap(pos + (((isK ? p.dk[k] : p.dv[k]) + 127) >> 7), p.nslot);
+                    pos = ring_wrap(pos + (((isK ? p.dk[k] : p.dv[k]) + 127) >> 7) * p.rb[k], p.nslot);
                 }
                 ti.next();
                 if (isK) kit = ti;
@@ -1062,50 +817,10 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
         c.lane_off = (uint32_t)(q4 * 32) << 16;
         c.t_S = t_S;
         c.aw = aw;
-        float l_part[NP];
+        const int G = p.G;
+        float l_part[NP], mref[NP];
 
-        // ---- query images: this CTA's units of the batch elements its run touches
-        const int b_lo = u0 / p.tiles_per_b, b_hi = (u1 - 1) / p.tiles_per_b;
-        // U_K blocks of this CTA's latent units (weights, read before the wait): the first
-        // is copied into the query buffer (free until the first image is copied, which
-        // waits for this CTA's flag), the others are pulled into L2
-        int staged = -1;
-        {
-            int g0, cb0;
-            if (first_latent_unit(p, cta, b_lo, b_hi, g0, cb0)) {
-                stage_ublock(p, g0, cb0, qbuf, c.tid);
-                staged = g0 * p.ncb + cb0;
-            }
-            const int per_g = p.ncb + p.img_raw;
-#pragma unroll 1
-            for (int b = b_lo; b <= b_hi && p.ncb > 0; ++b) {
-                const int n_b = p.cta_last[b] - p.cta_first[b] + 1;
-#pragma unroll 1
-                for (int u = cta - p.cta_first[b]; u < p.Hkv * per_g; u += n_b) {
-                    const int g = u / per_g, cb = u - g * per_g;
-                    if (cb < p.ncb && g * p.ncb + cb != staged) {
-                        const char* row = reinterpret_cast<const char*>(p.U_K + ((size_t)g * 128 + c.tid) * p.r_k + cb * 64);
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
-                    }
-                }
-            }
-        }
-        // the workspace partials and images may still be read by the preceding calls'
-        // kernels, and q / q_pos may be written by the preceding kernel
-        pdl_wait();
-        unsigned long long tok = 0;
-        if (c.tid == 0) {
-            tok = launch_token(p.ch);
-            *tok_s = tok;
-            ptx::mbar_arrive(bar.tok);
-        }
-        float* qr = reinterpret_cast<float*>(pbuf);   // scratch until the first P is written
-#pragma unroll 1
-        for (int b = b_lo; b <= b_hi; ++b) make_image_units(p, cta, b, qr, qbuf, staged, c.tid);
-        fence_proxy_async_global();
-        __threadfence();
-        ptx::named_bar(1, 128);
-        if (c.tid == 0) st_release(p.flags + cta, tok);
+        pdl_wait();   // the workspace partials may still be read by the preceding calls' kernels
 
         TileIter it;
         it.init(p, u0, u1);
@@ -1114,31 +829,32 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
             const int piece = it.piece;
             const int k = pc.k;
             const bool lat = (k == 0);
+            const int nvalid = lat ? p.Hq : G;
             c.nMB = (p.dv[k] + 127) >> 7;
             c.t_accp = t_acc + (uint32_t)((p.accbuf == 2 ? (piece & 1) : 0) * p.accstride);
             if (c.tid < NP) m_ref_s[c.tid] = -INFINITY;
 #pragma unroll
-            for (int h = 0; h < NP; ++h) l_part[h] = 0.f;
+            for (int h = 0; h < NP; ++h) {
+                l_part[h] = 0.f;
+                mref[h] = -INFINITY;
+            }
             ptx::named_bar(1, 128);
             int jl = it.j;
             #pragma unroll 1
             for (int n = 0; n < pc.n; ++n) {
-                const int row = it.t * kTile + c.myrow;   // row of this thread inside the segment
-                const bool row_ok = row < p.rows[k];
+                const int t = it.t;
+                const int row0 = t * kTile * p.rb[k] + c.myrow;
                 jl = it.j;
-                if (lat) {
-                    softmax_tile<NP, false>(c, it.j, row_ok, 0, NP, it.t > pc.t0, l_part);
-                } else {
-                    // raw row = token * Hkv + KV group: the row is scored by its group's heads
-                    const int hlo = (row % p.Hkv) * p.G;
-                    softmax_tile<NP, true>(c, it.j, row_ok, hlo, p.G, it.t > pc.t0, l_part);
-                }
+                if (lat) softmax_tile<NP, NP, 1, false>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref);
+                else softmax_tile<kNG, NP, kRBRaw, true>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref);
                 it.next();
             }
             // ---- partial of (CTA, piece): reference max, row sum and accumulator
             ptx::mbar_wait(&bar.vfree[jl % kR], ph_of(jl), abort_flag);   // V(jl) complete
             ptx::tc_fence_after();
-            write_partial<NP>(p, c, p.slot_base[cta] + piece, p.dv[k], l_part);
+            const int slot = p.slot_base[cta] + piece;
+            if (lat) write_partial<NP, NP>(p, c, slot, kSlotLatent, 0, nvalid, p.dv[k], l_part);
+            else write_partial<kNG, NP>(p, c, slot, kSlotRawGroup + pc.g, pc.g * G, nvalid, p.dv[k], l_part);
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bar.accfree[p.accbuf == 2 ? (piece & 1) : 0]);
             ptx::named_bar(1, 128);
@@ -1181,50 +897,48 @@ __global__ void __maxnreg__(200) tc_decode_kernel(const __grid_constant__ TcPara
 
 // Shared-memory plan of one launch.
 struct SmemPlan {
-    int NP, nslot, accbuf, accstride;
+    int NP, nslot, q_cols, accbuf, accstride;
     uint32_t off_q, off_p, off_bar, off_red, total, tmem_cols;
     bool ok;
 };
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// Plan within `budget` bytes of dynamic shared memory.
-SmemPlan plan_smem_within(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], const int rows[kNumKinds],
-                          int budget) {
+// TMEM columns of one score buffer (host copy of SBuf<NP>::W).
+int sbuf_w(int NP) { return std::max(NP, 2 * kNG * kRBRaw); }
+
+SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], const int rows[kNumKinds]) {
     SmemPlan s{};
     s.NP = round_up(Hq, 16);
-    int nmb = 0, maxK = 0, maxV = 0;
-    bool raw = false;
+    int qc = 0, nmb = 0, maxK = 0, maxV = 0;
     for (int k = 0; k < kNumKinds; ++k) {
         if (rows[k] <= 0) continue;
-        raw = raw || k > 0;
+        const int rbk = k == 0 ? 1 : kRBRaw;
+        qc = std::max(qc, dk[k]);
         nmb = std::max(nmb, (dv[k] + 127) / 128);
-        maxK = std::max(maxK, (dk[k] + 127) / 128);   // ring slots of a tile's keys
-        maxV = std::max(maxV, (dv[k] + 127) / 128);
+        maxK = std::max(maxK, (dk[k] + 127) / 128 * rbk);   // ring slots of a tile's keys
+        maxV = std::max(maxV, (dv[k] + 127) / 128 * rbk);
     }
+    s.q_cols = round_up(qc, 64);
     s.ok = false;
     if (s.NP > 64) return s;
-    // TMEM: two score buffers of 2 NP columns, then one or two accumulator buffers
-    // (two when they fit, so a piece's write-out overlaps the next piece)
-    const int sw = 2 * s.NP;
+    // TMEM: two score buffers of sbuf_w(NP) columns, then one or two accumulator
+    // buffers (two when they fit, so a piece's write-out overlaps the next piece)
     s.accstride = nmb * s.NP;
     int tmem = 0;
     for (s.accbuf = 2; s.accbuf >= 1; --s.accbuf) {
-        tmem = 2 * sw + s.accbuf * s.accstride;
+        tmem = 2 * sbuf_w(s.NP) + s.accbuf * s.accstride;
         if (tmem <= 512) break;
     }
     if (tmem > 512) return s;
     s.tmem_cols = 32;
     while ((int)s.tmem_cols < tmem) s.tmem_cols *= 2;
-    // query buffer: the latent image (NP rows, bf16) or the raw image (hi and lo parts);
-    // before the first image it stages a 128 x 64 block of U_K (16 KB) for the latent image
-    const int q_bytes = std::max({rows[0] > 0 ? s.NP * round_up(dk[0], 64) * 2 : 0, rows[0] > 0 ? 128 * 128 : 0,
-                                  raw ? 2 * s.NP * 128 * 2 : 0});
-    const int p_bytes = 2 * s.NP * 256;   // two P buffers (bf16)
-    const int nbars = 4 * kR + 6;
-    // red, m_ref, alpha (6 NP floats), then flags, TMEM base, slot owners and the token
-    const int misc_bytes = (6 * s.NP + 40) * 4;
-    const int avail = budget - q_bytes - p_bytes - round_up(nbars * 8, 16) - misc_bytes - 1024;
+    // query buffer: the latent image (NP rows, bf16) or a raw image (hi and lo parts of kNG heads)
+    const int q_bytes = std::max(rows[0] > 0 ? s.NP * round_up(dk[0], 64) * 2 : 0, 2 * kNG * 128 * 2);
+    const int p_bytes = 2 * std::max(s.NP, kNG * kRBRaw) * 256;   // two P buffers (bf16)
+    const int nbars = 4 * kR + 5;
+    const int misc_bytes = (6 * s.NP + 32) * 4;
+    const int avail = kSmemMax - q_bytes - p_bytes - round_up(nbars * 8, 16) - misc_bytes - 1024;
     s.nslot = std::min(kMaxSlots, avail / kSlot);
     // One tile part (keys or values) must fit the ring. The loads run in consumption
     // order and each waits only for earlier parts to be consumed, so a ring smaller
@@ -1236,19 +950,8 @@ SmemPlan plan_smem_within(int Hq, const int dk[kNumKinds], const int dv[kNumKind
     s.off_bar = s.off_p + p_bytes;
     s.off_red = s.off_bar + round_up(nbars * 8, 16);
     s.total = s.off_red + misc_bytes + 1024;
-    s.ok = s.total <= (uint32_t)budget;
+    s.ok = s.total <= (uint32_t)kSmemMax;
     return s;
-}
-
-// The shared budget when the ring still holds a key and a value tile part, else the
-// whole of what a CTA may use.
-SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], const int rows[kNumKinds]) {
-    int maxKV = 0;
-    for (int k = 0; k < kNumKinds; ++k)
-        if (rows[k] > 0) maxKV = std::max(maxKV, (dk[k] + 127) / 128 + (dv[k] + 127) / 128);
-    const SmemPlan s = plan_smem_within(Hq, dk, dv, rows, kSmemShared);
-    if (s.ok && s.nslot > maxKV) return s;
-    return plan_smem_within(Hq, dk, dv, rows, kSmemMax);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1269,9 +972,9 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// A segment operand: 3-D bf16 tensor [B][rows][cols] (cols contiguous) read in boxes of
-// 128 rows x 64 columns with the 128-byte swizzle; rows / columns past the end read as zero.
-bool make_map(CUtensorMap* tm, const void* base, int cols, int64_t rows, int B) {
+// Latent operand: 3-D bf16 tensor [B][rows][cols] (cols contiguous) read in boxes of
+// 128 rows x 64 columns with the 128-byte swizzle; rows/columns past the end read as zero.
+bool make_map_latent(CUtensorMap* tm, const void* base, int cols, int rows, int B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)B};
@@ -1283,37 +986,56 @@ bool make_map(CUtensorMap* tm, const void* base, int cols, int64_t rows, int B) 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Raw operand: 4-D bf16 tensor [B][T][Hkv][d] read per KV head in boxes of 128
+// tokens x 64 columns (one head), 128-byte swizzle; tokens past the end read as zero.
+bool make_map_raw(CUtensorMap* tm, const void* base, int d, int Hkv, int T, int B) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * d * 2, (cuuint64_t)T * Hkv * d * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Encoded tensor maps are reused by later calls on the same buffers and sizes
 // (encoding is a driver call; a decode step makes four per layer). Direct-mapped.
-bool cached_map(CUtensorMap* tm, const void* base, int cols, int64_t rows, int B) {
+bool cached_map(CUtensorMap* tm, bool latent, const void* base, int a, int b, int c, int d) {
     struct Entry {
         bool valid = false;
+        bool latent = false;
         const void* base = nullptr;
-        int cols = 0, B = 0;
-        int64_t rows = 0;
+        int dims[4] = {0, 0, 0, 0};
         CUtensorMap tm;
     };
     static std::mutex mu;
     static Entry cache[512];
     const uint64_t h = ((uint64_t)(uintptr_t)base >> 8) * 0x9E3779B97F4A7C15ull ^
-                       ((uint64_t)cols * 31 + (uint64_t)rows) * 0xBF58476D1CE4E5B9ull ^ (uint64_t)B;
+                       ((uint64_t)a * 31 + b) * 0xBF58476D1CE4E5B9ull ^ ((uint64_t)c * 131 + d + latent);
     Entry& e = cache[(h >> 40) % 512];
     {
         std::lock_guard<std::mutex> g(mu);
-        if (e.valid && e.base == base && e.cols == cols && e.rows == rows && e.B == B) {
+        if (e.valid && e.latent == latent && e.base == base && e.dims[0] == a && e.dims[1] == b &&
+            e.dims[2] == c && e.dims[3] == d) {
             *tm = e.tm;
             return true;
         }
     }
-    if (!make_map(tm, base, cols, rows, B)) return false;
-    std::lock_guard<std::mutex> g(mu);
-    e.valid = true;
-    e.base = base;
-    e.cols = cols;
-    e.rows = rows;
-    e.B = B;
-    e.tm = *tm;
-    return true;
+    const bool ok = latent ? make_map_latent(tm, base, a, b, c) : make_map_raw(tm, base, a, b, c, d);
+    if (ok) {
+        std::lock_guard<std::mutex> g(mu);
+        e.valid = true;
+        e.latent = latent;
+        e.base = base;
+        e.dims[0] = a;
+        e.dims[1] = b;
+        e.dims[2] = c;
+        e.dims[3] = d;
+        e.tm = *tm;
+    }
+    return ok;
 }
 
 int sm_count() {
@@ -1331,59 +1053,21 @@ using plan::WorkPlan;
 using plan::SegList;
 using plan::make_plan;
 
-// Launch-token channel of a workspace on the current device: each workspace in use
-// keeps its own channel, so that launches on different workspaces (which may run
-// concurrently on different streams) never share an epoch. When more than kChannels
-// workspaces are in use, the least recently used one gives up its channel.
-int channel_for(const void* ws) {
-    struct Dev {
-        std::map<const void*, int> of;
-        const void* owner[kChannels] = {};
-        uint64_t last[kChannels] = {};
-        uint64_t tick = 0;
-    };
-    static std::mutex mu;
-    static Dev devs[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    Dev& d = devs[dev & 63];
-    std::lock_guard<std::mutex> g(mu);
-    ++d.tick;
-    auto it = d.of.find(ws);
-    if (it != d.of.end()) {
-        d.last[it->second] = d.tick;
-        return it->second;
-    }
-    int ch = 0;
-    for (int i = 1; i < kChannels; ++i)
-        if (d.last[i] < d.last[ch]) ch = i;
-    if (d.owner[ch] != nullptr) d.of.erase(d.owner[ch]);
-    d.owner[ch] = ws;
-    d.last[ch] = d.tick;
-    d.of[ws] = ch;
-    return ch;
-}
-
 struct PlanKey {
     int B, max_ctas;
     std::vector<std::pair<int, int>> segs;
     bool operator<(const PlanKey& o) const { return std::tie(B, max_ctas, segs) < std::tie(o.B, o.max_ctas, o.segs); }
 };
 
-// Plans are built once per (batch, segment list, grid limit) and shared: the cache
-// hands out shared ownership, so a plan stays valid for a caller even when another
-// thread clears the cache.
-std::shared_ptr<const WorkPlan> cached_plan(int B, const SegList& sl, int max_ctas) {
+const WorkPlan& cached_plan(int B, const SegList& sl, int max_ctas) {
     static std::mutex mu;
-    static std::map<PlanKey, std::shared_ptr<const WorkPlan>> cache;
+    static std::map<PlanKey, WorkPlan> cache;
     PlanKey key{B, max_ctas, sl.segs};
     std::lock_guard<std::mutex> g(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     if (cache.size() > 256) cache.clear();
-    auto w = std::make_shared<const WorkPlan>(make_plan(B, sl, max_ctas));
-    cache.emplace(std::move(key), w);
-    return w;
+    return cache.emplace(key, make_plan(B, sl, max_ctas)).first->second;
 }
 
 template <int NP>
@@ -1406,7 +1090,8 @@ cudaError_t launch_decode(const TcParams& prm, int grid, uint32_t smem, cudaStre
 
 // Kinds of key rows of one call: rows / widths per segment and operands.
 struct Kinds {
-    int64_t rows[kNumKinds] = {0, 0, 0};
+    int rows[kNumKinds] = {0, 0, 0};
+    int ngroups[kNumKinds] = {0, 0, 0};
     int dk[kNumKinds] = {0, 0, 0};
     int dv[kNumKinds] = {0, 0, 0};
     const void* K[kNumKinds] = {nullptr, nullptr, nullptr};
@@ -1415,10 +1100,10 @@ struct Kinds {
 
 Kinds kinds_of(const TcCall& c) {
     Kinds s;
-    // a raw source [B, T, Hkv, d] is read as [B, T * Hkv, d]
     auto raw = [&](int k, int T, const void* K, const void* V) {
         if (T <= 0) return;
-        s.rows[k] = (int64_t)T * c.Hkv;
+        s.rows[k] = T;
+        s.ngroups[k] = c.Hkv;
         s.dk[k] = s.dv[k] = c.d;
         s.K[k] = K;
         s.V[k] = V;
@@ -1426,6 +1111,7 @@ Kinds kinds_of(const TcCall& c) {
     if (c.which == SLIMKV_LATENT) {
         if (c.N_b > 0) {
             s.rows[0] = c.N_b;
+            s.ngroups[0] = 1;
             s.dk[0] = c.r_k;
             s.dv[0] = c.r_v;
             s.K[0] = c.C_K;
@@ -1444,7 +1130,7 @@ Kinds kinds_of(const TcCall& c) {
 }  // namespace
 
 bool tc_supported(int Hq, int Hkv, int d, int N_b, int r_k, int r_v) {
-    if (d != 128 || Hq > 64 || Hkv > Hq) return false;
+    if (d != 128 || Hq > 64 || Hkv > 128 || Hq / Hkv > kNG) return false;
     int rows[kNumKinds] = {N_b, 1, 1}, dk[kNumKinds] = {r_k, d, d}, dv[kNumKinds] = {r_v, d, d};
     if (N_b <= 0) rows[0] = 0;
     return plan_smem(Hq, dk, dv, rows).ok;
@@ -1453,8 +1139,11 @@ bool tc_supported(int Hq, int Hkv, int d, int N_b, int r_k, int r_v) {
 cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     typedef __nv_bfloat16 bf16;
     const bool lat = c.which == SLIMKV_LATENT && c.N_b > 0;
-    const bool has_raw = c.which != SLIMKV_LATENT || c.W > 0;
-    cudaError_t e = cudaSuccess;
+    const int NPq = (c.Hq + 15) / 16 * 16;
+    cudaError_t e = launch_qproj<bf16>((const bf16*)c.q, lat ? (const bf16*)c.U_K : nullptr, c.q_pos, nullptr,
+                                       nullptr, c.B, c.Hq, c.Hkv, c.d, c.r_k, c.rope_base, c.scale_log2, st, true,
+                                       lat ? c.lat_img : nullptr, c.raw_img, NPq);
+    if (e != cudaSuccess) return e;
     if (c.which == SLIMKV_RECONSTRUCT) {
         // plain launches (no early trigger): the decode below reads K_b / V_b
         // before its own dependency wait, so they must be complete when it starts
@@ -1465,34 +1154,36 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     const Kinds s = kinds_of(c);
-    int rows_i[kNumKinds];
-    for (int k = 0; k < kNumKinds; ++k) rows_i[k] = s.rows[k] > 0 ? 1 : 0;
-    const SmemPlan sp = plan_smem(c.Hq, s.dk, s.dv, rows_i);
+    const SmemPlan sp = plan_smem(c.Hq, s.dk, s.dv, s.rows);
     if (!sp.ok) return cudaErrorInvalidValue;
 
     TcParams prm;   // copied into the launch's parameter space
     memset(&prm, 0, sizeof(prm));
     SegList sl;
-    int lat_segs = 0;   // segments of a batch element before the first raw one
     prm.tiles_per_b = 0;
     for (int k = 0; k < kNumKinds; ++k) {
-        prm.rows[k] = (int)s.rows[k];
+        prm.rows[k] = s.rows[k];
+        prm.ngroups[k] = s.ngroups[k];
         prm.dk[k] = s.dk[k];
         prm.dv[k] = s.dv[k];
-        const int tiles = s.rows[k] > 0 ? (int)((s.rows[k] + kTile - 1) / kTile) : 0;
+        prm.rb[k] = k == 0 ? 1 : kRBRaw;
+        const int tile_rows = kTile * prm.rb[k];
+        const int tiles = s.rows[k] > 0 ? (s.rows[k] + tile_rows - 1) / tile_rows : 0;
         prm.tiles[k] = tiles;
-        prm.tiles_per_b += tiles;
-        if (tiles == 0) continue;
+        prm.tiles_per_b += tiles * s.ngroups[k];
         // cost of a tile: the 32 KB slots it streams (+1 for its fixed per-tile work)
-        const int cost = (s.dk[k] + 127) / 128 + (s.dv[k] + 127) / 128 + 1;
-        sl.segs.push_back({tiles, cost});
-        if (k == 0) lat_segs = 1;
-        if (!cached_map(&prm.tm[2 * k], s.K[k], s.dk[k], s.rows[k], c.B) ||
-            !cached_map(&prm.tm[2 * k + 1], s.V[k], s.dv[k], s.rows[k], c.B))
-            return cudaErrorInvalidValue;
+        const int cost = ((s.dk[k] + 127) / 128 + (s.dv[k] + 127) / 128) * prm.rb[k] + 1;
+        for (int g = 0; g < s.ngroups[k]; ++g) sl.segs.push_back({tiles, cost});
+        if (s.rows[k] > 0) {
+            const bool ok = k == 0
+                                ? cached_map(&prm.tm[0], true, s.K[0], s.dk[0], s.rows[0], c.B, 0) &&
+                                      cached_map(&prm.tm[1], true, s.V[0], s.dv[0], s.rows[0], c.B, 0)
+                                : cached_map(&prm.tm[2 * k], false, s.K[k], c.d, c.Hkv, s.rows[k], c.B) &&
+                                      cached_map(&prm.tm[2 * k + 1], false, s.V[k], c.d, c.Hkv, s.rows[k], c.B);
+            if (!ok) return cudaErrorInvalidValue;
+        }
     }
-    const std::shared_ptr<const WorkPlan> wp = cached_plan(c.B, sl, std::min(kMaxCtas, sm_count()));
-    const WorkPlan& w = *wp;
+    const WorkPlan& w = cached_plan(c.B, sl, std::min(kMaxCtas, sm_count()));
     if (w.slots > c.slots) return cudaErrorInvalidValue;
     prm.B = c.B;
     prm.Hq = c.Hq;
@@ -1501,9 +1192,10 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     prm.lat_img = c.lat_img;
     prm.raw_img = c.raw_img;
     prm.lat_img_bytes = (uint32_t)lat_img_bytes(sp.NP, c.r_k);
-    prm.raw_img_bytes = (uint32_t)raw_img_bytes(sp.NP, c.d);
+    prm.raw_img_bytes = (uint32_t)raw_img_bytes(c.d);
     prm.acc = c.acc;
     prm.ml = c.ml;
+    prm.kind = c.kind;
     prm.Dmax = c.Dmax;
     prm.nslot = sp.nslot;
     prm.accbuf = sp.accbuf;
@@ -1515,32 +1207,6 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     prm.tmem_cols = sp.tmem_cols;
     for (int i = 0; i <= w.n_ctas; ++i) prm.u_begin[i] = w.u_begin[i];
     for (int i = 0; i < w.n_ctas; ++i) prm.slot_base[i] = w.slot_base[i];
-    // query images: the CTAs whose runs touch batch element b make b's images
-    prm.q = (const bf16*)c.q;
-    prm.U_K = lat ? (const bf16*)c.U_K : nullptr;
-    prm.q_pos = c.q_pos;
-    prm.flags = c.flags;
-    prm.ch = channel_for(c.flags);
-    prm.r_k = c.r_k;
-    prm.ncb = lat ? (c.r_k + 63) / 64 : 0;
-    {
-        // about kPrefetchBytes per CTA, in tiles of the largest kind
-        int tile_bytes = 0;
-        for (int k = 0; k < kNumKinds; ++k)
-            if (s.rows[k] > 0) tile_bytes = std::max(tile_bytes, kTile * (s.dk[k] + s.dv[k]) * 2);
-        prm.pf_tiles = tile_bytes > 0 ? kPrefetchBytes / tile_bytes : 0;
-    }
-    prm.img_raw = has_raw ? 1 : 0;
-    prm.scale_log2 = c.scale_log2;
-    rope_turns(c.rope_base, c.d, prm.turn);
-    for (int b = 0; b < c.B; ++b) prm.cta_first[b] = -1;
-    for (int i = 0; i < w.n_ctas; ++i) {
-        const int b0 = w.u_begin[i] / prm.tiles_per_b, b1 = (w.u_begin[i + 1] - 1) / prm.tiles_per_b;
-        for (int b = b0; b <= b1; ++b) {
-            if (prm.cta_first[b] < 0) prm.cta_first[b] = (short)i;
-            prm.cta_last[b] = (short)i;
-        }
-    }
 
     timer_before(st);
     switch (sp.NP) {
@@ -1563,9 +1229,9 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     cb.U_V = lat ? c.U_V : nullptr;
     cb.acc = c.acc;
     cb.ml = c.ml;
+    cb.kind = c.kind;
     cb.out = c.out;
     for (int b = 0; b <= c.B; ++b) cb.slot_begin[b] = w.batch_slot[b];
-    for (int b = 0; b < c.B; ++b) cb.slot_mid[b] = plan::first_slot_from_seg(w, b, lat_segs);
     return launch_combine<bf16>(cb, st, true);
 }
 

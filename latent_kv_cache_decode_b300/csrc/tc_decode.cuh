@@ -23,11 +23,11 @@ struct TcCall {
     float* out;
     float* q_rot;
     float* q_lat;
-    uint8_t* lat_img;          // query images (made by the decode kernel)
+    uint8_t* lat_img;          // query images written by the query kernel
     uint8_t* raw_img;
-    unsigned long long* flags; // [kMaxCtas] per-CTA flags of the decode kernel
     float* acc;
     float* ml;
+    int* kind;
     void* kb;
     void* vb;
     int slots;

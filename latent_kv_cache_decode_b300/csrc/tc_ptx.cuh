@@ -118,13 +118,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* tm, in
         "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
         : "memory");
 }
-// Pull one box of a 3-D tensor into L2 (no shared-memory destination, no completion
-// to wait for): later loads of the box hit L2.
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* tm, int c0, int c1, int c2) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tm), "r"(c0), "r"(c1),
-                 "r"(c2)
-                 : "memory");
-}
 // L2 policy for data read once: evict first, so a stream much larger than L2 does
 // not push out the small, reused data (projections, partials, kernel code).
 __device__ __forceinline__ uint64_t policy_evict_first() {

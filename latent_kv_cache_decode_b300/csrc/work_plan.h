@@ -14,11 +14,10 @@ namespace slimkv {
 namespace plan {
 
 // Work plan: contiguous unit ranges per CTA with balanced cost, one partial slot
-// per (CTA, segment piece), the slot range of every batch element, and the segment
-// (index into SegList::segs) that each slot's piece belongs to.
+// per (CTA, segment piece), and the slot range of every batch element.
 struct WorkPlan {
     int n_ctas = 0;
-    std::vector<int> u_begin, slot_base, batch_slot, slot_seg;
+    std::vector<int> u_begin, slot_base, batch_slot;
     int slots = 0;
 };
 
@@ -27,12 +26,13 @@ struct SegList {
     std::vector<std::pair<int, int>> segs;
 };
 
-// Fixed cost of a piece in tile-cost units: its first tile waits for a query image
-// and takes the rescale path, and its end waits for the last value MMAs and writes a
-// partial. The planner splits a segment across CTAs only when that pays for itself.
+// Fixed cost of a piece in tile-cost units (about 1.6 tiles): its first tile waits for
+// a query image and takes the rescale path, and its end waits for the last value MMAs
+// and writes a partial. The planner avoids splitting a segment across CTAs unless
+// that pays for itself.
 constexpr int kPieceCost = 8;
 
-inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas, int piece_cost = kPieceCost) {
+inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas) {
     // runs of equal-cost units in unit order (batch-major, then segment)
     int64_t total = 0, units = 0;
     int cmax = 1;
@@ -45,33 +45,32 @@ inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas, int piece_cost
     const int G = (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, units));
     // Greedy packing with per-CTA budget T: a CTA takes units in order until the next
     // one would exceed T; every piece (a CTA's run inside one segment) costs
-    // piece_cost on top of its units. `visit(u, new_cta, b, seg)` sees every unit
-    // boundary where a CTA or a piece starts; returns the number of CTAs.
+    // kPieceCost on top of its units. `visit(u, new_cta, new_piece, b)` sees every
+    // unit boundary where a CTA or a piece starts; returns the number of CTAs.
     auto pack = [&](int64_t T, auto&& visit) {
         int ctas = 1;
         int64_t cur = 0, u = 0;
         for (int b = 0; b < B; ++b)
-            for (int si = 0; si < (int)sl.segs.size(); ++si) {
-                const auto& r = sl.segs[si];
+            for (auto& r : sl.segs) {
                 int n = r.first;
                 bool open = false;   // a piece of this segment is open in the current CTA
                 while (n > 0) {
                     if (!open) {
-                        if (cur > 0 && cur + piece_cost + r.second > T) {
+                        if (cur > 0 && cur + kPieceCost + r.second > T) {
                             ++ctas;
                             cur = 0;
-                            visit(u, true, b, si);
+                            visit(u, true, b);
                         } else {
-                            visit(u, false, b, si);
+                            visit(u, false, b);
                         }
-                        cur += piece_cost;
+                        cur += kPieceCost;
                         open = true;
                     }
                     int64_t room = (T - cur) / r.second;
                     if (room == 0) {
                         ++ctas;
-                        cur = piece_cost;
-                        visit(u, true, b, si);
+                        cur = kPieceCost;
+                        visit(u, true, b);
                         room = (T - cur) / r.second;
                     }
                     const int take = (int)std::min<int64_t>(n, room);
@@ -82,9 +81,9 @@ inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas, int piece_cost
             }
         return ctas;
     };
-    auto no_visit = [](int64_t, bool, int, int) {};
-    int64_t lo = std::max<int64_t>(cmax + piece_cost, (total + G - 1) / G),
-            hi = std::max<int64_t>(lo, total + (int64_t)piece_cost * B * (int64_t)sl.segs.size());
+    auto no_visit = [](int64_t, bool, int) {};
+    int64_t lo = std::max<int64_t>(cmax + kPieceCost, (total + G - 1) / G),
+            hi = std::max<int64_t>(lo, total + (int64_t)kPieceCost * B * (int64_t)sl.segs.size());
     while (lo < hi) {
         const int64_t mid = (lo + hi) / 2;
         if (pack(mid, no_visit) <= G) hi = mid;
@@ -96,12 +95,11 @@ inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas, int piece_cost
     std::vector<int> piece_b;
     w.u_begin.push_back(0);
     bool first = true;
-    pack(T, [&](int64_t u, bool new_cta, int b, int si) {
+    pack(T, [&](int64_t u, bool new_cta, int b) {
         if (new_cta && !first) w.u_begin.push_back((int)u);
         first = false;
         piece_cta.push_back((int)w.u_begin.size() - 1);
         piece_b.push_back(b);
-        w.slot_seg.push_back(si);
     });
     w.u_begin.push_back((int)units);
     w.n_ctas = (int)w.u_begin.size() - 1;
@@ -116,15 +114,6 @@ inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas, int piece_cost
     w.batch_slot[B] = (int)piece_cta.size();
     w.slots = (int)piece_cta.size();
     return w;
-}
-
-// First slot of batch element b whose piece lies in a segment with index >= seg
-// (batch_slot[b + 1] if none): with the segments of a batch element in kind order,
-// the slots of b below it hold the partials of the segments before `seg`.
-inline int first_slot_from_seg(const WorkPlan& w, int b, int seg) {
-    int s = w.batch_slot[b];
-    while (s < w.batch_slot[b + 1] && w.slot_seg[s] < seg) ++s;
-    return s;
 }
 
 }  // namespace plan

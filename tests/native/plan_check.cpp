@@ -47,15 +47,15 @@ static int check(int B, const SegList& sl, int G, int* n_ctas, int* max_pieces, 
 }
 
 int main() {
-    // the 128K / 16x layer: per batch element 64 latent tiles (128 beacons, four 32 KB
-    // slots + 1) and 128 raw tiles (128 rows of token x KV head, two slots + 1)
+    // the 128K / 16x layer: per batch element 64 latent tiles and 8 raw segments of 8 tiles,
+    // each tile costing 5 (four 32 KB slots + 1)
     SegList h;
     h.segs.push_back({64, 5});
-    h.segs.push_back({128, 3});
+    for (int g = 0; g < 8; ++g) h.segs.push_back({8, 5});
     int n = 0, mp = 0, mn = 0, mx = 0;
     if (check(8, h, 148, &n, &mp, &mn, &mx)) return 10;
     std::printf("headline: %d CTAs, max %d pieces, %d..%d tiles\n", n, mp, mn, mx);
-    if (n != 144 || mp != 1) return 11;
+    if (n != 128 || mp != 1 || mn != 8 || mx != 8) return 11;
     srand(1);
     for (int t = 0; t < 20000; ++t) {
         SegList s;

@@ -19,4 +19,4 @@ def test_work_planner_invariants(tmp_path):
                     "-o", str(exe)], check=True, capture_output=True, text=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
-    assert "headline: 144 CTAs, max 1 pieces" in r.stdout
+    assert "headline: 128 CTAs, max 1 pieces, 8..8 tiles" in r.stdout
