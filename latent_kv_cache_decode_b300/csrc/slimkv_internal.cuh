@@ -89,6 +89,7 @@ struct CombineArgs {
     const int* kind;
     float* out;
     int slot_begin[kMaxB + 1];   // partial slots of batch element b: [slot_begin[b], slot_begin[b+1])
+    int slot_mid[kMaxB];         // tensor-core path: b's latent slots [slot_begin, slot_mid), raw after
 };
 
 // Arguments of the query kernel (RoPE + latent projection). The RoPE angle of pair
@@ -171,6 +172,9 @@ template <typename T>
 cudaError_t launch_simt_decode(const SimtDecodeArgs& a, cudaStream_t st);
 template <typename T>
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl);
+// The tensor-core path's combine (bf16 U_V, d = 128; tc_combine.cu), launched with
+// programmatic dependent launch.
+cudaError_t launch_tc_combine(const CombineArgs& a, cudaStream_t st);
 template <typename T>
 cudaError_t launch_simt_reconstruct(const T* C, const T* U, T* out, int rows, int n, int r,
                                     cudaStream_t st);

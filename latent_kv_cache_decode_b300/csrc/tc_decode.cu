@@ -45,6 +45,7 @@
 
 #include <algorithm>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <tuple>
 #include <vector>
@@ -63,7 +64,7 @@ constexpr int kTile = 128;            // rows per tile (MMA M)
 constexpr int kBox = 16384;           // one TMA box: 128 rows x 64 bf16 columns, 128B-swizzled
 constexpr int kSlot = 2 * kBox;       // ring slot: 128 rows x 128 columns
 constexpr int kThreads = 224;
-constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory we may use per CTA
+constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory one CTA may use
 constexpr int kNumKinds = 3;          // latent, raw source 0, raw source 1
 constexpr int kNG = 16;               // heads of a raw tile's query operand (the group's heads, padded)
 // m_ref moves only when a score exceeds it by more than this (log2 units). P values up
@@ -908,6 +909,7 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 int sbuf_w(int NP) { return std::max(NP, 2 * kNG * kRBRaw); }
 
 SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], const int rows[kNumKinds]) {
+    const int budget = kSmemMax;
     SmemPlan s{};
     s.NP = round_up(Hq, 16);
     int qc = 0, nmb = 0, maxK = 0, maxV = 0;
@@ -938,7 +940,7 @@ SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], con
     const int p_bytes = 2 * std::max(s.NP, kNG * kRBRaw) * 256;   // two P buffers (bf16)
     const int nbars = 4 * kR + 5;
     const int misc_bytes = (6 * s.NP + 32) * 4;
-    const int avail = kSmemMax - q_bytes - p_bytes - round_up(nbars * 8, 16) - misc_bytes - 1024;
+    const int avail = budget - q_bytes - p_bytes - round_up(nbars * 8, 16) - misc_bytes - 1024;
     s.nslot = std::min(kMaxSlots, avail / kSlot);
     // One tile part (keys or values) must fit the ring. The loads run in consumption
     // order and each waits only for earlier parts to be consumed, so a ring smaller
@@ -950,9 +952,10 @@ SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], con
     s.off_bar = s.off_p + p_bytes;
     s.off_red = s.off_bar + round_up(nbars * 8, 16);
     s.total = s.off_red + misc_bytes + 1024;
-    s.ok = s.total <= (uint32_t)kSmemMax;
+    s.ok = s.total <= (uint32_t)budget;
     return s;
 }
+
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1054,20 +1057,38 @@ using plan::SegList;
 using plan::make_plan;
 
 struct PlanKey {
-    int B, max_ctas;
+    int B, max_ctas, lat_segs;
     std::vector<std::pair<int, int>> segs;
-    bool operator<(const PlanKey& o) const { return std::tie(B, max_ctas, segs) < std::tie(o.B, o.max_ctas, o.segs); }
+    bool operator<(const PlanKey& o) const {
+        return std::tie(B, max_ctas, lat_segs, segs) < std::tie(o.B, o.max_ctas, o.lat_segs, o.segs);
+    }
 };
 
-const WorkPlan& cached_plan(int B, const SegList& sl, int max_ctas) {
+// A work plan and, per batch element, its first raw partial slot (the latent slots of b
+// come first: units are ordered by segment, latent before raw).
+struct CtaPlan {
+    WorkPlan w;
+    std::vector<int> batch_mid;
+};
+
+// Plans are built once per (batch, segment list, grid limit) and shared: the cache hands
+// out shared ownership, so a plan stays valid for a caller while another thread clears
+// the cache. lat_segs: segments of a batch element before the first raw one.
+std::shared_ptr<const CtaPlan> cached_plan(int B, const SegList& sl, int lat_segs, int max_ctas) {
     static std::mutex mu;
-    static std::map<PlanKey, WorkPlan> cache;
-    PlanKey key{B, max_ctas, sl.segs};
+    static std::map<PlanKey, std::shared_ptr<const CtaPlan>> cache;
+    PlanKey key{B, max_ctas, lat_segs, sl.segs};
     std::lock_guard<std::mutex> g(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     if (cache.size() > 256) cache.clear();
-    return cache.emplace(key, make_plan(B, sl, max_ctas)).first->second;
+    auto cp = std::make_shared<CtaPlan>();
+    cp->w = make_plan(B, sl, max_ctas);
+    cp->batch_mid.resize(B);
+    for (int b = 0; b < B; ++b) cp->batch_mid[b] = plan::first_slot_from_seg(cp->w, b, lat_segs);
+    std::shared_ptr<const CtaPlan> r = cp;
+    cache.emplace(std::move(key), r);
+    return r;
 }
 
 template <int NP>
@@ -1183,7 +1204,9 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
             if (!ok) return cudaErrorInvalidValue;
         }
     }
-    const WorkPlan& w = cached_plan(c.B, sl, std::min(kMaxCtas, sm_count()));
+    const int lat_segs = s.rows[0] > 0 ? s.ngroups[0] : 0;   // latent segments come first
+    const std::shared_ptr<const CtaPlan> plan = cached_plan(c.B, sl, lat_segs, std::min(kMaxCtas, sm_count()));
+    const WorkPlan& w = plan->w;
     if (w.slots > c.slots) return cudaErrorInvalidValue;
     prm.B = c.B;
     prm.Hq = c.Hq;
@@ -1232,7 +1255,8 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     cb.kind = c.kind;
     cb.out = c.out;
     for (int b = 0; b <= c.B; ++b) cb.slot_begin[b] = w.batch_slot[b];
-    return launch_combine<bf16>(cb, st, true);
+    for (int b = 0; b < c.B; ++b) cb.slot_mid[b] = plan->batch_mid[b];
+    return launch_tc_combine(cb, st);
 }
 
 }  // namespace slimkv

@@ -17,7 +17,7 @@ namespace plan {
 // per (CTA, segment piece), and the slot range of every batch element.
 struct WorkPlan {
     int n_ctas = 0;
-    std::vector<int> u_begin, slot_base, batch_slot;
+    std::vector<int> u_begin, slot_base, batch_slot, slot_seg;
     int slots = 0;
 };
 
@@ -45,13 +45,14 @@ inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas) {
     const int G = (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, units));
     // Greedy packing with per-CTA budget T: a CTA takes units in order until the next
     // one would exceed T; every piece (a CTA's run inside one segment) costs
-    // kPieceCost on top of its units. `visit(u, new_cta, new_piece, b)` sees every
-    // unit boundary where a CTA or a piece starts; returns the number of CTAs.
+    // kPieceCost on top of its units. `visit(u, new_cta, b, seg)` sees every unit
+    // boundary where a CTA or a piece starts; returns the number of CTAs.
     auto pack = [&](int64_t T, auto&& visit) {
         int ctas = 1;
         int64_t cur = 0, u = 0;
         for (int b = 0; b < B; ++b)
-            for (auto& r : sl.segs) {
+            for (int si = 0; si < (int)sl.segs.size(); ++si) {
+                const auto& r = sl.segs[si];
                 int n = r.first;
                 bool open = false;   // a piece of this segment is open in the current CTA
                 while (n > 0) {
@@ -59,9 +60,9 @@ inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas) {
                         if (cur > 0 && cur + kPieceCost + r.second > T) {
                             ++ctas;
                             cur = 0;
-                            visit(u, true, b);
+                            visit(u, true, b, si);
                         } else {
-                            visit(u, false, b);
+                            visit(u, false, b, si);
                         }
                         cur += kPieceCost;
                         open = true;
@@ -70,7 +71,7 @@ inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas) {
                     if (room == 0) {
                         ++ctas;
                         cur = kPieceCost;
-                        visit(u, true, b);
+                        visit(u, true, b, si);
                         room = (T - cur) / r.second;
                     }
                     const int take = (int)std::min<int64_t>(n, room);
@@ -81,7 +82,7 @@ inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas) {
             }
         return ctas;
     };
-    auto no_visit = [](int64_t, bool, int) {};
+    auto no_visit = [](int64_t, bool, int, int) {};
     int64_t lo = std::max<int64_t>(cmax + kPieceCost, (total + G - 1) / G),
             hi = std::max<int64_t>(lo, total + (int64_t)kPieceCost * B * (int64_t)sl.segs.size());
     while (lo < hi) {
@@ -95,11 +96,12 @@ inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas) {
     std::vector<int> piece_b;
     w.u_begin.push_back(0);
     bool first = true;
-    pack(T, [&](int64_t u, bool new_cta, int b) {
+    pack(T, [&](int64_t u, bool new_cta, int b, int si) {
         if (new_cta && !first) w.u_begin.push_back((int)u);
         first = false;
         piece_cta.push_back((int)w.u_begin.size() - 1);
         piece_b.push_back(b);
+        w.slot_seg.push_back(si);
     });
     w.u_begin.push_back((int)units);
     w.n_ctas = (int)w.u_begin.size() - 1;
@@ -114,6 +116,15 @@ inline WorkPlan make_plan(int B, const SegList& sl, int max_ctas) {
     w.batch_slot[B] = (int)piece_cta.size();
     w.slots = (int)piece_cta.size();
     return w;
+}
+
+// First slot of batch element b whose piece lies in a segment with index >= seg
+// (batch_slot[b + 1] if none): with the segments of a batch element in kind order,
+// the slots of b below it hold the partials of the segments before `seg`.
+inline int first_slot_from_seg(const WorkPlan& w, int b, int seg) {
+    int s = w.batch_slot[b];
+    while (s < w.batch_slot[b + 1] && w.slot_seg[s] < seg) ++s;
+    return s;
 }
 
 }  // namespace plan

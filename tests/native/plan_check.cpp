@@ -39,6 +39,19 @@ static int check(int B, const SegList& sl, int G, int* n_ctas, int* max_pieces, 
     // batch element b's slots are contiguous and hold exactly its pieces
     for (int b = 0; b < B; ++b)
         if (w.batch_slot[b + 1] < w.batch_slot[b]) return 6;
+    // every slot records its piece's segment; inside a batch element the segments rise, so
+    // first_slot_from_seg splits b's slots into those before and from a given segment
+    if ((int)w.slot_seg.size() != w.slots) return 8;
+    for (int b = 0; b < B; ++b) {
+        for (int s = w.batch_slot[b] + 1; s < w.batch_slot[b + 1]; ++s)
+            if (w.slot_seg[s] < w.slot_seg[s - 1]) return 9;
+        for (int seg = 0; seg <= (int)sl.segs.size(); ++seg) {
+            const int m = first_slot_from_seg(w, b, seg);
+            if (m < w.batch_slot[b] || m > w.batch_slot[b + 1]) return 12;
+            for (int s = w.batch_slot[b]; s < w.batch_slot[b + 1]; ++s)
+                if ((s < m) != (w.slot_seg[s] < seg)) return 13;
+        }
+    }
     if (n_ctas) *n_ctas = w.n_ctas;
     if (max_pieces) *max_pieces = maxp;
     if (min_units) *min_units = minu;
