@@ -26,6 +26,7 @@ sample of the same workload (the pages describe a method, not a program).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -227,8 +228,11 @@ def run_slimkv(args):
     full = []
     n_buf = 0
     if mode == "full":
-        # uncompressed cache of T_full tokens per layer, drawn on the device from a
-        # seeded generator; cycled over distinct buffers when HBM is short
+        # uncompressed cache of T_full tokens per layer (the context the compressed cache
+        # stands for, N_b x ratio, when the workload names none), drawn on the device from
+        # a seeded generator; cycled over distinct buffers when HBM is short
+        if not w.T_full:
+            w = dataclasses.replace(w, T_full=w.N_b * w.ratio)
         free, _ = torch.cuda.mem_get_info()
         per_layer = 2 * w.B * w.T_full * w.Hkv * w.d * 2
         n_buf = max(2, min(w.layers, int(0.8 * free // per_layer)))

@@ -56,8 +56,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             raise RuntimeError(f"nvcc failed on {src}")
         objs.append(obj)
     tmp = LIB + ".tmp"
-    # cuBLAS serves only the reconstruction baseline's plain GEMM
-    cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas", "-lcudart_static", "-ldl", "-lrt", "-lpthread"]
+    cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lrt", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode:
         sys.stderr.write(r.stdout + r.stderr)

@@ -179,7 +179,8 @@ template <typename T>
 cudaError_t launch_simt_reconstruct(const T* C, const T* U, T* out, int rows, int n, int r,
                                     cudaStream_t st);
 
-// Materialise out[rows, n] = C[rows, r] . U[n, r]^T in bf16 (reconstruction baseline).
+// Materialise out[rows, n] = C[rows, r] . U[n, r]^T in bf16 on the tensor cores (reconstruction
+// baseline, tc_gemm.cu; n a multiple of 128, r a multiple of 16 up to 512).
 cudaError_t launch_reconstruct_gemm(const __nv_bfloat16* C, const __nv_bfloat16* U, __nv_bfloat16* out,
                                     int rows, int n, int r, cudaStream_t st);
 

@@ -1166,8 +1166,9 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
                                        lat ? c.lat_img : nullptr, c.raw_img, NPq);
     if (e != cudaSuccess) return e;
     if (c.which == SLIMKV_RECONSTRUCT) {
-        // plain launches (no early trigger): the decode below reads K_b / V_b
-        // before its own dependency wait, so they must be complete when it starts
+        // the reconstruction GEMMs (tc_gemm.cu) never release their dependents early: the
+        // decode below reads K_b / V_b before its own dependency wait, so they must be
+        // complete when it starts
         const int rows = c.B * c.N_b, n = c.Hkv * c.d;
         e = launch_reconstruct_gemm((const bf16*)c.C_K, (const bf16*)c.U_K, (bf16*)c.kb, rows, n, c.r_k, st);
         if (e != cudaSuccess) return e;
