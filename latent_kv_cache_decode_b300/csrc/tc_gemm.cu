@@ -7,19 +7,23 @@
 //
 // out[rows, n] = C[rows, r] . U[n, r]^T, bf16 operands, float32 accumulation, bf16
 // result, on the fifth-generation tensor cores (sm_103a):
-//   * one CTA per 128 rows of C; its C tile (128 x r) is loaded once by TMA into shared
-//     memory (128-byte swizzled, K-major) and serves every 128-column block of out;
+//   * one CTA per 256 rows of C (two 128-row tiles; 128 rows for ranks above 384),
+//     loaded once by TMA into shared memory (128-byte swizzled, K-major); the tiles
+//     serve every 128-column block of out, and each U chunk serves both tiles, so that
+//     U (re-read from L2 by every CTA) costs half the traffic;
 //   * U streams through a ring of 128 x 64 chunks (TMA), one per 64 of r;
-//   * warp 1 issues tcgen05.mma (M = 128, N = 128, K = 16) into one of two TMEM
-//     accumulators, so the next column block's MMAs overlap the previous block's
-//     write-out;
-//   * warps 2-5 read the accumulator with tcgen05.ld (thread = output row), round to
-//     bf16 and store 32 contiguous bytes per thread and step (whole 32-byte sectors).
+//   * warp 1 issues tcgen05.mma (M = 128, N = 128, K = 16, one per C tile) into one of
+//     two TMEM accumulators, so the next column block's MMAs overlap the previous
+//     block's write-out;
+//   * warps 2-9 read the accumulator with tcgen05.ld (thread = output row, two warps
+//     per row quarter, 32 columns per load), round to bf16 and store 64 contiguous
+//     bytes of the row per load (whole 32-byte sectors);
 // The write of `out` (rows x n bf16) dominates the traffic, so the kernel is bound by
 // HBM bandwidth, not by the tensor cores.
 #include <cuda.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "slimkv_internal.cuh"
@@ -29,12 +33,13 @@ namespace slimkv {
 
 namespace {
 
-constexpr int kGM = 128;         // rows of C per CTA (MMA M)
+constexpr int kGM = 128;         // rows of one C tile (MMA M); a CTA holds msub of them
 constexpr int kGN = 128;         // columns of out per block (MMA N)
 constexpr int kGK = 64;          // columns of r per chunk (one 128-byte swizzle span)
 constexpr int kChunk = 16384;    // bytes of one 128 x 64 bf16 chunk
-constexpr int kStages = 4;       // ring of U chunks
-constexpr int kThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 write-out
+constexpr int kMaxStages = 8;    // ring of U chunks (fewer when the C tile is large)
+constexpr int kSmemMax = 227 * 1024;
+constexpr int kThreads = 320;    // warp 0 TMA, warp 1 MMA, warps 2-9 write-out
 constexpr int kMaxR = 512;
 
 struct GemmParams {
@@ -42,6 +47,8 @@ struct GemmParams {
     CUtensorMap tmU;   // [n, r] bf16, boxes of 128 rows x 64 columns
     __nv_bfloat16* out;
     int rows, n, r;
+    int stages;        // ring slots of U (2..kMaxStages)
+    int msub;          // C tiles per CTA (1 or 2): every U chunk serves all of them
 };
 
 __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -50,20 +57,25 @@ __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_co
     const int nkc = (p.r + kGK - 1) / kGK;   // chunks of r
     const int ksteps = p.r / 16;              // 16-wide MMA k-steps
     const int nblk = p.n / kGN;               // column blocks of out
-    uint8_t* a_s = smem;                      // nkc chunks of the C tile
-    uint8_t* b_s = smem + nkc * kChunk;       // kStages chunks of U
+    const int msub = p.msub;
+    uint8_t* a_s = smem;                      // msub x nkc chunks of the C tiles
+    const int kStages = p.stages;
+    uint8_t* b_s = smem + msub * nkc * kChunk;   // kStages chunks of U
     uint64_t* bars = reinterpret_cast<uint64_t*>(b_s + kStages * kChunk);
     uint64_t* a_full = bars;                  // the C tile landed            [TMA tx]
     uint64_t* full = bars + 1;                // ring slot s holds its chunk  [TMA tx]
-    uint64_t* empty = full + kStages;         // ring slot s consumed         [commit]
-    uint64_t* acc_full = empty + kStages;     // accumulator b complete       [commit]
-    uint64_t* acc_empty = acc_full + 2;       // accumulator b read out       [128 arrivals]
+    uint64_t* empty = full + kMaxStages;      // ring slot s consumed         [commit]
+    uint64_t* acc_full = empty + kMaxStages;  // accumulator b complete       [commit]
+    uint64_t* acc_empty = acc_full + 2;       // accumulator b read out       [256 arrivals]
     uint64_t* drain = acc_empty + 2;          // every MMA of the CTA done    [commit]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(drain + 1);
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(drain + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = blockIdx.x * kGM;
+    const int row0 = blockIdx.x * kGM * msub;
+    // the CTAs take the column blocks in rotated orders, so that they do not all read the
+    // same rows of U (held by the same few L2 slices) at the same time
+    auto col_block = [&](int nb) { return (nb + blockIdx.x) % nblk; };
     if (threadIdx.x == 0) {
         ptx::mbar_init(a_full, 1);
         for (int s = 0; s < kStages; ++s) {
@@ -72,13 +84,13 @@ __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_co
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
-            ptx::mbar_init(&acc_empty[b], 128);
+            ptx::mbar_init(&acc_empty[b], 256);
         }
         ptx::mbar_init(drain, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 1) ptx::tmem_alloc(tmem_base_s, 2 * kGN);
+    if (warp == 1) ptx::tmem_alloc(tmem_base_s, 4 * kGN);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -92,15 +104,17 @@ __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_co
         if (lane == 0) {
             ptx::tma_prefetch_desc(&p.tmC);
             ptx::tma_prefetch_desc(&p.tmU);
-            ptx::mbar_expect_tx(a_full, nkc * kChunk);
-            for (int c = 0; c < nkc; ++c) ptx::tma_load_2d(a_s + c * kChunk, &p.tmC, c * kGK, row0, a_full);
+            ptx::mbar_expect_tx(a_full, msub * nkc * kChunk);
+            for (int m = 0; m < msub; ++m)
+                for (int c = 0; c < nkc; ++c)
+                    ptx::tma_load_2d(a_s + (m * nkc + c) * kChunk, &p.tmC, c * kGK, row0 + m * kGM, a_full);
             int it = 0;
             for (int nb = 0; nb < nblk && !*abort_flag; ++nb)
                 for (int c = 0; c < nkc; ++c, ++it) {
                     const int s = it % kStages;
                     if (it >= kStages) ptx::mbar_wait(&empty[s], (uint32_t)((it / kStages) - 1) & 1u, abort_flag);
                     ptx::mbar_expect_tx(&full[s], kChunk);
-                    ptx::tma_load_2d(b_s + s * kChunk, &p.tmU, c * kGK, nb * kGN, &full[s]);
+                    ptx::tma_load_2d(b_s + s * kChunk, &p.tmU, c * kGK, col_block(nb) * kGN, &full[s]);
                 }
         }
     } else if (warp == 1) {
@@ -115,7 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_co
                 const int buf = nb & 1;
                 if (nb >= 2) ptx::mbar_wait(&acc_empty[buf], (uint32_t)((nb >> 1) - 1) & 1u, abort_flag);
                 ptx::tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(buf * kGN);
+                // accumulator buf: msub blocks of kGN columns, one per C tile
+                const uint32_t d = tmem + (uint32_t)(buf * 2 * kGN);
                 for (int c = 0; c < nkc; ++c, ++it) {
                     const int s = it % kStages;
                     ptx::mbar_wait(&full[s], (uint32_t)(it / kStages) & 1u, abort_flag);
@@ -123,9 +138,11 @@ __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_co
 #pragma unroll
                     for (int kk = 0; kk < kGK / 16; ++kk) {
                         if (c * (kGK / 16) + kk >= ksteps) break;
-                        const uint64_t a = dA + (uint64_t)((c * kChunk + kk * 32) >> 4);
                         const uint64_t b = dB + (uint64_t)((s * kChunk + kk * 32) >> 4);
-                        ptx::mma_bf16(d, a, b, idesc, (c | kk) != 0 ? 1u : 0u);
+                        for (int m = 0; m < msub; ++m) {
+                            const uint64_t a = dA + (uint64_t)((((m * nkc + c) * kChunk) + kk * 32) >> 4);
+                            ptx::mma_bf16(d + (uint32_t)(m * kGN), a, b, idesc, (c | kk) != 0 ? 1u : 0u);
+                        }
                     }
                     ptx::mma_commit(&empty[s]);
                 }
@@ -135,8 +152,14 @@ __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_co
         }
     } else {
         // ------------------------------------------------------------- write-out
+        // warps 2-9: two warps per TMEM lane quadrant; with two C tiles each warp takes one
+        // tile's 32 rows, else one 64-column half of the block. A thread stores 64
+        // contiguous bytes of its row per load (whole 32-byte sectors).
         const int q4 = warp & 3;
-        const int row = q4 * 32 + lane;
+        const int w2 = (warp - 2) >> 2;          // 0 or 1
+        const int m = msub == 2 ? w2 : 0;        // C tile
+        const int c_lo = msub == 2 ? 0 : w2 * 64, c_n = msub == 2 ? kGN : 64;
+        const int row = m * kGM + q4 * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const bool row_ok = row0 + row < p.rows;
         __nv_bfloat16* orow = p.out + (size_t)(row0 + row) * p.n;
@@ -145,25 +168,25 @@ __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_co
             const bool ok = ptx::mbar_wait(&acc_full[buf], (uint32_t)(nb >> 1) & 1u, abort_flag);
             ptx::tc_fence_after();
 #pragma unroll 1
-            for (int c0 = 0; c0 < kGN; c0 += 16) {
-                float v[16];
-                ptx::tmem_ld16(tmem + lane_off + (uint32_t)(buf * kGN + c0), v);
-                uint32_t pk[8];
+            for (int c32 = c_lo; c32 < c_lo + c_n; c32 += 32) {
+                float v[32];
+                ptx::tmem_ld32(tmem + lane_off + (uint32_t)(buf * 2 * kGN + m * kGN + c32), v);
+                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     const __nv_bfloat162 h2 = ok ? __floats2bfloat162_rn(v[2 * i], v[2 * i + 1])
                                                  : __floats2bfloat162_rn(__int_as_float(0x7fc00000),
                                                                          __int_as_float(0x7fc00000));
                     pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
                 if (row_ok) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + nb * kGN + c0);
-                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    uint4* dst = reinterpret_cast<uint4*>(orow + col_block(nb) * kGN + c32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
                 }
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&acc_empty[buf]);
+            ptx::mbar_arrive(&acc_empty[buf]);   // the accumulator may take the next block
         }
     }
 
@@ -177,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_co
             ptx::mbar_wait(drain, 0, &never);   // every MMA of this CTA has completed
         }
         __syncwarp();
-        ptx::tmem_dealloc(tmem, 2 * kGN);
+        ptx::tmem_dealloc(tmem, 4 * kGN);
     }
 }
 
@@ -225,14 +248,20 @@ cudaError_t launch_reconstruct_gemm(const __nv_bfloat16* C, const __nv_bfloat16*
     p.rows = rows;
     p.n = n;
     p.r = r;
+    // shared memory: the C tiles, then ring slots of U. Two C tiles per CTA when they
+    // leave the ring at least four slots (each U chunk then serves 256 rows, halving
+    // the re-reads of U from L2), else one.
     const int nkc = (r + kGK - 1) / kGK;
-    const size_t smem = 1024 + (size_t)(nkc + kStages) * kChunk + 256;
+    p.msub = 1024 + 2 * nkc * kChunk + 256 + 4 * kChunk <= kSmemMax ? 2 : 1;
+    const int fixed = 1024 + p.msub * nkc * kChunk + 256;
+    p.stages = std::min(kMaxStages, (kSmemMax - fixed) / kChunk);
+    if (p.stages < 2) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)fixed + (size_t)p.stages * kChunk;
     static std::atomic<unsigned long long> attr_done{0};
-    const cudaError_t e = set_max_smem_once((const void*)recon_gemm_kernel,
-                                            (int)(1024 + (size_t)(kMaxR / kGK + kStages) * kChunk + 256), attr_done);
+    const cudaError_t e = set_max_smem_once((const void*)recon_gemm_kernel, kSmemMax, attr_done);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((rows + kGM - 1) / kGM);
+    cfg.gridDim = dim3((rows + kGM * p.msub - 1) / (kGM * p.msub));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
