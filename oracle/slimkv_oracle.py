@@ -153,6 +153,33 @@ def decode_attn_reconstruct(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, scale,
     return gqa_attn(q, K, V, q_pos, scale, rope_base, pairs=pairs)
 
 
+def beacon_positions(N_b: int, ratio: int) -> np.ndarray:
+    """Positions given to the beacon keys by the reconstruction baseline that keeps
+    beacon-key RoPE. Reading taken (the pages say the baseline keeps beacon key RoPE
+    but not where a beacon sits): beacon j condenses tokens j*ratio .. j*ratio +
+    ratio - 1 and takes the position of the last of them, j*ratio + ratio - 1."""
+    return np.arange(N_b, dtype=np.float64) * ratio + (ratio - 1)
+
+
+def decode_attn_reconstruct_rope(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, scale,
+                                 rope_base, ratio, pairs=None):
+    """The paper's reconstruction baseline ("Speedups are real, but memory is set by
+    the ratio": it keeps beacon key RoPE): materialise K_b = C_K U_K^T and V_b =
+    C_V U_V^T at full dimension, rotate every reconstructed beacon key of every KV
+    head at its beacon position (``beacon_positions``), then attend over beacons and
+    the raw window with standard GQA attention. Unlike ``decode_attn_reconstruct``
+    this is not equal to the latent path: a rotated key has no latent form."""
+    d = q.shape[2]
+    Hkv = U_K.shape[0] // d
+    K_b = reconstruct_kv(C_K, U_K, Hkv, d)
+    V_b = reconstruct_kv(C_V, U_V, Hkv, d)
+    for j, p in enumerate(beacon_positions(K_b.shape[1], ratio)):
+        K_b[:, j] = rope(K_b[:, j], p, rope_base)
+    K = np.concatenate([K_b, K_raw], axis=1)
+    V = np.concatenate([V_b, V_raw], axis=1)
+    return gqa_attn(q, K, V, q_pos, scale, rope_base, pairs=pairs)
+
+
 def decode_attn_full_kv(q, K, V, q_pos, scale, rope_base, pairs=None):
     """Uncompressed GQA decode over a full RoPE'd cache (the speed baseline)."""
     return gqa_attn(q, K, V, q_pos, scale, rope_base, pairs=pairs)

@@ -376,3 +376,85 @@ def test_appended_key_scores_like_the_unrotated_pair():
         assert abs(qr @ K2[0, 0, 0] - q[0, 0] @ kn[0, 0]) < 1e-5 * (1 + abs(q[0, 0] @ kn[0, 0]))
         out = O.decode_attn(q, None, None, K2, V2, None, None, np.array([p]), 0.25, 500000.0)
         assert np.allclose(out[0, 0], V2[0, 0, 0]) and np.allclose(out[0, 1], V2[0, 0, 0])
+
+
+# ------------------------------------------- reconstruction with beacon-key RoPE
+#
+# The paper's baseline keeps beacon key RoPE ("Speedups are real, but memory is set by
+# the ratio"); the pages do not say where a beacon sits, and the reading taken is the
+# last token of the block it condenses, j*ratio + ratio - 1.
+
+def _recon_rope_case(rng, B=2, Hq=4, Hkv=2, d=8, N_b=5, W=3, r=4, ratio=4):
+    return dict(q=_rand(rng, B, Hq, d), C_K=_rand(rng, B, N_b, r), C_V=_rand(rng, B, N_b, r),
+                K_raw=_rand(rng, B, W, Hkv, d), V_raw=_rand(rng, B, W, Hkv, d), U_K=_ortho(rng, Hkv * d, r),
+                U_V=_ortho(rng, Hkv * d, r), q_pos=np.array([37, 101])[:B], scale=1 / math.sqrt(d),
+                rope_base=10000.0, ratio=ratio)
+
+
+def _recon_rope_relative(c):
+    """The same attention written with relative rotations: q . R(p_j) k_j = R(p - p_j) q . k_j
+    for the beacon keys (RoPE as complex multiplication, unrotated reconstructed keys
+    built one row at a time), absolute RoPE on the query for the raw window."""
+    q, C_K, C_V, K_raw, V_raw, U_K, U_V = (c[k] for k in ("q", "C_K", "C_V", "K_raw", "V_raw", "U_K", "U_V"))
+    B, Hq, d = q.shape
+    Hkv = U_K.shape[0] // d
+    G = Hq // Hkv
+    N_b = C_K.shape[1]
+    out = np.zeros((B, Hq, d))
+    for b in range(B):
+        p = float(c["q_pos"][b])
+        for h in range(Hq):
+            g = h // G
+            s, vals = [], []
+            for j in range(N_b):
+                pj = j * c["ratio"] + c["ratio"] - 1
+                k = np.array([sum(C_K[b, j, t] * U_K[g * d + i, t] for t in range(C_K.shape[2])) for i in range(d)])
+                v = np.array([sum(C_V[b, j, t] * U_V[g * d + i, t] for t in range(C_V.shape[2])) for i in range(d)])
+                s.append(c["scale"] * float(_rope_complex(q[b, h], p - pj, c["rope_base"]) @ k))
+                vals.append(v)
+            qr = _rope_complex(q[b, h], p, c["rope_base"])
+            for t in range(K_raw.shape[1]):
+                s.append(c["scale"] * float(qr @ K_raw[b, t, g]))
+                vals.append(V_raw[b, t, g])
+            s = np.array(s)
+            e = np.exp(s - s.max())
+            out[b, h] = (e / e.sum()) @ np.array(vals)
+    return out
+
+
+def test_beacon_positions_are_the_last_token_of_each_block():
+    assert oracle.beacon_positions(4, 16).tolist() == [15.0, 31.0, 47.0, 63.0]
+    assert oracle.beacon_positions(3, 1).tolist() == [0.0, 1.0, 2.0]
+
+
+def test_reconstruct_rope_equals_relative_rotation_form():
+    rng = np.random.default_rng(31)
+    c = _recon_rope_case(rng)
+    got = oracle.decode_attn_reconstruct_rope(**c)
+    assert np.allclose(got, _recon_rope_relative(c), rtol=1e-12, atol=1e-12)
+
+
+def test_reconstruct_rope_single_beacon_at_position_zero_is_plain_reconstruction():
+    # ratio 1: the only beacon sits at position 0, where RoPE is the identity
+    rng = np.random.default_rng(32)
+    c = _recon_rope_case(rng, N_b=1, ratio=1)
+    got = oracle.decode_attn_reconstruct_rope(**c)
+    c.pop("ratio")
+    assert np.allclose(got, oracle.decode_attn_reconstruct(**c), rtol=1e-12, atol=1e-12)
+
+
+def test_reconstruct_rope_differs_from_the_latent_path():
+    # a rotated beacon key has no latent form: the two baselines disagree for ratio > 1
+    rng = np.random.default_rng(33)
+    c = _recon_rope_case(rng)
+    got = oracle.decode_attn_reconstruct_rope(**c)
+    c.pop("ratio")
+    assert not np.allclose(got, oracle.decode_attn_reconstruct(**c), rtol=1e-3, atol=1e-3)
+
+
+def test_pins_catch_wrong_beacon_position(monkeypatch):
+    rng = np.random.default_rng(34)
+    c = _recon_rope_case(rng)
+    monkeypatch.setattr(O, "beacon_positions", lambda N_b, ratio: np.arange(N_b, dtype=np.float64) * ratio)
+    got = O.decode_attn_reconstruct_rope(**c)
+    assert not np.allclose(got, _recon_rope_relative(c), rtol=1e-6, atol=1e-6)
