@@ -55,7 +55,7 @@ extern "C" {
 #endif
 
 /* 2: adds slimkv_append_kv (version 1 calls are unchanged) */
-#define SLIMKV_ABI_VERSION 2
+#define SLIMKV_ABI_VERSION 3
 
 typedef enum {
     SLIMKV_OK = 0,
@@ -127,15 +127,35 @@ slimkv_status slimkv_decode_attn(const slimkv_shape* shape, const void* q, const
  * the query only (beacon keys get none, so the result equals slimkv_decode_attn
  * up to rounding). Same arguments as slimkv_decode_attn; workspace >=
  * slimkv_workspace_bytes(shape, SLIMKV_RECONSTRUCT). Requires N_b > 0. With bf16
- * storage the materialisation is a plain cuBLAS GEMM (bf16 in, float32 accumulate);
- * its cuBLAS handle is created on the device's first reconstruction call (outside
- * any graph capture), the one allocation this library makes. */
+ * storage and d = 128 the materialisation is the library's tensor-core GEMM (bf16 in,
+ * float32 accumulate, bf16 out); otherwise a float32-accumulate SIMT GEMM. */
 slimkv_status slimkv_decode_attn_reconstruct(const slimkv_shape* shape, const void* q,
                                              const void* C_K, const void* C_V,
                                              const void* K_raw, const void* V_raw,
                                              const void* U_K, const void* U_V,
                                              const int32_t* q_pos, float* out,
                                              void* workspace, size_t ws_bytes, void* stream);
+
+/* The reconstruction baseline as the SlimKV pages run it ("Speedups are real, but
+ * memory is set by the ratio": the baseline keeps beacon key RoPE). As
+ * slimkv_decode_attn_reconstruct, except that every materialised beacon key of every
+ * KV head is rotated (rotate-half RoPE, base shape->rope_base) at its beacon's
+ * position before the attention. The pages do not say where a beacon sits; the
+ * position taken is that of the last token of the block the beacon condenses,
+ * j * beacon_ratio + beacon_ratio - 1 for beacon j. The result is therefore not
+ * equal to slimkv_decode_attn (a rotated key has no latent form); the call exists to
+ * time the pages' own baseline.
+ *   beacon_ratio   tokens per beacon (the compression ratio), >= 1
+ * Same other arguments, workspace size (SLIMKV_RECONSTRUCT) and requirements as
+ * slimkv_decode_attn_reconstruct. With bf16 storage and d = 128 the rotation is part
+ * of the tensor-core GEMM's write-out (float32, then rounded); otherwise a separate
+ * pass rotates K_b in place. */
+slimkv_status slimkv_decode_attn_reconstruct_rope(const slimkv_shape* shape, const void* q,
+                                                  const void* C_K, const void* C_V,
+                                                  const void* K_raw, const void* V_raw,
+                                                  const void* U_K, const void* U_V,
+                                                  const int32_t* q_pos, int beacon_ratio, float* out,
+                                                  void* workspace, size_t ws_bytes, void* stream);
 
 /* Uncompressed GQA decode attention ("Full KV" in the same section):
  * out[b,h,:] = softmax(scale * RoPE(q[b,h]) . K[b,:,g,:]^T) . V[b,:,g,:].

@@ -26,7 +26,7 @@ NOALLOC_SCRATCH_BYTES = 64 << 20   # SLIMKV_NOALLOC_SCRATCH_BYTES
 
 # every symbol include/slimkv.h declares
 EXPORTS = ("slimkv_workspace_bytes", "slimkv_decode_attn", "slimkv_decode_attn_reconstruct",
-           "slimkv_decode_attn_full_kv", "slimkv_status_str", "slimkv_abi_version",
+           "slimkv_decode_attn_reconstruct_rope", "slimkv_decode_attn_full_kv", "slimkv_status_str", "slimkv_abi_version",
            "slimkv_kernel_path", "slimkv_force_simt", "slimkv_time_next_decode",
            "slimkv_decode_attn_noalloc", "slimkv_append_kv")
 
@@ -64,6 +64,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.slimkv_decode_attn.restype = ctypes.c_int
     lib.slimkv_decode_attn_reconstruct.argtypes = [sp] + [vp] * 7 + [i32p, vp, vp, sz, vp]
     lib.slimkv_decode_attn_reconstruct.restype = ctypes.c_int
+    lib.slimkv_decode_attn_reconstruct_rope.argtypes = [sp] + [vp] * 7 + [i32p, ctypes.c_int, vp, vp, sz, vp]
+    lib.slimkv_decode_attn_reconstruct_rope.restype = ctypes.c_int
     lib.slimkv_decode_attn_full_kv.argtypes = [sp, vp, vp, vp, i32p, vp, vp, sz, vp]
     lib.slimkv_decode_attn_full_kv.restype = ctypes.c_int
     lib.slimkv_decode_attn_noalloc.argtypes = [sp] + [vp] * 7 + [i32p, vp, vp]
@@ -207,6 +209,28 @@ def decode_attn_reconstruct(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, *, scale
                                             _ptr(q_pos), _ptr(out), _ptr(ws), ws.numel(),
                                             _stream(stream))
     _check(st, "slimkv_decode_attn_reconstruct")
+    return out
+
+
+def decode_attn_reconstruct_rope(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, beacon_ratio, *, scale=None,
+                                 rope_base=10000.0, out=None, workspace: Optional[Workspace] = None,
+                                 stream=None):
+    """slimkv_decode_attn_reconstruct_rope on torch CUDA tensors."""
+    lib = load()
+    B, Hq, d = q.shape
+    W = K_raw.shape[1] if K_raw is not None else 0
+    sh, nb = _shape_and_bytes(SLIMKV_RECONSTRUCT, B, Hq, U_K.shape[0] // d, d, C_K.shape[1], C_K.shape[2],
+                              C_V.shape[2], W, q.dtype, scale, rope_base)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    if nb == 0:
+        _check(2, "slimkv_decode_attn_reconstruct_rope")
+    ws = (workspace or Workspace(q.device)).get(nb)
+    st = lib.slimkv_decode_attn_reconstruct_rope(ctypes.byref(sh), _ptr(q), _ptr(C_K), _ptr(C_V),
+                                                 _ptr(K_raw), _ptr(V_raw), _ptr(U_K), _ptr(U_V),
+                                                 _ptr(q_pos), int(beacon_ratio), _ptr(out), _ptr(ws),
+                                                 ws.numel(), _stream(stream))
+    _check(st, "slimkv_decode_attn_reconstruct_rope")
     return out
 
 

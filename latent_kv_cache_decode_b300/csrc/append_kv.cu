@@ -58,7 +58,48 @@ __global__ void __launch_bounds__(64) append_kv_kernel(const __grid_constant__ A
     V[dst + half + i] = vn[src + half + i];
 }
 
+// Beacon-key RoPE of the reconstruction baseline that keeps it: row R = b * N_b + j of
+// K_b [B * N_b, Hkv * d] is rotated in place at position j * ratio + ratio - 1 (the last
+// token of the block beacon j condenses). One CTA per (row, KV head); thread i rotates
+// the pair (i, i + d/2) with the same fixed-point angle reduction as the query kernel.
+struct BeaconRopeArgs {
+    void* K;                // [B * N_b, Hkv, d]
+    int N_b, Hkv, d, ratio;
+    unsigned long long turn[64];
+};
+
+template <typename T>
+__global__ void __launch_bounds__(64) beacon_rope_kernel(const __grid_constant__ BeaconRopeArgs a) {
+    const int row = blockIdx.x, g = blockIdx.y, i = threadIdx.x, half = a.d >> 1;
+    if (i >= half) return;
+    const unsigned long long j = (unsigned long long)(row % a.N_b);
+    const unsigned long long p = j * (unsigned long long)a.ratio + (unsigned long long)(a.ratio - 1);
+    T* K = static_cast<T*>(a.K) + ((size_t)row * a.Hkv + g) * a.d;
+    const float x1 = to_f(K[i]), x2 = to_f(K[half + i]);
+    const long long frac = (long long)(p * a.turn[i]);
+    float sn, cs;
+    sincospif((float)frac * 1.0842021724855044e-19f, &sn, &cs);   // x 2^-63: half-turns
+    K[i] = from_f<T>(x1 * cs - x2 * sn);
+    K[half + i] = from_f<T>(x2 * cs + x1 * sn);
+}
+
 }  // namespace
+
+template <typename T>
+cudaError_t launch_beacon_rope(T* K_b, int B, int N_b, int Hkv, int d, int ratio, double base, cudaStream_t st) {
+    BeaconRopeArgs a;
+    a.K = K_b;
+    a.N_b = N_b;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.ratio = ratio;
+    rope_turns(base, d, a.turn);
+    beacon_rope_kernel<T><<<dim3(B * N_b, Hkv), dim3(64), 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_beacon_rope<float>(float*, int, int, int, int, int, double, cudaStream_t);
+template cudaError_t launch_beacon_rope<__nv_bfloat16>(__nv_bfloat16*, int, int, int, int, int, double, cudaStream_t);
 
 template <typename T>
 cudaError_t launch_append_kv(const T* k_new, const T* v_new, T* K, T* V, const int32_t* pos, int B, int Hkv,

@@ -122,6 +122,7 @@ struct Ptrs {
     float* out;
     void* ws;
     size_t ws_bytes;
+    int beacon_ratio;   // reconstruction baseline with beacon-key RoPE (0: without)
 };
 
 slimkv_status check_ptrs(const slimkv_shape* s, int which, const Ptrs& p) {
@@ -176,6 +177,9 @@ slimkv_status run_simt(const slimkv_shape* s, int which, const Ptrs& p, cudaStre
         const int rows = s->B * s->N_b, n = s->Hkv * s->d;
         if (launch_simt_reconstruct<T>((const T*)p.C_K, (const T*)p.U_K, kb, rows, n, s->r_k, st) !=
             cudaSuccess)
+            return SLIMKV_ERR_CUDA;
+        if (p.beacon_ratio > 0 &&
+            launch_beacon_rope<T>(kb, s->B, s->N_b, s->Hkv, s->d, p.beacon_ratio, s->rope_base, st) != cudaSuccess)
             return SLIMKV_ERR_CUDA;
         if (launch_simt_reconstruct<T>((const T*)p.C_V, (const T*)p.U_V, vb, rows, n, s->r_v, st) !=
             cudaSuccess)
@@ -268,6 +272,7 @@ slimkv_status run(const slimkv_shape* s, int which, const Ptrs& p, void* stream)
         c.vb = ws + L.vb;
         c.slots = L.slots;
         c.Dmax = L.Dmax;
+        c.beacon_ratio = p.beacon_ratio;
         return tc_run(c, cs) == cudaSuccess ? SLIMKV_OK : SLIMKV_ERR_CUDA;
     }
     if (s->dtype == SLIMKV_F32) return run_simt<float>(s, which, p, cs);
@@ -287,7 +292,7 @@ slimkv_status slimkv_decode_attn(const slimkv_shape* shape, const void* q, const
                                  const void* C_V, const void* K_raw, const void* V_raw,
                                  const void* U_K, const void* U_V, const int32_t* q_pos,
                                  float* out, void* workspace, size_t ws_bytes, void* stream) {
-    Ptrs p{q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, out, workspace, ws_bytes};
+    Ptrs p{q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, out, workspace, ws_bytes, 0};
     return run(shape, SLIMKV_LATENT, p, stream);
 }
 
@@ -297,14 +302,25 @@ slimkv_status slimkv_decode_attn_reconstruct(const slimkv_shape* shape, const vo
                                              const void* U_K, const void* U_V,
                                              const int32_t* q_pos, float* out,
                                              void* workspace, size_t ws_bytes, void* stream) {
-    Ptrs p{q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, out, workspace, ws_bytes};
+    Ptrs p{q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, out, workspace, ws_bytes, 0};
+    return run(shape, SLIMKV_RECONSTRUCT, p, stream);
+}
+
+slimkv_status slimkv_decode_attn_reconstruct_rope(const slimkv_shape* shape, const void* q,
+                                                  const void* C_K, const void* C_V,
+                                                  const void* K_raw, const void* V_raw,
+                                                  const void* U_K, const void* U_V,
+                                                  const int32_t* q_pos, int beacon_ratio, float* out,
+                                                  void* workspace, size_t ws_bytes, void* stream) {
+    if (beacon_ratio < 1) return SLIMKV_ERR_SHAPE;
+    Ptrs p{q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, out, workspace, ws_bytes, beacon_ratio};
     return run(shape, SLIMKV_RECONSTRUCT, p, stream);
 }
 
 slimkv_status slimkv_decode_attn_full_kv(const slimkv_shape* shape, const void* q, const void* K,
                                          const void* V, const int32_t* q_pos, float* out,
                                          void* workspace, size_t ws_bytes, void* stream) {
-    Ptrs p{q, nullptr, nullptr, K, V, nullptr, nullptr, q_pos, out, workspace, ws_bytes};
+    Ptrs p{q, nullptr, nullptr, K, V, nullptr, nullptr, q_pos, out, workspace, ws_bytes, 0};
     return run(shape, SLIMKV_FULL_KV, p, stream);
 }
 

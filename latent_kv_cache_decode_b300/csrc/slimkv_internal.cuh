@@ -180,8 +180,15 @@ cudaError_t launch_simt_reconstruct(const T* C, const T* U, T* out, int rows, in
                                     cudaStream_t st);
 
 // Materialise out[rows, n] = C[rows, r] . U[n, r]^T in bf16 on the tensor cores (reconstruction
-// baseline, tc_gemm.cu; n a multiple of 128, r a multiple of 16 up to 512).
+// baseline, tc_gemm.cu; n a multiple of 128, r a multiple of 16 up to 512). With beacon_ratio > 0
+// every 128-column block of a row (one KV head, d = 128) is also rotated (rotate-half RoPE) at
+// position j * beacon_ratio + beacon_ratio - 1, j = row % rows_per_b (the beacon index).
 cudaError_t launch_reconstruct_gemm(const __nv_bfloat16* C, const __nv_bfloat16* U, __nv_bfloat16* out,
-                                    int rows, int n, int r, cudaStream_t st);
+                                    int rows, int n, int r, cudaStream_t st, int beacon_ratio = 0,
+                                    int rows_per_b = 0, double rope_base = 10000.0);
+// Rotate the rows of materialised beacon keys K_b [B * N_b, Hkv, d] in place at their beacon
+// positions j * ratio + ratio - 1 (append_kv.cu; the SIMT path of the same baseline).
+template <typename T>
+cudaError_t launch_beacon_rope(T* K_b, int B, int N_b, int Hkv, int d, int ratio, double base, cudaStream_t st);
 
 }  // namespace slimkv

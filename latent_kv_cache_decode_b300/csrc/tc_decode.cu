@@ -1170,7 +1170,8 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
         // decode below reads K_b / V_b before its own dependency wait, so they must be
         // complete when it starts
         const int rows = c.B * c.N_b, n = c.Hkv * c.d;
-        e = launch_reconstruct_gemm((const bf16*)c.C_K, (const bf16*)c.U_K, (bf16*)c.kb, rows, n, c.r_k, st);
+        e = launch_reconstruct_gemm((const bf16*)c.C_K, (const bf16*)c.U_K, (bf16*)c.kb, rows, n, c.r_k, st,
+                                    c.beacon_ratio, c.N_b, c.rope_base);
         if (e != cudaSuccess) return e;
         e = launch_reconstruct_gemm((const bf16*)c.C_V, (const bf16*)c.U_V, (bf16*)c.vb, rows, n, c.r_v, st);
         if (e != cudaSuccess) return e;

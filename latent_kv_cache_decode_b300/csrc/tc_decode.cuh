@@ -32,6 +32,7 @@ struct TcCall {
     void* vb;
     int slots;
     int Dmax;
+    int beacon_ratio;          // SLIMKV_RECONSTRUCT: > 0 rotates the beacon keys (RoPE at j*ratio + ratio - 1)
 };
 
 // Whether the tensor-core path handles these sizes (bf16 storage assumed).

@@ -18,6 +18,9 @@
 //   * warps 2-9 read the accumulator with tcgen05.ld (thread = output row, two warps
 //     per row quarter, 32 columns per load), round to bf16 and store 64 contiguous
 //     bytes of the row per load (whole 32-byte sectors);
+//   * for the baseline that keeps beacon-key RoPE the write-out also rotates each
+//     128-column block (one KV head) of a key row at its beacon's position, in float32
+//     before the rounding.
 // The write of `out` (rows x n bf16) dominates the traffic, so the kernel is bound by
 // HBM bandwidth, not by the tensor cores.
 #include <cuda.h>
@@ -49,6 +52,10 @@ struct GemmParams {
     int rows, n, r;
     int stages;        // ring slots of U (2..kMaxStages)
     int msub;          // C tiles per CTA (1 or 2): every U chunk serves all of them
+    // beacon-key RoPE (ratio > 0): row R is beacon j = R % rows_per_b, rotated at position
+    // j * ratio + ratio - 1; turn[i] = theta_i / (2 pi) as a 64-bit fraction of a turn
+    int ratio, rows_per_b;
+    unsigned long long turn[64];
 };
 
 __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -152,41 +159,92 @@ __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_co
         }
     } else {
         // ------------------------------------------------------------- write-out
-        // warps 2-9: two warps per TMEM lane quadrant; with two C tiles each warp takes one
-        // tile's 32 rows, else one 64-column half of the block. A thread stores 64
-        // contiguous bytes of its row per load (whole 32-byte sectors).
+        // warps 2-9: two warps per TMEM lane quadrant. A thread stores 64 contiguous bytes
+        // of its row per load (whole 32-byte sectors).
         const int q4 = warp & 3;
         const int w2 = (warp - 2) >> 2;          // 0 or 1
-        const int m = msub == 2 ? w2 : 0;        // C tile
-        const int c_lo = msub == 2 ? 0 : w2 * 64, c_n = msub == 2 ? kGN : 64;
-        const int row = m * kGM + q4 * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const bool row_ok = row0 + row < p.rows;
-        __nv_bfloat16* orow = p.out + (size_t)(row0 + row) * p.n;
-        for (int nb = 0; nb < nblk; ++nb) {
-            const int buf = nb & 1;
-            const bool ok = ptx::mbar_wait(&acc_full[buf], (uint32_t)(nb >> 1) & 1u, abort_flag);
-            ptx::tc_fence_after();
-#pragma unroll 1
-            for (int c32 = c_lo; c32 < c_lo + c_n; c32 += 32) {
-                float v[32];
-                ptx::tmem_ld32(tmem + lane_off + (uint32_t)(buf * 2 * kGN + m * kGN + c32), v);
-                uint32_t pk[16];
+        if (p.ratio > 0) {
+            // beacon-key RoPE (one C tile): a column block is one KV head (d = 128); warp
+            // half w2 rotates the pairs (i, i + 64) for i in [32 w2, 32 w2 + 32), holding the
+            // row's cos / sin for them across all blocks
+            const int row = q4 * 32 + lane;
+            const bool row_ok = row0 + row < p.rows;
+            __nv_bfloat16* orow = p.out + (size_t)(row0 + row) * p.n;
+            const unsigned long long j = (unsigned long long)((row0 + row) % p.rows_per_b);
+            const unsigned long long pos = j * (unsigned long long)p.ratio + (unsigned long long)(p.ratio - 1);
+            float cs[32], sn[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                // the angle reduced to a signed fraction of a turn (exact 64-bit wrap-around)
+                const long long frac = (long long)(pos * p.turn[w2 * 32 + k]);
+                sincospif((float)frac * 1.0842021724855044e-19f, &sn[k], &cs[k]);   // x 2^-63: half-turns
+            }
+            for (int nb = 0; nb < nblk; ++nb) {
+                const int buf = nb & 1;
+                const bool ok = ptx::mbar_wait(&acc_full[buf], (uint32_t)(nb >> 1) & 1u, abort_flag);
+                ptx::tc_fence_after();
+                float x1[32], x2[32];
+                ptx::tmem_ld32(tmem + lane_off + (uint32_t)(buf * 2 * kGN + w2 * 32), x1);
+                ptx::tmem_ld32(tmem + lane_off + (uint32_t)(buf * 2 * kGN + 64 + w2 * 32), x2);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&acc_empty[buf]);   // the accumulator may take the next block
+                uint32_t pk1[16], pk2[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const __nv_bfloat162 h2 = ok ? __floats2bfloat162_rn(v[2 * i], v[2 * i + 1])
-                                                 : __floats2bfloat162_rn(__int_as_float(0x7fc00000),
-                                                                         __int_as_float(0x7fc00000));
-                    pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
+                    const float a0 = x1[2 * i] * cs[2 * i] - x2[2 * i] * sn[2 * i];
+                    const float a1 = x1[2 * i + 1] * cs[2 * i + 1] - x2[2 * i + 1] * sn[2 * i + 1];
+                    const float b0 = x2[2 * i] * cs[2 * i] + x1[2 * i] * sn[2 * i];
+                    const float b1 = x2[2 * i + 1] * cs[2 * i + 1] + x1[2 * i + 1] * sn[2 * i + 1];
+                    const float nan = __int_as_float(0x7fc00000);
+                    const __nv_bfloat162 h1 = __floats2bfloat162_rn(ok ? a0 : nan, ok ? a1 : nan);
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(ok ? b0 : nan, ok ? b1 : nan);
+                    pk1[i] = *reinterpret_cast<const uint32_t*>(&h1);
+                    pk2[i] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
                 if (row_ok) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + col_block(nb) * kGN + c32);
+                    uint4* d1 = reinterpret_cast<uint4*>(orow + col_block(nb) * kGN + w2 * 32);
+                    uint4* d2 = reinterpret_cast<uint4*>(orow + col_block(nb) * kGN + 64 + w2 * 32);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    for (int k = 0; k < 4; ++k) {
+                        d1[k] = make_uint4(pk1[4 * k], pk1[4 * k + 1], pk1[4 * k + 2], pk1[4 * k + 3]);
+                        d2[k] = make_uint4(pk2[4 * k], pk2[4 * k + 1], pk2[4 * k + 2], pk2[4 * k + 3]);
+                    }
                 }
             }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&acc_empty[buf]);   // the accumulator may take the next block
+        } else {
+            // with two C tiles each warp takes one tile's 32 rows, else one 64-column half
+            const int m = msub == 2 ? w2 : 0;        // C tile
+            const int c_lo = msub == 2 ? 0 : w2 * 64, c_n = msub == 2 ? kGN : 64;
+            const int row = m * kGM + q4 * 32 + lane;
+            const bool row_ok = row0 + row < p.rows;
+            __nv_bfloat16* orow = p.out + (size_t)(row0 + row) * p.n;
+            for (int nb = 0; nb < nblk; ++nb) {
+                const int buf = nb & 1;
+                const bool ok = ptx::mbar_wait(&acc_full[buf], (uint32_t)(nb >> 1) & 1u, abort_flag);
+                ptx::tc_fence_after();
+#pragma unroll 1
+                for (int c32 = c_lo; c32 < c_lo + c_n; c32 += 32) {
+                    float v[32];
+                    ptx::tmem_ld32(tmem + lane_off + (uint32_t)(buf * 2 * kGN + m * kGN + c32), v);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const __nv_bfloat162 h2 = ok ? __floats2bfloat162_rn(v[2 * i], v[2 * i + 1])
+                                                     : __floats2bfloat162_rn(__int_as_float(0x7fc00000),
+                                                                             __int_as_float(0x7fc00000));
+                        pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+                    if (row_ok) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + col_block(nb) * kGN + c32);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    }
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&acc_empty[buf]);   // the accumulator may take the next block
+            }
         }
     }
 
@@ -239,8 +297,10 @@ bool make_map_2d(CUtensorMap* tm, const void* base, int cols, int64_t rows) {
 }  // namespace
 
 cudaError_t launch_reconstruct_gemm(const __nv_bfloat16* C, const __nv_bfloat16* U, __nv_bfloat16* out,
-                                    int rows, int n, int r, cudaStream_t st) {
+                                    int rows, int n, int r, cudaStream_t st, int beacon_ratio, int rows_per_b,
+                                    double rope_base) {
     if (rows <= 0 || n <= 0 || n % kGN != 0 || r < 16 || r % 16 != 0 || r > kMaxR) return cudaErrorInvalidValue;
+    if (beacon_ratio > 0 && rows_per_b <= 0) return cudaErrorInvalidValue;
     GemmParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map_2d(&p.tmC, C, r, rows) || !make_map_2d(&p.tmU, U, r, n)) return cudaErrorInvalidValue;
@@ -248,11 +308,14 @@ cudaError_t launch_reconstruct_gemm(const __nv_bfloat16* C, const __nv_bfloat16*
     p.rows = rows;
     p.n = n;
     p.r = r;
+    p.ratio = beacon_ratio > 0 ? beacon_ratio : 0;
+    p.rows_per_b = rows_per_b;
+    if (p.ratio > 0) rope_turns(rope_base, kGN, p.turn);
     // shared memory: the C tiles, then ring slots of U. Two C tiles per CTA when they
     // leave the ring at least four slots (each U chunk then serves 256 rows, halving
     // the re-reads of U from L2), else one.
     const int nkc = (r + kGK - 1) / kGK;
-    p.msub = 1024 + 2 * nkc * kChunk + 256 + 4 * kChunk <= kSmemMax ? 2 : 1;
+    p.msub = p.ratio == 0 && 1024 + 2 * nkc * kChunk + 256 + 4 * kChunk <= kSmemMax ? 2 : 1;
     const int fixed = 1024 + p.msub * nkc * kChunk + 256;
     p.stages = std::min(kMaxStages, (kSmemMax - fixed) / kChunk);
     if (p.stages < 2) return cudaErrorInvalidValue;

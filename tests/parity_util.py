@@ -34,6 +34,10 @@ def run_gpu(which, w, t, out=None):
         o = bd.decode_attn_reconstruct(d["q"], d["C_K"], d["C_V"], d["K_raw"] if w.W else None,
                                        d["V_raw"] if w.W else None, d["U_K"], d["U_V"],
                                        d["q_pos"], **kw)
+    elif which == "reconstruct_rope":
+        o = bd.decode_attn_reconstruct_rope(d["q"], d["C_K"], d["C_V"], d["K_raw"] if w.W else None,
+                                            d["V_raw"] if w.W else None, d["U_K"], d["U_V"],
+                                            d["q_pos"], w.ratio, **kw)
     else:
         o = bd.decode_attn_full_kv(d["q"], d["K_full"], d["V_full"], d["q_pos"], **kw)
     torch.cuda.synchronize()
@@ -50,6 +54,10 @@ def run_oracle(which, w, t, pairs=None):
         return oracle.decode_attn_reconstruct(f["q"], f["C_K"], f["C_V"], f["K_raw"], f["V_raw"],
                                               f["U_K"], f["U_V"], f["q_pos"], w.scale, w.rope_base,
                                               pairs=pairs)
+    if which == "reconstruct_rope":
+        return oracle.decode_attn_reconstruct_rope(f["q"], f["C_K"], f["C_V"], f["K_raw"], f["V_raw"],
+                                                   f["U_K"], f["U_V"], f["q_pos"], w.scale, w.rope_base,
+                                                   w.ratio, pairs=pairs)
     return oracle.decode_attn_full_kv(f["q"], f["K_full"], f["V_full"], f["q_pos"], w.scale,
                                       w.rope_base, pairs=pairs)
 

@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.slimkv_abi_version() == 2
+    assert lib.slimkv_abi_version() == 3
     for code, name in bd.STATUS.items():
         s = lib.slimkv_status_str(code)
         assert isinstance(s, bytes) and len(s) > 0
@@ -172,3 +172,19 @@ def test_plain_c_consumer(lib, tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "c abi ok" in r.stdout
+
+
+def test_reconstruct_rope_host_checks(lib):
+    # a beacon ratio below 1 is rejected before any launch; otherwise the checks of the
+    # plain reconstruction apply (here: a workspace one byte short, a NULL pointer)
+    s = _shape()
+    good = [256 * (i + 1) for i in range(7)] + [4096]
+    need = bd.workspace_bytes(s, bd.SLIMKV_RECONSTRUCT)
+    fn = lib.slimkv_decode_attn_reconstruct_rope
+    for bad_ratio in (0, -3):
+        assert fn(ctypes.byref(s), *good, bad_ratio, 8192, 1 << 20, need, None) == 2
+    assert fn(ctypes.byref(s), *good, 16, 8192, 1 << 20, need - 1, None) == 5
+    nul = list(good)
+    nul[1] = None
+    assert fn(ctypes.byref(s), *nul, 16, 8192, 1 << 20, need, None) == 1
+    assert fn(ctypes.byref(_shape(N_b=0)), *good, 16, 8192, 1 << 20, 1 << 40, None) == 2

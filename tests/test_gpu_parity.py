@@ -165,3 +165,28 @@ def test_repeated_calls_reuse_workspace():
                                    workspace=ws).cpu())
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+# The reconstruction baseline that keeps beacon-key RoPE: tensor-core path (the rotation
+# in the GEMM's write-out), and the SIMT path (float32 storage, or d = 64).
+@pytest.mark.parametrize("case", [
+    ("config0-f32", None),
+    ("bf16-tc", dict(B=2, Hq=8, Hkv=2, d=128, N_b=256, W=64, rank=64, ratio=4)),
+    ("bf16-tc-rank320", dict(B=1, Hq=8, Hkv=4, d=128, N_b=300, W=40, rank=320, ratio=16)),
+    ("bf16-simt-d64", dict(B=2, Hq=4, Hkv=1, d=64, N_b=96, W=32, rank=64, ratio=8)),
+])
+def test_reconstruct_rope_matches_oracle(case):
+    name, kw = case
+    w = wl.config(0) if kw is None else wl.custom(**kw)
+    t = wl.layer_tensors(w, 0)
+    got = run_gpu("reconstruct_rope", w, t)
+    ref = run_oracle("reconstruct_rope", w, t)
+    assert_close(got, ref, w.dtype, f"reconstruct-rope {name}")
+
+
+def test_config1_reconstruct_rope_one_layer():
+    # beacon positions up to 4095 * 8 + 7 at the 32K context of config 1
+    w = wl.config(1)
+    t = wl.layer_tensors(w, 1)
+    assert_close(run_gpu("reconstruct_rope", w, t), run_oracle("reconstruct_rope", w, t), "bf16",
+                 "config1 reconstruct-rope")
