@@ -9,7 +9,8 @@ with its own cache buffers in HBM (4 GiB of cache per step, far larger than L2,
 so no flush is needed between steps).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl slimkv|reference]
-                  [--config 2] [--mode latent|reconstruct|full] [--loop 128] [--layers N]
+                  [--config 2] [--mode latent|reconstruct|reconstruct_rope|full] [--loop 128]
+                  [--layers N] [--no-companions]
 
 Besides the device-timed step (`value`), the line carries the split-decode
 kernel's roofline (CUDA events around its launch; DRAM traffic from the committed
@@ -18,7 +19,11 @@ public API with one packed host copy of every layer's inputs in and of every
 output out per step (`e2e`), the CPU oracle's time on a sample of the step
 (`cpu_baseline`), the SM clocks sampled during the timed region, and a
 multi-step decode of `--loop` generated tokens (window append + decode per layer,
-`decode_loop`). Under torchrun each rank decodes its own share of the batch.
+`decode_loop`), and, for the headline workload, the comparison kernels timed on the
+same layers (`baselines`: the reconstruction baseline without and with beacon-key
+RoPE, full-KV attention over the 131072-token uncompressed cache) and the other two
+workloads' decode steps (`configs`). Under torchrun each rank decodes its own share
+of the batch.
 
 --impl reference times the float64 CPU oracle on the host cores on a bounded
 sample of the same workload (the pages describe a method, not a program).
@@ -183,6 +188,91 @@ def oracle_layer_seconds(w, layers_sample):
     return secs
 
 
+def time_layer_graph(calls, dev, steps: int, warmup: int):
+    """Device time (us) of one step: every call of `calls` once, in a CUDA graph on a
+    stream of its own, CUDA events around `steps` replays after `warmup`."""
+    import torch
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in calls:
+            c(stream)
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return a.elapsed_time(b) * 1e3 / steps
+
+
+def companion_measurements(args, w, layers, dev, peak):
+    """The comparison kernels on the headline workload's own layers (the reconstruction
+    baseline without and with beacon-key RoPE, full-KV attention over the uncompressed
+    131072-token cache), and the other two workloads' decode steps, each timed as a CUDA
+    graph of all layers (device time per step)."""
+    import torch
+    from latent_kv_cache_decode_b300 import binding as bd
+    from latent_kv_cache_decode_b300 import workloads as wl
+    steps, warm = max(3, min(args.steps, 10)), 3
+    ws = bd.Workspace(dev)
+    outs = [torch.empty((w.B, w.Hq, w.d), dtype=torch.float32, device=dev) for _ in layers]
+    kw = lambda l, st: dict(scale=w.scale, rope_base=w.rope_base, out=outs[l], workspace=ws, stream=st)
+    rec = [lambda st, l=l, t=t: bd.decode_attn_reconstruct(t["q"], t["C_K"], t["C_V"], t["K_raw"], t["V_raw"],
+                                                             t["U_K"], t["U_V"], t["q_pos"], **kw(l, st))
+           for l, t in enumerate(layers)]
+    rec_rope = [lambda st, l=l, t=t: bd.decode_attn_reconstruct_rope(t["q"], t["C_K"], t["C_V"], t["K_raw"],
+                                                                       t["V_raw"], t["U_K"], t["U_V"], t["q_pos"],
+                                                                       w.ratio, **kw(l, st))
+                for l, t in enumerate(layers)]
+    base = {"workload": w.name, "layers": w.layers,
+            "reconstruct_us": time_layer_graph(rec, dev, steps, warm),
+            "reconstruct_rope_us": time_layer_graph(rec_rope, dev, steps, warm)}
+    # full KV: the uncompressed cache the beacons stand for (N_b x ratio = 131072 tokens),
+    # two distinct per-layer buffers of 4 GiB each (>> L2) cycled over the layers
+    T = w.T_full or w.N_b * w.ratio
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    full = [(torch.randn((w.B, T, w.Hkv, w.d), generator=g, device=dev, dtype=torch.bfloat16),
+             torch.randn((w.B, T, w.Hkv, w.d), generator=g, device=dev, dtype=torch.bfloat16)) for _ in range(2)]
+    fkv = [lambda st, l=l, t=t: bd.decode_attn_full_kv(t["q"], full[l % 2][0], full[l % 2][1], t["q_pos"],
+                                                         **kw(l, st))
+           for l, t in enumerate(layers)]
+    base["full_kv_us"] = time_layer_graph(fkv, dev, max(3, steps // 2), warm)
+    base["full_kv_cache_tokens"] = T
+    base["full_kv_buffers"] = "2 distinct per-layer buffers of 4 GiB, cycled"
+    del full
+    torch.cuda.empty_cache()
+    cfgs = {}
+    for cfg in (1, 3):
+        wc = _workload(cfg, args.layers)
+        lc = build_layers(wc, dev)
+        oc = [torch.empty((wc.B, wc.Hq, wc.d), dtype=torch.float32, device=dev) for _ in lc]
+        wsc = bd.Workspace(dev)
+        calls = [lambda st, l=l, t=t: bd.decode_attn(t["q"], t["C_K"], t["C_V"], t["K_raw"], t["V_raw"], t["U_K"],
+                                                      t["U_V"], t["q_pos"], scale=wc.scale, rope_base=wc.rope_base,
+                                                      out=oc[l], workspace=wsc, stream=st)
+                 for l, t in enumerate(lc)]
+        us = time_layer_graph(calls, dev, steps, warm)
+        cache_b = sum(wl.cache_bytes(wc, l) for l in range(wc.layers))
+        cfgs[wc.name] = {"us_per_step": us, "layers": wc.layers, "batch": wc.B, "cache_bytes_per_step": cache_b,
+                         "hbm_gbs": cache_b / (us * 1e-6) / 1e9,
+                         "frac_of_measured_copy": cache_b / (us * 1e-6) / 1e9 / peak}
+        del lc, oc, wsc
+        torch.cuda.empty_cache()
+    return base, cfgs
+
+
 def run_reference(args):
     """CPU oracle arm: each step is one sampled layer, reported per full step."""
     w = _workload(args.config, args.layers)
@@ -254,6 +344,9 @@ def run_slimkv(args):
         elif mode == "reconstruct":
             bd.decode_attn_reconstruct(t["q"], t["C_K"], t["C_V"], t["K_raw"], t["V_raw"], t["U_K"],
                                        t["U_V"], t["q_pos"], **kw)
+        elif mode == "reconstruct_rope":
+            bd.decode_attn_reconstruct_rope(t["q"], t["C_K"], t["C_V"], t["K_raw"], t["V_raw"], t["U_K"],
+                                            t["U_V"], t["q_pos"], w.ratio, **kw)
         else:
             K, V = full[l % n_buf]
             bd.decode_attn_full_kv(t["q"], K, V, t["q_pos"], **kw)
@@ -397,7 +490,7 @@ def run_slimkv(args):
     us = ms * 1e3
     layer_bytes = cache_b / w.layers
     achieved = layer_bytes / (kern_avg_ms * 1e-3) / 1e9
-    launches_per_call = {"latent": 3, "reconstruct": 5, "full": 3}[mode]
+    launches_per_call = {"latent": 3, "reconstruct": 5, "reconstruct_rope": 5, "full": 3}[mode]
     res = {
         "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
@@ -423,6 +516,8 @@ def run_slimkv(args):
     }
     if loop is not None:
         res["decode_loop"] = loop
+    if args.companions and world == 1 and mode == "latent" and args.config == 2:
+        res["baselines"], res["configs"] = companion_measurements(args, w, layers, dev, peak)
     if not args.no_cpu_baseline and world == 1:
         sample_layers = [0, w.layers // 2]
         secs = oracle_layer_seconds(w, sample_layers)
@@ -442,10 +537,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="slimkv", choices=["slimkv", "reference"])
     ap.add_argument("--config", type=int, default=2)
-    ap.add_argument("--mode", default="latent", choices=["latent", "reconstruct", "full"])
+    ap.add_argument("--mode", default="latent", choices=["latent", "reconstruct", "reconstruct_rope", "full"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--loop", type=int, default=128,
                     help="generated tokens of the multi-step decode measurement (0: skip)")
+    ap.add_argument("--no-companions", dest="companions", action="store_false",
+                    help="skip the comparison kernels and the other workloads in the line")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers (small profiling captures; 0 = all)")
     args = ap.parse_args()
