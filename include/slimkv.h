@@ -186,7 +186,10 @@ slimkv_status slimkv_decode_attn_full_kv(const slimkv_shape* shape, const void* 
  *    launch; other argument errors are reported as by slimkv_decode_attn.
  *  - The first call on a device looks up the array's device address on that device
  *    (cudaGetSymbolAddress, with that device current); make that first call before
- *    any stream capture. A failed lookup returns SLIMKV_ERR_CUDA.
+ *    any stream capture. A failed lookup returns SLIMKV_ERR_CUDA. The address is kept
+ *    for the life of the process: it does not survive cudaDeviceReset (or any other
+ *    teardown of the device's primary context), after which this call must not be
+ *    used again in the same process.
  *  - All calls on a device share the one array, and it keeps the previous call's
  *    contents; no call depends on them (each writes every scratch word before
  *    reading it). Calls that may overlap on the GPU (different streams, or

@@ -8,9 +8,13 @@ from latent_kv_cache_decode_b300 import binding as bd
 from latent_kv_cache_decode_b300 import workloads as wl
 
 # tolerances: float32 storage -> max-abs 1e-5; bf16 storage (float32 accumulate)
-# -> relative L2 <= 3e-3 and max-abs <= 2e-2
+# -> relative L2 <= 3e-3 over the whole output, <= 1.2e-2 for every single (b, h) row
+# (a row is one head's weighted average: the rounding of its bf16 inputs and weights
+# does not average out over other heads, so its bar is 4x the global one), and
+# max-abs <= 2e-2
 F32_MAX_ABS = 1e-5
 BF16_REL_L2 = 3e-3
+BF16_ROW_REL_L2 = 1.2e-2
 BF16_MAX_ABS = 2e-2
 
 
@@ -68,6 +72,14 @@ def errors(got, ref):
     return rel, float(np.abs(diff).max())
 
 
+def row_errors(got, ref):
+    """Relative L2 error of every (b, h) output row (last axis), and the worst row."""
+    g = got.reshape(-1, got.shape[-1])
+    r = ref.reshape(-1, ref.shape[-1])
+    rel = np.linalg.norm(g - r, axis=1) / np.maximum(np.linalg.norm(r, axis=1), 1e-30)
+    return rel, int(np.argmax(rel))
+
+
 def assert_close(got, ref, dtype, what=""):
     rel, mx = errors(got, ref)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
@@ -76,4 +88,8 @@ def assert_close(got, ref, dtype, what=""):
     else:
         assert rel <= BF16_REL_L2 and mx <= BF16_MAX_ABS, \
             f"{what}: rel-L2 {rel:.3e} (bar {BF16_REL_L2}), max-abs {mx:.3e} (bar {BF16_MAX_ABS})"
+        rows, worst = row_errors(got, ref)
+        assert rows[worst] <= BF16_ROW_REL_L2, \
+            f"{what}: row {worst} (b, h) = {divmod(worst, got.shape[-2])} rel-L2 {rows[worst]:.3e} " \
+            f"(bar {BF16_ROW_REL_L2}; whole-output rel-L2 {rel:.3e})"
     return rel, mx

@@ -20,6 +20,10 @@ CASES = {
     "f32-simt": dict(dtype="f32", B=1, Hq=4, Hkv=1, d=64, N_b=64, W=32, rank=32, ratio=32),
     # raw window only (no beacons), tensor-core path
     "bf16-window-only": dict(B=1, Hq=8, Hkv=2, d=128, N_b=0, W=32, rank=64, ratio=4),
+    # the headline shape per batch element (32 / 8 heads, rank 256, 16x) with its peaked
+    # raw keys (1% of the window's tokens scaled x8 before RoPE), two batch elements
+    "bf16-headline-peaked": dict(B=2, Hq=32, Hkv=8, d=128, N_b=512, W=256, rank=256, ratio=16,
+                                 peak_frac=0.01, peak_scale=8.0),
 }
 
 

@@ -5,7 +5,11 @@ is a fixed device array inside the library, so the call takes no workspace.
 
 Checked through the C ABI against slimkv_decode_attn (same inputs, caller-allocated
 workspace) on two calls in a row with different inputs: the second call must not be
-affected by what the first left in the shared array. Collected last on purpose.
+affected by what the first left in the shared array. Both entry points run the same
+kernels with the same plan, so their outputs are compared bit for bit, and both are
+compared with the float64 oracle. A large call followed by a small one checks that the
+small call reads nothing the large one left behind: its reference runs on a fresh
+workspace filled with NaN bytes. Collected last on purpose.
 """
 import ctypes
 import dataclasses
@@ -15,7 +19,7 @@ import torch
 
 from latent_kv_cache_decode_b300 import binding as bd
 from latent_kv_cache_decode_b300 import workloads as wl
-from tests.parity_util import assert_close, to_dev
+from tests.parity_util import assert_close, run_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -35,9 +39,13 @@ def _noalloc_call(lib, sh, t, out):
         t["q_pos"].data_ptr(), out.data_ptr(), stream)
 
 
-def _with_workspace(w, t):
+def _with_workspace(w, t, nan_fill=False):
+    ws = bd.Workspace(torch.device("cuda", 0))
+    if nan_fill:
+        nb = bd.workspace_bytes(_shape(w), bd.SLIMKV_LATENT)
+        ws.get(nb).fill_(0xFF)                   # every float32 word reads as NaN
     return bd.decode_attn(t["q"], t["C_K"], t["C_V"], t["K_raw"], t["V_raw"], t["U_K"],
-                          t["U_V"], t["q_pos"], scale=w.scale, rope_base=w.rope_base)
+                          t["U_V"], t["q_pos"], scale=w.scale, rope_base=w.rope_base, workspace=ws)
 
 
 @pytest.mark.parametrize("w", [
@@ -56,8 +64,28 @@ def test_noalloc_matches_workspace_entry_on_two_calls(w):
         got = torch.full((w.B, w.Hq, w.d), float("nan"), dtype=torch.float32, device="cuda")
         assert _noalloc_call(lib, sh, t, got) == 0
         torch.cuda.synchronize()
-        assert_close(got.double().cpu().numpy(), want.double().cpu().numpy(), w.dtype,
-                     f"noalloc call {layer + 1} vs slimkv_decode_attn")
+        assert torch.equal(got, want), f"noalloc call {layer + 1} differs from slimkv_decode_attn"
+        ref = run_oracle("latent", w_l, wl.layer_tensors(w_l, 0))
+        assert_close(got.double().cpu().numpy(), ref, w.dtype, f"noalloc call {layer + 1} vs oracle")
+
+
+def test_noalloc_small_call_after_large_call_reads_nothing_stale():
+    lib = bd.load()
+    torch.cuda.set_device(0)
+    big = wl.custom(B=8, Hq=32, Hkv=8, N_b=4000, W=700, rank=256, seed=11)
+    small = wl.custom(B=1, Hq=8, Hkv=2, N_b=130, W=20, rank=64, seed=12)
+    assert bd.workspace_bytes(_shape(big), bd.SLIMKV_LATENT) <= bd.NOALLOC_SCRATCH_BYTES
+    tb = to_dev(wl.layer_tensors(big, 0))
+    ob = torch.empty((big.B, big.Hq, big.d), dtype=torch.float32, device="cuda")
+    assert _noalloc_call(lib, _shape(big), tb, ob) == 0
+    ts = to_dev(wl.layer_tensors(small, 0))
+    got = torch.full((small.B, small.Hq, small.d), float("nan"), dtype=torch.float32, device="cuda")
+    assert _noalloc_call(lib, _shape(small), ts, got) == 0
+    want = _with_workspace(small, ts, nan_fill=True)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+    assert_close(got.double().cpu().numpy(), run_oracle("latent", small, wl.layer_tensors(small, 0)), "bf16",
+                 "small noalloc call after a large one vs oracle")
 
 
 def test_noalloc_rejects_oversized_shape_without_launch():
