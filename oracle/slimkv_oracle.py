@@ -115,6 +115,51 @@ def decode_attn(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, scale, rope_base,
     return (out, weights) if return_weights else out
 
 
+def window_positions(W: int, q_pos: int) -> np.ndarray:
+    """Absolute positions of the W raw-window slots for a query at q_pos. The window is
+    the ring of the decode loop (token p in slot p mod W, the current token appended
+    before the decode), so slot s holds the latest position congruent to s mod W that
+    does not exceed q_pos: q_pos - ((q_pos - s) mod W)."""
+    s = np.arange(W)
+    return (q_pos - np.mod(q_pos - s, W)).astype(np.float64)
+
+
+def decode_attn_alibi(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, scale, rope_base, slopes, ratio,
+                      pairs=None):
+    """The reconstruction-free decode with an ALiBi bias added after the QK product
+    ("Latent-space attention removes the rebuild step" claims the latent scores stay
+    compatible with ALiBi because the bias enters after QK). Head h adds
+    slopes[h] * (key position - q_pos) to every score: beacon j sits at
+    ``beacon_positions(N_b, ratio)[j]``, window slot s at ``window_positions``. The
+    rest is ``decode_attn``: RoPE on the query and the raw keys, latent beacon scores
+    (RoPE(q) U_K^(g)) C_K^T, one softmax, (A C_V) U_V^(g)T + A V_raw."""
+    B, Hq, d = q.shape
+    Hkv = U_K.shape[0] // d if U_K is not None else K_raw.shape[2]
+    G = _groups(Hq, Hkv)
+    N_b = 0 if C_K is None else C_K.shape[1]
+    W = 0 if K_raw is None else K_raw.shape[1]
+    out = np.zeros((B, Hq, d))
+    for b, h in _pairs(B, Hq, pairs):
+        g = h // G
+        p = float(q_pos[b])
+        qr = rope(q[b, h], p, rope_base)
+        parts = []
+        if N_b:
+            qt = qr @ U_K[g * d:(g + 1) * d, :]
+            parts.append(scale * (C_K[b] @ qt) + slopes[h] * (beacon_positions(N_b, ratio) - p))
+        if W:
+            parts.append(scale * (K_raw[b, :, g, :] @ qr) + slopes[h] * (window_positions(W, int(q_pos[b])) - p))
+        s = np.concatenate(parts)
+        w, l, _ = softmax_weights(s)
+        o = np.zeros(d)
+        if N_b:
+            o = o + (w[:N_b] @ C_V[b]) @ U_V[g * d:(g + 1) * d, :].T
+        if W:
+            o = o + w[N_b:] @ V_raw[b, :, g, :]
+        out[b, h] = o / l
+    return out
+
+
 def reconstruct_kv(C, U, Hkv: int, d: int):
     """Explicit reconstruction C . U^T reshaped to [B, N_b, Hkv, d] (no RoPE)."""
     B, N_b, _ = C.shape

@@ -458,3 +458,87 @@ def test_pins_catch_wrong_beacon_position(monkeypatch):
     monkeypatch.setattr(O, "beacon_positions", lambda N_b, ratio: np.arange(N_b, dtype=np.float64) * ratio)
     got = O.decode_attn_reconstruct_rope(**c)
     assert not np.allclose(got, _recon_rope_relative(c), rtol=1e-6, atol=1e-6)
+
+
+# ---------------------------------------------------------------- ALiBi latent path
+#
+# "Latent-space attention removes the rebuild step": the bias enters after QK, so it
+# applies to the latent beacon scores unchanged. Readings: beacon j at position
+# j*ratio + ratio - 1; window slot s holds the latest position = s mod W not above q_pos.
+
+def _alibi_case(rng, B=2, Hq=4, Hkv=2, d=8, N_b=6, W=5, r=4, ratio=3):
+    return dict(q=_rand(rng, B, Hq, d), C_K=_rand(rng, B, N_b, r), C_V=_rand(rng, B, N_b, r),
+                K_raw=_rand(rng, B, W, Hkv, d), V_raw=_rand(rng, B, W, Hkv, d), U_K=_ortho(rng, Hkv * d, r),
+                U_V=_ortho(rng, Hkv * d, r), q_pos=np.array([23, 41])[:B], scale=1 / math.sqrt(d),
+                rope_base=10000.0, slopes=np.array([0.5, 0.25, 0.125, 0.0625])[:Hq], ratio=ratio)
+
+
+def _ring_positions(W, q_pos):
+    """Window slot contents after appending tokens 0 .. q_pos one by one to a ring of W."""
+    slots = [None] * W
+    for p in range(q_pos + 1):
+        slots[p % W] = p
+    return np.array(slots, dtype=np.float64)
+
+
+def test_window_positions_match_a_simulated_ring():
+    for W, qp in [(5, 23), (4, 8), (7, 7), (3, 100)]:
+        assert oracle.window_positions(W, qp).tolist() == _ring_positions(W, qp).tolist()
+
+
+def test_alibi_with_zero_slopes_is_the_plain_decode():
+    rng = np.random.default_rng(41)
+    c = _alibi_case(rng)
+    c["slopes"] = np.zeros(4)
+    got = oracle.decode_attn_alibi(**c)
+    c.pop("slopes"), c.pop("ratio")
+    assert np.allclose(got, oracle.decode_attn(**c), rtol=1e-13, atol=1e-13)
+
+
+def test_alibi_equals_explicit_reconstruction_with_bias():
+    # beacon keys expanded to full dimension (no RoPE), biases from a simulated ring
+    rng = np.random.default_rng(42)
+    c = _alibi_case(rng)
+    q, C_K, C_V, K_raw, V_raw, U_K, U_V = (c[k] for k in ("q", "C_K", "C_V", "K_raw", "V_raw", "U_K", "U_V"))
+    B, Hq, d = q.shape
+    Hkv, N_b, W = K_raw.shape[2], C_K.shape[1], K_raw.shape[1]
+    G = Hq // Hkv
+    Kb = np.einsum("bjr,nr->bjn", C_K, U_K).reshape(B, N_b, Hkv, d)
+    Vb = np.einsum("bjr,nr->bjn", C_V, U_V).reshape(B, N_b, Hkv, d)
+    want = np.zeros((B, Hq, d))
+    for b in range(B):
+        p = int(c["q_pos"][b])
+        pos = np.concatenate([np.array([j * c["ratio"] + c["ratio"] - 1 for j in range(N_b)], float),
+                              _ring_positions(W, p)])
+        for h in range(Hq):
+            g = h // G
+            qr = _rope_complex(q[b, h], p, c["rope_base"])
+            keys = np.concatenate([Kb[b, :, g], K_raw[b, :, g]])
+            vals = np.concatenate([Vb[b, :, g], V_raw[b, :, g]])
+            s = c["scale"] * keys @ qr + c["slopes"][h] * (pos - p)
+            e = np.exp(s - s.max())
+            want[b, h] = e @ vals / e.sum()
+    assert np.allclose(oracle.decode_attn_alibi(**c), want, rtol=1e-12, atol=1e-12)
+
+
+def test_alibi_steep_slope_selects_the_newest_window_token():
+    rng = np.random.default_rng(43)
+    c = _alibi_case(rng)
+    c["slopes"] = np.full(4, 200.0)
+    out = oracle.decode_attn_alibi(**c)
+    G = 2
+    for b in range(2):
+        slot = int(c["q_pos"][b]) % c["K_raw"].shape[1]
+        for h in range(4):
+            assert np.allclose(out[b, h], c["V_raw"][b, slot, h // G], atol=1e-9)
+
+
+def test_pins_catch_flipped_alibi_sign(monkeypatch):
+    rng = np.random.default_rng(44)
+    c = _alibi_case(rng)
+    c["slopes"] = np.full(4, 200.0)
+    orig = O.window_positions
+    monkeypatch.setattr(O, "window_positions", lambda W, qp: 2.0 * qp - orig(W, qp))
+    out = O.decode_attn_alibi(**c)
+    slot = int(c["q_pos"][0]) % c["K_raw"].shape[1]
+    assert not np.allclose(out[0, 0], c["V_raw"][0, slot, 0], atol=1e-6)
