@@ -136,6 +136,26 @@ slimkv_status slimkv_decode_attn_reconstruct(const slimkv_shape* shape, const vo
                                              const int32_t* q_pos, float* out,
                                              void* workspace, size_t ws_bytes, void* stream);
 
+/* slimkv_decode_attn with an ALiBi bias ("Latent-space attention removes the rebuild
+ * step" and "Where SlimKV fits and where it does not": the bias is added after the QK
+ * product, so the latent beacon scores take it unchanged). Every score of head h,
+ * beacon or window, gains slopes[h] * (key position - q_pos[b]) before the softmax.
+ * The pages give no key positions for beacons or the window; the positions taken are:
+ *   beacon j      j * beacon_ratio + beacon_ratio - 1 (the last token of its block)
+ *   window slot s q_pos[b] - ((q_pos[b] - s) mod W), the latest position congruent to s
+ *                 modulo W that does not exceed q_pos[b] (the ring of slimkv_append_kv,
+ *                 with the current token appended before the decode)
+ *   alibi_slopes  host array of Hq finite slopes (natural-log units of the scores),
+ *                 read during the call (NULL: SLIMKV_ERR_NULL)
+ *   beacon_ratio  tokens per beacon (the compression ratio), >= 1
+ * RoPE is applied as in slimkv_decode_attn. Other arguments, workspace size
+ * (SLIMKV_LATENT) and requirements as slimkv_decode_attn. */
+slimkv_status slimkv_decode_attn_alibi(const slimkv_shape* shape, const void* q, const void* C_K,
+                                       const void* C_V, const void* K_raw, const void* V_raw,
+                                       const void* U_K, const void* U_V, const int32_t* q_pos,
+                                       const float* alibi_slopes, int beacon_ratio, float* out,
+                                       void* workspace, size_t ws_bytes, void* stream);
+
 /* The reconstruction baseline as the SlimKV pages run it ("Speedups are real, but
  * memory is set by the ratio": the baseline keeps beacon key RoPE). As
  * slimkv_decode_attn_reconstruct, except that every materialised beacon key of every

@@ -25,7 +25,7 @@ STATUS = {0: "SLIMKV_OK", 1: "SLIMKV_ERR_NULL", 2: "SLIMKV_ERR_SHAPE", 3: "SLIMK
 NOALLOC_SCRATCH_BYTES = 64 << 20   # SLIMKV_NOALLOC_SCRATCH_BYTES
 
 # every symbol include/slimkv.h declares
-EXPORTS = ("slimkv_workspace_bytes", "slimkv_decode_attn", "slimkv_decode_attn_reconstruct",
+EXPORTS = ("slimkv_workspace_bytes", "slimkv_decode_attn", "slimkv_decode_attn_alibi", "slimkv_decode_attn_reconstruct",
            "slimkv_decode_attn_reconstruct_rope", "slimkv_decode_attn_full_kv", "slimkv_status_str", "slimkv_abi_version",
            "slimkv_kernel_path", "slimkv_force_simt", "slimkv_time_next_decode",
            "slimkv_decode_attn_noalloc", "slimkv_append_kv")
@@ -64,6 +64,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.slimkv_decode_attn.restype = ctypes.c_int
     lib.slimkv_decode_attn_reconstruct.argtypes = [sp] + [vp] * 7 + [i32p, vp, vp, sz, vp]
     lib.slimkv_decode_attn_reconstruct.restype = ctypes.c_int
+    lib.slimkv_decode_attn_alibi.argtypes = [sp] + [vp] * 7 + [i32p, vp, ctypes.c_int, vp, vp, sz, vp]
+    lib.slimkv_decode_attn_alibi.restype = ctypes.c_int
     lib.slimkv_decode_attn_reconstruct_rope.argtypes = [sp] + [vp] * 7 + [i32p, ctypes.c_int, vp, vp, sz, vp]
     lib.slimkv_decode_attn_reconstruct_rope.restype = ctypes.c_int
     lib.slimkv_decode_attn_full_kv.argtypes = [sp, vp, vp, vp, i32p, vp, vp, sz, vp]
@@ -209,6 +211,42 @@ def decode_attn_reconstruct(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, *, scale
                                             _ptr(q_pos), _ptr(out), _ptr(ws), ws.numel(),
                                             _stream(stream))
     _check(st, "slimkv_decode_attn_reconstruct")
+    return out
+
+
+def alibi_slopes(n_heads: int):
+    """The usual ALiBi slopes for n_heads heads: 2^(-8 i / n) for i = 1 .. n when n is a
+    power of two; otherwise those of the largest power of two m < n, followed by every
+    other slope of 2m heads (the first n - m of them)."""
+    def pow2(n):
+        return [2.0 ** (-8.0 * (i + 1) / n) for i in range(n)]
+    m = 1 << (n_heads.bit_length() - 1)
+    if m == n_heads:
+        return pow2(n_heads)
+    return pow2(m) + pow2(2 * m)[0::2][: n_heads - m]
+
+
+def decode_attn_alibi(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, slopes, beacon_ratio, *, scale=None,
+                      rope_base=10000.0, out=None, workspace: Optional[Workspace] = None, stream=None):
+    """slimkv_decode_attn_alibi on torch CUDA tensors; `slopes` is a sequence of Hq floats."""
+    lib = load()
+    B, Hq, d = q.shape
+    N_b = C_K.shape[1] if C_K is not None else 0
+    W = K_raw.shape[1] if K_raw is not None else 0
+    Hkv = U_K.shape[0] // d if U_K is not None else K_raw.shape[2]
+    r_k = C_K.shape[2] if C_K is not None else 0
+    r_v = C_V.shape[2] if C_V is not None else 0
+    sh, nb = _shape_and_bytes(SLIMKV_LATENT, B, Hq, Hkv, d, N_b, r_k, r_v, W, q.dtype, scale, rope_base)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    if nb == 0:
+        _check(2, "slimkv_decode_attn_alibi")
+    sl = (ctypes.c_float * Hq)(*[float(x) for x in slopes])
+    ws = (workspace or Workspace(q.device)).get(nb)
+    st = lib.slimkv_decode_attn_alibi(ctypes.byref(sh), _ptr(q), _ptr(C_K), _ptr(C_V), _ptr(K_raw), _ptr(V_raw),
+                                      _ptr(U_K), _ptr(U_V), _ptr(q_pos), ctypes.cast(sl, ctypes.c_void_p),
+                                      int(beacon_ratio), _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "slimkv_decode_attn_alibi")
     return out
 
 

@@ -302,6 +302,12 @@ __global__ void __launch_bounds__(128) simt_decode_kernel(SimtDecodeArgs a) {
             float dot = 0.f;
             for (int i = 0; i < Dk; ++i) dot = fmaf(q_s[i], to_f(kr[i]), dot);
             s = dot;   // the query carries scale * log2(e)
+            if (a.alibi) {
+                const long long qp = a.q_pos[b];
+                const long long dk = kind == 0 ? (long long)j * a.ratio + a.ratio - 1 - qp
+                                               : -((((qp - j) % n_rows) + n_rows) % n_rows);
+                s = fmaf(a.slope_l2[h], (float)dk, s);
+            }
         }
         float cm = warp_max(s);
         if (lane == 0) red[warp] = cm;

@@ -122,7 +122,8 @@ struct Ptrs {
     float* out;
     void* ws;
     size_t ws_bytes;
-    int beacon_ratio;   // reconstruction baseline with beacon-key RoPE (0: without)
+    int beacon_ratio;   // reconstruction baseline with beacon-key RoPE (0: without); ALiBi beacon spacing
+    const float* alibi_slopes = nullptr;   // host [Hq]: ALiBi slopes of slimkv_decode_attn_alibi (NULL: none)
 };
 
 slimkv_status check_ptrs(const slimkv_shape* s, int which, const Ptrs& p) {
@@ -171,6 +172,12 @@ slimkv_status run_simt(const slimkv_shape* s, int which, const Ptrs& p, cudaStre
     a.ml = reinterpret_cast<float*>(ws + L.ml);
     a.kind = reinterpret_cast<int*>(ws + L.kind);
     a.Dmax = L.Dmax;
+    if (p.alibi_slopes != nullptr) {
+        a.alibi = 1;
+        a.ratio = p.beacon_ratio;
+        a.q_pos = p.q_pos;
+        for (int h = 0; h < s->Hq; ++h) a.slope_l2[h] = p.alibi_slopes[h] * kLog2e;
+    }
     if (which == SLIMKV_RECONSTRUCT) {
         T* kb = reinterpret_cast<T*>(ws + L.kb);
         T* vb = reinterpret_cast<T*>(ws + L.vb);
@@ -273,6 +280,7 @@ slimkv_status run(const slimkv_shape* s, int which, const Ptrs& p, void* stream)
         c.slots = L.slots;
         c.Dmax = L.Dmax;
         c.beacon_ratio = p.beacon_ratio;
+        c.alibi_slopes = p.alibi_slopes;
         return tc_run(c, cs) == cudaSuccess ? SLIMKV_OK : SLIMKV_ERR_CUDA;
     }
     if (s->dtype == SLIMKV_F32) return run_simt<float>(s, which, p, cs);
@@ -315,6 +323,20 @@ slimkv_status slimkv_decode_attn_reconstruct_rope(const slimkv_shape* shape, con
     if (beacon_ratio < 1) return SLIMKV_ERR_SHAPE;
     Ptrs p{q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, out, workspace, ws_bytes, beacon_ratio};
     return run(shape, SLIMKV_RECONSTRUCT, p, stream);
+}
+
+slimkv_status slimkv_decode_attn_alibi(const slimkv_shape* shape, const void* q, const void* C_K,
+                                       const void* C_V, const void* K_raw, const void* V_raw,
+                                       const void* U_K, const void* U_V, const int32_t* q_pos,
+                                       const float* alibi_slopes, int beacon_ratio, float* out,
+                                       void* workspace, size_t ws_bytes, void* stream) {
+    if (alibi_slopes == nullptr) return SLIMKV_ERR_NULL;
+    if (beacon_ratio < 1) return SLIMKV_ERR_SHAPE;
+    if (shape != nullptr && shape->Hq >= 1 && shape->Hq <= kMaxHq)
+        for (int h = 0; h < shape->Hq; ++h)
+            if (!isfinite(alibi_slopes[h])) return SLIMKV_ERR_SHAPE;
+    Ptrs p{q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, out, workspace, ws_bytes, beacon_ratio, alibi_slopes};
+    return run(shape, SLIMKV_LATENT, p, stream);
 }
 
 slimkv_status slimkv_decode_attn_full_kv(const slimkv_shape* shape, const void* q, const void* K,

@@ -77,6 +77,12 @@ struct SimtDecodeArgs {
     int Dmax;
     int rpi_L, rpi_R;            // rows (beacons / tokens) per item
     int nit_L, nit_R0, nit_R1;   // items per batch element
+    // ALiBi (alibi != 0): head h adds slope_l2[h] * (key position - q_pos[b]) to its scores
+    // (log2 units); beacon j sits at j * ratio + ratio - 1, window slot s (source 0) at the
+    // latest position = s mod W0 not above q_pos[b]
+    int alibi, ratio;
+    const int32_t* q_pos;
+    float slope_l2[kMaxHq];
 };
 
 // Arguments of the split-combine kernel (merges partials, applies U_V^(g)T).

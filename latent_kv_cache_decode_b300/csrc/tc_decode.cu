@@ -98,6 +98,12 @@ struct TcParams {
     int accstride;                    // TMEM columns of one accumulator buffer
     uint32_t off_q, off_p, off_bar, off_red;
     uint32_t tmem_cols;
+    // ALiBi (alibi != 0): head h adds slope_l2[h] * (key position - q_pos[b]) to its scores
+    // (log2 units); beacon j sits at j * ratio + ratio - 1, window slot s at the latest
+    // position = s mod W not above q_pos[b]
+    int alibi, ratio;
+    const int32_t* q_pos;
+    float slope_l2[64];
     int u_begin[kMaxCtas + 1];        // CTA i owns units (tiles) [u_begin[i], u_begin[i+1])
     int slot_base[kMaxCtas];          // first partial slot of CTA i
 };
@@ -201,7 +207,20 @@ struct SoftCtx {
     uint32_t t_S, t_accp, lane_off;   // t_accp: accumulator of the current piece
     int tid, wq, lane, myrow, nMB;
     int aw;               // TMEM columns per 128 value rows of the accumulator
+    const float* slope_s; // [NS] ALiBi slopes of the piece's score columns (log2 units)
+    int alibi;
 };
+
+// ALiBi offsets of this thread's rows in a tile (key position - query position, one per
+// 128-row block); zero when ALiBi is off.
+struct RowBias {
+    float d[2];
+};
+// Add the ALiBi bias of 16 score columns (slopes at `sl`) for key offset `dk`.
+__device__ __forceinline__ void add_bias(float (&x)[16], const float* sl, float dk) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = fmaf(sl[i], dk, x[i]);
+}
 
 
 // TMEM columns of one score buffer: hi and lo scores (2 x NS columns) for each of
@@ -261,7 +280,8 @@ __device__ __forceinline__ float warp_reduce16(float* v, int lane) {
 template <int NS, int NP, int RB, bool LO>
 __device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* alpha_s, uint64_t* vfree,
                                              volatile int* abort, uint32_t tS0, uint32_t t_acc_lane, int row0,
-                                             int rows, int j, int nMB, int aw, int tid, int lane, int wq) {
+                                             int rows, int j, int nMB, int aw, int tid, int lane, int wq,
+                                             const float* slope_s, int alibi, float dk0, float dk1) {
     // per-head maximum over this warp's valid rows, then over the four warps
     float x[NS];
 #pragma unroll
@@ -275,6 +295,7 @@ __device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* 
         for (int hc = 0; hc < NS / 16; ++hc) {
             float sc[16];
             load_scores<LO, NS>(tS + hc * 16, sc);
+            if (alibi) add_bias(sc, slope_s + hc * 16, rb == 0 ? dk0 : dk1);
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[hc * 16 + i] = valid ? fmaxf(x[hc * 16 + i], sc[i]) : x[hc * 16 + i];
         }
@@ -323,7 +344,7 @@ __device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* 
 // their columns, which are never written out, cost no branches.
 template <int NS, int NP, int RB, bool LO>
 __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, int rows, bool has_prev,
-                                             float (&l_part)[NP], float (&mref)[NP]) {
+                                             float (&l_part)[NP], float (&mref)[NP], const RowBias& rbias) {
     constexpr int SW = SBuf<NP>::W;
     const int jr = j % kR;
     ptx::mbar_wait(&c.bar.kfree[jr], ph_of(j), c.abort);   // S(j) complete
@@ -344,6 +365,7 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
             for (int hc = 0; hc < NS / 16; ++hc) {
                 float sc[16];
                 load_scores<LO, NS>(tS + hc * 16, sc);
+                if (c.alibi) add_bias(sc, c.slope_s + hc * 16, rbias.d[rb]);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) dm = fmaxf(dm, sc[i] - mref[hc * 16 + i]);
             }
@@ -357,7 +379,8 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
     }
     if (slow) {
         softmax_new_ref<NS, NP, RB, LO>(c.red, c.m_ref_s, c.alpha_s, c.bar.vfree, c.abort, tS0, c.t_accp + c.lane_off,
-                                        row0, rows, j, has_prev ? c.nMB : 0, c.aw, c.tid, c.lane, c.wq);
+                                        row0, rows, j, has_prev ? c.nMB : 0, c.aw, c.tid, c.lane, c.wq, c.slope_s,
+                                        c.alibi, rbias.d[0], rbias.d[RB - 1]);
 #pragma unroll
         for (int h = 0; h < NS; ++h) {
             mref[h] = c.m_ref_s[h];
@@ -380,6 +403,7 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
         for (int hc = 0; hc < NS / 16; ++hc) {
             float sc[16];
             load_scores<LO, NS>(tS + hc * 16, sc);
+            if (c.alibi) add_bias(sc, c.slope_s + hc * 16, rbias.d[rb]);
             uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -473,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
     volatile int* flag = reinterpret_cast<volatile int*>(alpha_s + NP);
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(alpha_s + NP) + 12;
     int* owner = reinterpret_cast<int*>(alpha_s + NP) + 16;    // [kMaxSlots] producer's slot owners
+    float* slope_s = reinterpret_cast<float*>(alpha_s + NP) + 32;   // [NP] ALiBi slopes of the piece's columns
 
     Bars bar;
     bar.kready = bars;
@@ -809,6 +834,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         c.m_ref_s = m_ref_s;
         c.alpha_s = alpha_s;
         c.flags = flag + 1;
+        c.slope_s = slope_s;
+        c.alibi = p.alibi;
         c.abort = abort_flag;
         c.tid = threadIdx.x - 64;            // 0..127
         c.wq = c.tid >> 5;                   // softmax warp 0..3
@@ -833,21 +860,41 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
             const int nvalid = lat ? p.Hq : G;
             c.nMB = (p.dv[k] + 127) >> 7;
             c.t_accp = t_acc + (uint32_t)((p.accbuf == 2 ? (piece & 1) : 0) * p.accstride);
-            if (c.tid < NP) m_ref_s[c.tid] = -INFINITY;
+            if (c.tid < NP) {
+                m_ref_s[c.tid] = -INFINITY;
+                // ALiBi slopes of the piece's score columns: every head (latent), or the
+                // heads of the piece's KV group (raw; padded columns get 0)
+                if (p.alibi)
+                    slope_s[c.tid] = lat ? (c.tid < p.Hq ? p.slope_l2[c.tid] : 0.f)
+                                         : (c.tid < G ? p.slope_l2[pc.g * G + c.tid] : 0.f);
+            }
 #pragma unroll
             for (int h = 0; h < NP; ++h) {
                 l_part[h] = 0.f;
                 mref[h] = -INFINITY;
             }
+            const long long qp = p.alibi ? (long long)p.q_pos[pc.b] : 0;
             ptx::named_bar(1, 128);
             int jl = it.j;
             #pragma unroll 1
             for (int n = 0; n < pc.n; ++n) {
                 const int t = it.t;
                 const int row0 = t * kTile * p.rb[k] + c.myrow;
+                // key position - query position of this thread's rows (beacon j at
+                // j * ratio + ratio - 1; window slot s at qp - ((qp - s) mod W))
+                RowBias rbias = {{0.f, 0.f}};
+                if (p.alibi) {
+#pragma unroll
+                    for (int rb = 0; rb < 2; ++rb) {
+                        const long long row = row0 + rb * 128;
+                        const long long W = p.rows[k];
+                        rbias.d[rb] = lat ? (float)(row * p.ratio + p.ratio - 1 - qp)
+                                          : -(float)((((qp - row) % W) + W) % W);
+                    }
+                }
                 jl = it.j;
-                if (lat) softmax_tile<NP, NP, 1, false>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref);
-                else softmax_tile<kNG, NP, kRBRaw, true>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref);
+                if (lat) softmax_tile<NP, NP, 1, false>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref, rbias);
+                else softmax_tile<kNG, NP, kRBRaw, true>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref, rbias);
                 it.next();
             }
             // ---- partial of (CTA, piece): reference max, row sum and accumulator
@@ -939,7 +986,7 @@ SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], con
     const int q_bytes = std::max(rows[0] > 0 ? s.NP * round_up(dk[0], 64) * 2 : 0, 2 * kNG * 128 * 2);
     const int p_bytes = 2 * std::max(s.NP, kNG * kRBRaw) * 256;   // two P buffers (bf16)
     const int nbars = 4 * kR + 5;
-    const int misc_bytes = (6 * s.NP + 32) * 4;
+    const int misc_bytes = (7 * s.NP + 32) * 4;
     const int avail = budget - q_bytes - p_bytes - round_up(nbars * 8, 16) - misc_bytes - 1024;
     s.nslot = std::min(kMaxSlots, avail / kSlot);
     // One tile part (keys or values) must fit the ring. The loads run in consumption
@@ -1230,6 +1277,13 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     prm.off_bar = sp.off_bar;
     prm.off_red = sp.off_red;
     prm.tmem_cols = sp.tmem_cols;
+    if (c.alibi_slopes != nullptr) {
+        // ALiBi biases enter in the kernel's log2 units
+        prm.alibi = 1;
+        prm.ratio = c.beacon_ratio;
+        prm.q_pos = c.q_pos;
+        for (int h = 0; h < c.Hq; ++h) prm.slope_l2[h] = c.alibi_slopes[h] * kLog2e;
+    }
     for (int i = 0; i <= w.n_ctas; ++i) prm.u_begin[i] = w.u_begin[i];
     for (int i = 0; i < w.n_ctas; ++i) prm.slot_base[i] = w.slot_base[i];
 

@@ -33,6 +33,7 @@ struct TcCall {
     int slots;
     int Dmax;
     int beacon_ratio;          // SLIMKV_RECONSTRUCT: > 0 rotates the beacon keys (RoPE at j*ratio + ratio - 1)
+    const float* alibi_slopes; // SLIMKV_LATENT: host array [Hq] of ALiBi slopes (NULL: no bias)
 };
 
 // Whether the tensor-core path handles these sizes (bf16 storage assumed).

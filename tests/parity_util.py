@@ -38,6 +38,11 @@ def run_gpu(which, w, t, out=None):
         o = bd.decode_attn_reconstruct(d["q"], d["C_K"], d["C_V"], d["K_raw"] if w.W else None,
                                        d["V_raw"] if w.W else None, d["U_K"], d["U_V"],
                                        d["q_pos"], **kw)
+    elif which == "alibi":
+        o = bd.decode_attn_alibi(d["q"], d["C_K"] if w.N_b else None, d["C_V"] if w.N_b else None,
+                                 d["K_raw"] if w.W else None, d["V_raw"] if w.W else None,
+                                 d["U_K"] if w.N_b else None, d["U_V"] if w.N_b else None,
+                                 d["q_pos"], bd.alibi_slopes(w.Hq), w.ratio, **kw)
     elif which == "reconstruct_rope":
         o = bd.decode_attn_reconstruct_rope(d["q"], d["C_K"], d["C_V"], d["K_raw"] if w.W else None,
                                             d["V_raw"] if w.W else None, d["U_K"], d["U_V"],
@@ -58,6 +63,11 @@ def run_oracle(which, w, t, pairs=None):
         return oracle.decode_attn_reconstruct(f["q"], f["C_K"], f["C_V"], f["K_raw"], f["V_raw"],
                                               f["U_K"], f["U_V"], f["q_pos"], w.scale, w.rope_base,
                                               pairs=pairs)
+    if which == "alibi":
+        return oracle.decode_attn_alibi(f["q"], f["C_K"] if w.N_b else None, f["C_V"] if w.N_b else None,
+                                        f["K_raw"] if w.W else None, f["V_raw"] if w.W else None,
+                                        f["U_K"], f["U_V"], f["q_pos"], w.scale, w.rope_base,
+                                        np.array(bd.alibi_slopes(w.Hq)), w.ratio, pairs=pairs)
     if which == "reconstruct_rope":
         return oracle.decode_attn_reconstruct_rope(f["q"], f["C_K"], f["C_V"], f["K_raw"], f["V_raw"],
                                                    f["U_K"], f["U_V"], f["q_pos"], w.scale, w.rope_base,

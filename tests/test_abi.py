@@ -188,3 +188,24 @@ def test_reconstruct_rope_host_checks(lib):
     nul[1] = None
     assert fn(ctypes.byref(s), *nul, 16, 8192, 1 << 20, need, None) == 1
     assert fn(ctypes.byref(_shape(N_b=0)), *good, 16, 8192, 1 << 20, 1 << 40, None) == 2
+
+
+def test_alibi_host_checks(lib):
+    # slopes are required and finite, the beacon ratio >= 1; nothing launches
+    s = _shape()
+    good = [256 * (i + 1) for i in range(7)] + [4096]
+    need = bd.workspace_bytes(s, bd.SLIMKV_LATENT)
+    fn = lib.slimkv_decode_attn_alibi
+    sl = (ctypes.c_float * s.Hq)(*([0.25] * s.Hq))
+    slp = ctypes.cast(sl, ctypes.c_void_p)
+    assert fn(ctypes.byref(s), *good, None, 16, 8192, 1 << 20, need, None) == 1
+    assert fn(ctypes.byref(s), *good, slp, 0, 8192, 1 << 20, need, None) == 2
+    bad = (ctypes.c_float * s.Hq)(*([0.25] * (s.Hq - 1) + [float("inf")]))
+    assert fn(ctypes.byref(s), *good, ctypes.cast(bad, ctypes.c_void_p), 16, 8192, 1 << 20, need, None) == 2
+    assert fn(ctypes.byref(s), *good, slp, 16, 8192, 1 << 20, need - 1, None) == 5
+
+
+def test_alibi_slopes_follow_the_geometric_rule():
+    assert bd.alibi_slopes(8) == [2.0 ** (-i) for i in range(1, 9)]
+    s12 = bd.alibi_slopes(12)
+    assert s12[:8] == bd.alibi_slopes(8) and s12[8:] == bd.alibi_slopes(16)[0::2][:4]

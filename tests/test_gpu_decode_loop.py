@@ -24,6 +24,9 @@ CASES = {
     # raw keys (1% of the window's tokens scaled x8 before RoPE), two batch elements
     "bf16-headline-peaked": dict(B=2, Hq=32, Hkv=8, d=128, N_b=512, W=256, rank=256, ratio=16,
                                  peak_frac=0.01, peak_scale=8.0),
+    # ALiBi through the ring wrap: the window positions follow the appends
+    "bf16-tc-alibi": dict(B=2, Hq=8, Hkv=2, d=128, N_b=256, W=64, rank=64, ratio=4),
+    "f32-simt-alibi": dict(dtype="f32", B=1, Hq=4, Hkv=1, d=64, N_b=64, W=32, rank=32, ratio=32),
 }
 
 
@@ -39,18 +42,28 @@ def test_decode_loop_matches_oracle(case):
     f = f64(t)
     Ko, Vo = f["K_raw"], f["V_raw"]
     lat = w.N_b > 0
+    alibi = case.endswith("-alibi")
+    slopes = bd.alibi_slopes(w.Hq)
     for s in range(steps):
         pos = st["pos"][s]
         pd = pos.cuda()
         bd.append_kv(st["k_new"][s].cuda(), st["v_new"][s].cuda(), K, V, pd, rope_base=w.rope_base)
-        got = bd.decode_attn(st["q"][s].cuda(), dev["C_K"] if lat else None, dev["C_V"] if lat else None,
-                             K, V, dev["U_K"] if lat else None, dev["U_V"] if lat else None, pd,
-                             scale=w.scale, rope_base=w.rope_base)
+        if alibi:
+            got = bd.decode_attn_alibi(st["q"][s].cuda(), dev["C_K"], dev["C_V"], K, V, dev["U_K"], dev["U_V"], pd,
+                                       slopes, w.ratio, scale=w.scale, rope_base=w.rope_base)
+        else:
+            got = bd.decode_attn(st["q"][s].cuda(), dev["C_K"] if lat else None, dev["C_V"] if lat else None,
+                                 K, V, dev["U_K"] if lat else None, dev["U_V"] if lat else None, pd,
+                                 scale=w.scale, rope_base=w.rope_base)
         torch.cuda.synchronize()
         Ko, Vo = oracle.append_kv(Ko, Vo, wl.as_f64(st["k_new"][s]), wl.as_f64(st["v_new"][s]), pos.numpy(),
                                   w.rope_base, storage=w.dtype)
-        ref = oracle.decode_attn(wl.as_f64(st["q"][s]), f["C_K"] if lat else None, f["C_V"] if lat else None,
-                                 Ko, Vo, f["U_K"], f["U_V"], pos.numpy(), w.scale, w.rope_base)
+        if alibi:
+            ref = oracle.decode_attn_alibi(wl.as_f64(st["q"][s]), f["C_K"], f["C_V"], Ko, Vo, f["U_K"], f["U_V"],
+                                           pos.numpy(), w.scale, w.rope_base, np.array(slopes), w.ratio)
+        else:
+            ref = oracle.decode_attn(wl.as_f64(st["q"][s]), f["C_K"] if lat else None, f["C_V"] if lat else None,
+                                     Ko, Vo, f["U_K"], f["U_V"], pos.numpy(), w.scale, w.rope_base)
         assert_close(got.cpu().double().numpy(), ref, w.dtype, f"{case} step {s}")
     # the window after the loop: values copied exactly, keys rotated in float32
     # then rounded to the storage type (the oracle rotates in float64)

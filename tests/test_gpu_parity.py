@@ -190,3 +190,20 @@ def test_config1_reconstruct_rope_one_layer():
     t = wl.layer_tensors(w, 1)
     assert_close(run_gpu("reconstruct_rope", w, t), run_oracle("reconstruct_rope", w, t), "bf16",
                  "config1 reconstruct-rope")
+
+
+# ALiBi on the reconstruction-free decode (tensor-core path for bf16 / d = 128, SIMT path
+# for float32 storage or d = 64), with the slopes of bd.alibi_slopes.
+@pytest.mark.parametrize("case", [
+    ("config0-f32", None),
+    ("bf16-tc", dict(B=2, Hq=8, Hkv=2, d=128, N_b=256, W=64, rank=64, ratio=4)),
+    ("bf16-headline-shape", dict(B=2, Hq=32, Hkv=8, d=128, N_b=512, W=256, rank=256, ratio=16)),
+    ("bf16-window-only", dict(B=1, Hq=8, Hkv=2, d=128, N_b=0, W=300, rank=64, ratio=4)),
+    ("bf16-beacons-only", dict(B=1, Hq=8, Hkv=2, d=128, N_b=300, W=0, rank=64, ratio=8)),
+    ("bf16-simt-d64", dict(B=2, Hq=4, Hkv=1, d=64, N_b=96, W=32, rank=64, ratio=8)),
+])
+def test_alibi_matches_oracle(case):
+    name, kw = case
+    w = wl.config(0) if kw is None else wl.custom(**kw)
+    t = wl.layer_tensors(w, 0)
+    assert_close(run_gpu("alibi", w, t), run_oracle("alibi", w, t), w.dtype, f"alibi {name}")
