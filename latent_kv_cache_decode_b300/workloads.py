@@ -34,7 +34,7 @@ import torch
 # tensor ids used as part of the per-tensor seed
 _TID = {"U_K": 0, "U_V": 1, "C_K": 2, "C_V": 3, "K_raw": 4, "V_raw": 5, "q": 6,
         "peaks": 7, "ranks": 8, "K_full": 9, "V_full": 10, "k_new": 11, "v_new": 12,
-        "q_step": 13}
+        "q_step": 13, "q_chunk": 14, "K_chunk": 15, "V_chunk": 16, "chunk_peaks": 17}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -211,6 +211,32 @@ def decode_steps(w: Workload, layer: int, steps: int,
     pos = w.q_pos + np.arange(steps, dtype=np.int64)[:, None] + np.zeros((1, len(bs)), dtype=np.int64)
     return {"k_new": _store(kn, w), "v_new": _store(vn, w), "q": _store(qq, w),
             "pos": torch.from_numpy(pos.astype(np.int32))}
+
+
+def prefill_chunk(w: Workload, layer: int, T: int,
+                  batch: Optional[List[int]] = None) -> Dict[str, torch.Tensor]:
+    """CPU tensors (storage dtype) for one prefill chunk of T tokens of one layer.
+
+    Keys: q [B,T,Hq,d] (before RoPE), K_chunk, V_chunk [B,T,Hkv,d] (keys stored after
+    RoPE, drawn directly as N(0,1) like the window keys) and p0 [B] int32, the position
+    of chunk token 0. The chunk follows the tokens the beacons fold: p0 = N_b * ratio.
+    With ``peak_frac`` set, that fraction of the chunk's tokens have their keys scaled
+    by ``peak_scale`` on every KV head, as in the raw window."""
+    bs = list(range(w.B)) if batch is None else list(batch)
+    s = w.seed
+    qq, kc, vc = [], [], []
+    for b in bs:
+        qq.append(_normal(_rng(s, layer, b, _TID["q_chunk"]), (T, w.Hq, w.d)))
+        k = _normal(_rng(s, layer, b, _TID["K_chunk"]), (T, w.Hkv, w.d))
+        if w.peak_frac > 0 and T > 0:
+            n_peak = int(round(w.peak_frac * T))
+            idx = _rng(s, layer, b, _TID["chunk_peaks"]).choice(T, size=n_peak, replace=False)
+            k[idx] *= np.float32(w.peak_scale)
+        kc.append(k)
+        vc.append(_normal(_rng(s, layer, b, _TID["V_chunk"]), (T, w.Hkv, w.d)))
+    return {"q": _store(np.stack(qq), w), "K_chunk": _store(np.stack(kc), w),
+            "V_chunk": _store(np.stack(vc), w),
+            "p0": torch.full((len(bs),), w.N_b * w.ratio, dtype=torch.int32)}
 
 
 def as_f64(t: torch.Tensor) -> np.ndarray:

@@ -268,3 +268,59 @@ def append_kv(K_raw, V_raw, k_new, v_new, pos, rope_base, storage: str = "bf16")
         K[b, slot] = rnd(rope(np.asarray(k_new[b], np.float64), float(pos[b]), rope_base))
         V[b, slot] = rnd(np.asarray(v_new[b], np.float64))
     return K, V
+
+
+# ---------------------------------------------------------------------------
+# Prefill: a chunk of new tokens attending to the beacons and, causally, to itself.
+#
+# "Speedups are real, but memory is set by the ratio" reports time-to-first-token
+# gains over the reconstruction variant from skipping key-side RoPE and full-key
+# materialisation for beacon states, i.e. the prompt's chunks are processed against
+# the latent beacon memory by the same rule as a decode query. Reading taken here
+# (the pages give no chunked-prefill formula): every query token t of a chunk of T
+# tokens, at position p0 + t, sees every beacon of the memory (latent scores, no
+# key-side RoPE) and the chunk's own tokens s <= t (keys stored after RoPE at
+# p0 + s), all in one softmax. This is the decode rule with the raw window replaced
+# by the causal prefix of the chunk.
+# ---------------------------------------------------------------------------
+
+def _triples(B, T, Hq, triples):
+    if triples is None:
+        return [(b, t, h) for b in range(B) for t in range(T) for h in range(Hq)]
+    return list(triples)
+
+
+def prefill_attn(q, C_K, C_V, K_chunk, V_chunk, U_K, U_V, p0, scale, rope_base, triples=None):
+    """Chunked-prefill attention of one layer over the beacon memory and the chunk.
+
+    q [B,T,Hq,d] (the chunk's queries, before RoPE); C_K [B,N_b,r_k]; C_V [B,N_b,r_v];
+    K_chunk, V_chunk [B,T,Hkv,d] (the chunk's keys stored after RoPE at p0 + s, and its
+    values); U_K [Hkv*d,r_k]; U_V [Hkv*d,r_v]; p0 [B] the position of chunk token 0.
+    Returns out [B,T,Hq,d] (entries not in ``triples`` stay zero). For every (b, t, h),
+    with g the KV group of h and p = p0[b] + t:
+      qr = RoPE(q[b,t,h], p);  qt = qr . U_K^(g)
+      s  = [scale * C_K[b] qt ; scale * K_chunk[b, 0..t, g] qr]
+      A  = softmax(s)
+      out = (A_beacon . C_V[b]) . U_V^(g)T + A_chunk . V_chunk[b, 0..t, g]
+    """
+    B, T, Hq, d = q.shape
+    Hkv = U_K.shape[0] // d if U_K is not None else K_chunk.shape[2]
+    G = _groups(Hq, Hkv)
+    N_b = 0 if C_K is None else C_K.shape[1]
+    out = np.zeros((B, T, Hq, d))
+    for b, t, h in _triples(B, T, Hq, triples):
+        g = h // G
+        qr = rope(q[b, t, h], float(p0[b]) + t, rope_base)
+        parts = []
+        if N_b:
+            qt = qr @ U_K[g * d:(g + 1) * d, :]
+            parts.append(scale * (C_K[b] @ qt))
+        parts.append(scale * (K_chunk[b, :t + 1, g, :] @ qr))   # causal: s <= t
+        s = np.concatenate(parts)
+        w, l, _ = softmax_weights(s)
+        o = np.zeros(d)
+        if N_b:
+            o = o + (w[:N_b] @ C_V[b]) @ U_V[g * d:(g + 1) * d, :].T
+        o = o + w[N_b:] @ V_chunk[b, :t + 1, g, :]
+        out[b, t, h] = o / l
+    return out

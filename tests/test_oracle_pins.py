@@ -542,3 +542,164 @@ def test_pins_catch_flipped_alibi_sign(monkeypatch):
     out = O.decode_attn_alibi(**c)
     slot = int(c["q_pos"][0]) % c["K_raw"].shape[1]
     assert not np.allclose(out[0, 0], c["V_raw"][0, slot, 0], atol=1e-6)
+
+
+# ------------------------------------------------------ prefill over chunk + beacons
+
+def _prefill_case(rng, B=2, T=7, Hq=4, Hkv=2, d=8, N_b=5, r_k=4, r_v=6):
+    return dict(q=_rand(rng, B, T, Hq, d), C_K=_rand(rng, B, N_b, r_k), C_V=_rand(rng, B, N_b, r_v),
+                K_chunk=_rand(rng, B, T, Hkv, d), V_chunk=_rand(rng, B, T, Hkv, d),
+                U_K=_ortho(rng, Hkv * d, r_k), U_V=_ortho(rng, Hkv * d, r_v),
+                p0=np.array([64, 1000])[:B], scale=1 / math.sqrt(d), rope_base=10000.0)
+
+
+def _causal_sdpa(qr, K, V, scale, prefix=None):
+    """torch fp64 SDPA, causal over the chunk; qr [B,T,Hq,d] (rotated), K/V [B,T,Hq,d].
+    With ``prefix`` (K_b, V_b [B,N,Hq,d]) every query also sees those N keys."""
+    qt = torch.from_numpy(qr).permute(0, 2, 1, 3)                 # [B,Hq,T,d]
+    kt = torch.from_numpy(K).permute(0, 2, 1, 3)
+    vt = torch.from_numpy(V).permute(0, 2, 1, 3)
+    T = qr.shape[1]
+    mask = torch.ones(T, T, dtype=torch.bool).tril()
+    if prefix is not None:
+        kt = torch.cat([torch.from_numpy(prefix[0]).permute(0, 2, 1, 3), kt], dim=2)
+        vt = torch.cat([torch.from_numpy(prefix[1]).permute(0, 2, 1, 3), vt], dim=2)
+        mask = torch.cat([torch.ones(T, prefix[0].shape[1], dtype=torch.bool), mask], dim=1)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+    return o.permute(0, 2, 1, 3).numpy()
+
+
+def _rotate_chunk_queries(c):
+    B, T = c["q"].shape[:2]
+    return np.stack([np.stack([_rope_complex(c["q"][b, t], c["p0"][b] + t, c["rope_base"])
+                               for t in range(T)]) for b in range(B)])
+
+
+def test_prefill_without_beacons_is_causal_rope_attention():
+    rng = np.random.default_rng(50)
+    c = _prefill_case(rng, N_b=0)
+    c["C_K"] = c["C_V"] = None
+    out = oracle.prefill_attn(**c)
+    G = 2
+    ref = _causal_sdpa(_rotate_chunk_queries(c), _expand_heads(c["K_chunk"], G),
+                       _expand_heads(c["V_chunk"], G), c["scale"])
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_prefill_latent_equals_explicit_reconstruction_with_causal_mask():
+    # associativity again: the beacons are plain (unrotated) keys C_K U_K^T and values
+    # C_V U_V^T that every chunk query sees; the chunk is causal
+    rng = np.random.default_rng(51)
+    c = _prefill_case(rng, T=9, N_b=6)
+    d, Hkv = 8, 2
+    out = oracle.prefill_attn(**c)
+    Kb = (c["C_K"] @ c["U_K"].T).reshape(2, 6, Hkv, d)
+    Vb = (c["C_V"] @ c["U_V"].T).reshape(2, 6, Hkv, d)
+    ref = _causal_sdpa(_rotate_chunk_queries(c), _expand_heads(c["K_chunk"], 2),
+                       _expand_heads(c["V_chunk"], 2), c["scale"],
+                       prefix=(_expand_heads(Kb, 2), _expand_heads(Vb, 2)))
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_prefill_is_causal():
+    rng = np.random.default_rng(52)
+    c = _prefill_case(rng, T=8)
+    base = oracle.prefill_attn(**c)
+    t_cut = 4
+    c2 = dict(c)
+    c2["K_chunk"] = c["K_chunk"].copy()
+    c2["V_chunk"] = c["V_chunk"].copy()
+    c2["K_chunk"][:, t_cut:] += 3.0
+    c2["V_chunk"][:, t_cut:] -= 5.0
+    out = oracle.prefill_attn(**c2)
+    np.testing.assert_array_equal(out[:, :t_cut], base[:, :t_cut])     # the past never sees the future
+    assert not np.allclose(out[:, t_cut:], base[:, t_cut:])
+
+
+def test_prefill_first_token_sees_beacons_and_itself():
+    # token 0 of the chunk: one raw key (its own); with a dominant self-score its output
+    # is its own value, with the beacons' scores pushed far down
+    rng = np.random.default_rng(53)
+    c = _prefill_case(rng, T=3)
+    qr0 = np.stack([_rope_complex(c["q"][b, 0], c["p0"][b], c["rope_base"]) for b in range(2)])
+    for b in range(2):
+        for g in range(2):
+            c["K_chunk"][b, 0, g] = 400.0 * qr0[b, 2 * g] / np.linalg.norm(qr0[b, 2 * g])
+    out = oracle.prefill_attn(**c, triples=[(0, 0, 0), (1, 0, 2)])
+    np.testing.assert_allclose(out[0, 0, 0], c["V_chunk"][0, 0, 0], atol=1e-9)
+    np.testing.assert_allclose(out[1, 0, 2], c["V_chunk"][1, 0, 1], atol=1e-9)
+
+
+def _brute_prefill(c):
+    """Scalar loops straight from the prefill rule, no numpy linear algebra."""
+    q, C_K, C_V, K, V, U_K, U_V = (c[k] for k in ("q", "C_K", "C_V", "K_chunk", "V_chunk", "U_K", "U_V"))
+    B, T, Hq, d = q.shape
+    N_b, r_k, r_v = C_K.shape[1], C_K.shape[2], C_V.shape[2]
+    G = Hq // K.shape[2]
+    out = np.zeros((B, T, Hq, d))
+    for b in range(B):
+        for t in range(T):
+            p = float(c["p0"][b] + t)
+            for h in range(Hq):
+                g = h // G
+                qr = [0.0] * d
+                for i in range(d // 2):
+                    a = p * c["rope_base"] ** (-2.0 * i / d)
+                    qr[i] = q[b, t, h, i] * math.cos(a) - q[b, t, h, i + d // 2] * math.sin(a)
+                    qr[i + d // 2] = q[b, t, h, i + d // 2] * math.cos(a) + q[b, t, h, i] * math.sin(a)
+                s = []
+                for j in range(N_b):
+                    acc = 0.0
+                    for k in range(r_k):
+                        acc += sum(qr[i] * U_K[g * d + i, k] for i in range(d)) * C_K[b, j, k]
+                    s.append(c["scale"] * acc)
+                for u in range(t + 1):
+                    s.append(c["scale"] * sum(qr[i] * K[b, u, g, i] for i in range(d)))
+                m = max(s)
+                e = [math.exp(x - m) for x in s]
+                l = sum(e)
+                for i in range(d):
+                    v = 0.0
+                    for j in range(N_b):
+                        v += e[j] * sum(C_V[b, j, k] * U_V[g * d + i, k] for k in range(r_v))
+                    for u in range(t + 1):
+                        v += e[N_b + u] * V[b, u, g, i]
+                    out[b, t, h, i] = v / l
+    return out
+
+
+def test_prefill_brute_force_scalar_loops():
+    rng = np.random.default_rng(54)
+    c = _prefill_case(rng, B=2, T=4, Hq=4, Hkv=2, d=4, N_b=3, r_k=3, r_v=2)
+    np.testing.assert_allclose(oracle.prefill_attn(**c), _brute_prefill(c), rtol=1e-12, atol=1e-13)
+
+
+def _mutated_prefill(old, new):
+    """A copy of the oracle's prefill with one planted change in its source."""
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(O.prefill_attn))
+    assert src.count(old) >= 1
+    ns = dict(vars(O))
+    exec(compile(src.replace(old, new), "<mutated prefill>", "exec"), ns)
+    return ns["prefill_attn"]
+
+
+@pytest.mark.parametrize("old,new", [
+    (":t + 1, g, :]", ":t, g, :]"),                         # token t does not see itself
+    (":t + 1, g, :]", ":t + 2, g, :]"),                     # one token of the future leaks in
+    ("float(p0[b]) + t", "float(p0[b])"),                   # every token rotated at p0
+])
+def test_pins_catch_prefill_mistakes(old, new):
+    rng = np.random.default_rng(55)
+    c = _prefill_case(rng, N_b=0, T=6)
+    c["C_K"] = c["C_V"] = None
+    ref = _causal_sdpa(_rotate_chunk_queries(c), _expand_heads(c["K_chunk"], 2),
+                       _expand_heads(c["V_chunk"], 2), c["scale"])
+    np.testing.assert_allclose(O.prefill_attn(**c), ref, rtol=1e-11, atol=1e-12)
+    bad = _mutated_prefill(old, new)
+    try:
+        out = bad(**c)
+    except ValueError:      # an empty score vector for t = 0 is caught too
+        return
+    assert not np.allclose(out, ref, atol=1e-6)
