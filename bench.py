@@ -273,6 +273,60 @@ def companion_measurements(args, w, layers, dev, peak):
     return base, cfgs
 
 
+def prefill_flops(w, layer: int, T: int) -> float:
+    """Algorithmic flops of one prefill chunk of T tokens for one layer, all batch
+    elements: latent scores and values (2 T Hq N_b (r_k + r_v)), the causal chunk
+    (scores and values over T (T + 1) / 2 pairs: 4 Hq d T (T + 1) / 2), and the query
+    and value projections (2 T Hq d (r_k + r_v))."""
+    r = w.r(layer)
+    per_b = (2 * T * w.Hq * w.N_b * 2 * r + 4 * w.Hq * w.d * T * (T + 1) / 2 + 2 * T * w.Hq * w.d * 2 * r)
+    return w.B * per_b
+
+
+def prefill_measurement(args, w, layers, dev, chunk: int = 1024):
+    """Prefill-side attention on the headline workload's layers: one chunk of `chunk`
+    tokens per batch element attends to the layer's 8192 beacons and, causally, to
+    itself (the chunk right after the beacons' span), timed as a CUDA graph of all
+    layers. Chunk queries, keys and values are seeded device draws, four distinct sets
+    cycled over the layers."""
+    import torch
+    from latent_kv_cache_decode_b300 import binding as bd
+    steps, warm = 3, 2
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 100)
+    sets = []
+    for _ in range(4):
+        q = torch.randn((w.B, chunk, w.Hq, w.d), generator=g, device=dev).to(torch.bfloat16)
+        k = torch.randn((w.B, chunk, w.Hkv, w.d), generator=g, device=dev).to(torch.bfloat16)
+        v = torch.randn((w.B, chunk, w.Hkv, w.d), generator=g, device=dev).to(torch.bfloat16)
+        sets.append((q, k, v))
+    p0 = torch.full((w.B,), w.N_b * w.ratio, dtype=torch.int32, device=dev)
+    out = torch.empty((w.B, chunk, w.Hq, w.d), dtype=torch.float32, device=dev)
+    ws = bd.Workspace(dev)
+    calls = [lambda st, l=l, t=t: bd.prefill_attn(sets[l % 4][0], t["C_K"], t["C_V"], sets[l % 4][1], sets[l % 4][2],
+                                                   t["U_K"], t["U_V"], p0, scale=w.scale, rope_base=w.rope_base,
+                                                   out=out, workspace=ws, stream=st)
+             for l, t in enumerate(layers)]
+    us = time_layer_graph(calls, dev, steps, warm)
+    fl = sum(prefill_flops(w, l, chunk) for l in range(len(layers)))
+    tf = fl / (us * 1e-6) / 1e12
+    peak_tf = None
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pp):
+        with open(pp) as f:
+            peak_tf = float(json.load(f)["bf16_tflops_sustained"])
+    del sets, out, ws
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "chunk_tokens": chunk, "beacons": w.N_b, "layers": len(layers),
+            "us_per_step": us, "us_per_layer": us / len(layers),
+            "tokens_per_s": w.B * chunk / (us * 1e-6),
+            "flops_per_step": fl, "tflops": tf,
+            "peak_tflops": peak_tf, "peak_kind": "measured bf16 sustained (cuBLAS, long loop)",
+            "frac": tf / peak_tf if peak_tf else None,
+            "how": "CUDA graph of all layers (staging kernel + tensor-core prefill kernel per layer), "
+                   "CUDA events over 3 replays after 2"}
+
+
 def run_reference(args):
     """CPU oracle arm: each step is one sampled layer, reported per full step."""
     w = _workload(args.config, args.layers)
@@ -543,6 +597,7 @@ def run_slimkv(args):
         res["decode_loop"] = loop
     if args.companions and world == 1 and mode == "latent" and args.config == 2:
         res["baselines"], res["configs"] = companion_measurements(args, w, layers, dev, peak)
+        res["prefill"] = prefill_measurement(args, w, layers, dev)
     if not args.no_cpu_baseline and world == 1:
         sample_layers = [0, w.layers // 2]
         secs = oracle_layer_seconds(w, sample_layers)

@@ -55,7 +55,7 @@ extern "C" {
 #endif
 
 /* 2: adds slimkv_append_kv (version 1 calls are unchanged) */
-#define SLIMKV_ABI_VERSION 3
+#define SLIMKV_ABI_VERSION 4
 
 typedef enum {
     SLIMKV_OK = 0,
@@ -90,8 +90,9 @@ typedef struct {
 } slimkv_shape;
 
 /* which: SLIMKV_LATENT for slimkv_decode_attn, SLIMKV_RECONSTRUCT for
- * slimkv_decode_attn_reconstruct, SLIMKV_FULL_KV for slimkv_decode_attn_full_kv. */
-enum { SLIMKV_LATENT = 0, SLIMKV_RECONSTRUCT = 1, SLIMKV_FULL_KV = 2 };
+ * slimkv_decode_attn_reconstruct, SLIMKV_FULL_KV for slimkv_decode_attn_full_kv,
+ * SLIMKV_PREFILL for slimkv_prefill_attn. */
+enum { SLIMKV_LATENT = 0, SLIMKV_RECONSTRUCT = 1, SLIMKV_FULL_KV = 2, SLIMKV_PREFILL = 3 };
 
 /* Bytes of device workspace the call `which` needs for `shape` (0 if the shape
  * is invalid). The workspace holds the rotated and latent queries, per-split
@@ -185,6 +186,30 @@ slimkv_status slimkv_decode_attn_full_kv(const slimkv_shape* shape, const void* 
                                          const void* K, const void* V,
                                          const int32_t* q_pos, float* out,
                                          void* workspace, size_t ws_bytes, void* stream);
+
+/* Prefill-side attention of one chunk of new tokens over the beacon memory and the
+ * chunk itself ("Can SlimKV compress KV cache jointly across tokens and features",
+ * section "Speedups are real, but memory is set by the ratio": time-to-first-token
+ * gains come from skipping key-side RoPE and full-key materialisation for beacon
+ * states). Query token t of the chunk sits at position p0[b] + t and sees every beacon
+ * (latent scores, as in slimkv_decode_attn) and the chunk's tokens 0..t, in one softmax:
+ *   s   = [scale*(RoPE(q[b,t,h]) . U_K^(g)) . C_K[b]^T ; scale*RoPE(q[b,t,h]) . K_chunk[b,0..t,g,:]^T]
+ *   out[b,t,h,:] = ( (A_b . C_V[b]) . U_V^(g)T + A_c . V_chunk[b,0..t,g,:] ) / l
+ *   q        [B, T, Hq, d]    chunk queries before RoPE, T = shape->W
+ *   C_K, C_V [B, N_b, r_k / r_v] latent beacons (N_b may be 0)
+ *   K_chunk  [B, T, Hkv, d]   the chunk's keys, stored after RoPE at p0[b] + s
+ *   V_chunk  [B, T, Hkv, d]   the chunk's values
+ *   U_K, U_V [Hkv*d, r_k / r_v]
+ *   p0       [B] int32        position of chunk token 0 (device)
+ *   out      [B, T, Hq, d] f32
+ *   workspace >= slimkv_workspace_bytes(shape, SLIMKV_PREFILL) (the staged queries)
+ * Runs on the tensor cores only: bf16 storage, d = 128 and, with beacons, r_k and r_v
+ * multiples of 64 up to 256; other shapes return SLIMKV_ERR_SHAPE. Same pointer rules
+ * and errors as slimkv_decode_attn. */
+slimkv_status slimkv_prefill_attn(const slimkv_shape* shape, const void* q, const void* C_K,
+                                  const void* C_V, const void* K_chunk, const void* V_chunk,
+                                  const void* U_K, const void* U_V, const int32_t* p0, float* out,
+                                  void* workspace, size_t ws_bytes, void* stream);
 
 /* Size of the fixed device scratch array behind slimkv_decode_attn_noalloc. */
 #define SLIMKV_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)

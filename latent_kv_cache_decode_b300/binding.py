@@ -18,7 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libslimkv.so")
 
 SLIMKV_F32, SLIMKV_BF16 = 0, 1
-SLIMKV_LATENT, SLIMKV_RECONSTRUCT, SLIMKV_FULL_KV = 0, 1, 2
+SLIMKV_LATENT, SLIMKV_RECONSTRUCT, SLIMKV_FULL_KV, SLIMKV_PREFILL = 0, 1, 2, 3
 STATUS = {0: "SLIMKV_OK", 1: "SLIMKV_ERR_NULL", 2: "SLIMKV_ERR_SHAPE", 3: "SLIMKV_ERR_DTYPE",
           4: "SLIMKV_ERR_ALIGN", 5: "SLIMKV_ERR_WORKSPACE", 6: "SLIMKV_ERR_CUDA",
           7: "SLIMKV_ERR_TOO_LARGE"}
@@ -28,7 +28,7 @@ NOALLOC_SCRATCH_BYTES = 64 << 20   # SLIMKV_NOALLOC_SCRATCH_BYTES
 EXPORTS = ("slimkv_workspace_bytes", "slimkv_decode_attn", "slimkv_decode_attn_alibi", "slimkv_decode_attn_reconstruct",
            "slimkv_decode_attn_reconstruct_rope", "slimkv_decode_attn_full_kv", "slimkv_status_str", "slimkv_abi_version",
            "slimkv_kernel_path", "slimkv_force_simt", "slimkv_time_next_decode",
-           "slimkv_decode_attn_noalloc", "slimkv_append_kv")
+           "slimkv_decode_attn_noalloc", "slimkv_append_kv", "slimkv_prefill_attn")
 
 
 class SlimkvError(RuntimeError):
@@ -73,6 +73,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.slimkv_decode_attn_noalloc.argtypes = [sp] + [vp] * 7 + [i32p, vp, vp]
     lib.slimkv_decode_attn_noalloc.restype = ctypes.c_int
     lib.slimkv_append_kv.argtypes = [sp, vp, vp, vp, vp, i32p, vp]
+    lib.slimkv_prefill_attn.restype = ctypes.c_int
+    lib.slimkv_prefill_attn.argtypes = [sp] + [vp] * 7 + [i32p, vp, vp, sz, vp]
     lib.slimkv_append_kv.restype = ctypes.c_int
     lib.slimkv_status_str.argtypes = [ctypes.c_int]
     lib.slimkv_status_str.restype = ctypes.c_char_p
@@ -287,6 +289,30 @@ def decode_attn_full_kv(q, K, V, q_pos, *, scale=None, rope_base=10000.0, out=No
     st = lib.slimkv_decode_attn_full_kv(ctypes.byref(sh), _ptr(q), _ptr(K), _ptr(V), _ptr(q_pos),
                                         _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "slimkv_decode_attn_full_kv")
+    return out
+
+
+def prefill_attn(q, C_K, C_V, K_chunk, V_chunk, U_K, U_V, p0, *, scale=None, rope_base=10000.0,
+                 out=None, workspace: Optional[Workspace] = None, stream=None):
+    """slimkv_prefill_attn on torch CUDA tensors: a chunk q [B,T,Hq,d] over the beacons
+    and, causally, the chunk's own keys K_chunk / V_chunk [B,T,Hkv,d]; p0 [B] int32 is
+    the position of chunk token 0. Returns out [B,T,Hq,d] float32."""
+    lib = load()
+    B, T, Hq, d = q.shape
+    N_b = C_K.shape[1] if C_K is not None else 0
+    Hkv = K_chunk.shape[2]
+    r_k = C_K.shape[2] if C_K is not None else 0
+    r_v = C_V.shape[2] if C_V is not None else 0
+    sh, nb = _shape_and_bytes(SLIMKV_PREFILL, B, Hq, Hkv, d, N_b, r_k, r_v, T, q.dtype, scale, rope_base)
+    if out is None:
+        out = torch.empty((B, T, Hq, d), dtype=torch.float32, device=q.device)
+    if nb == 0:
+        _check(2, "slimkv_prefill_attn")
+    ws = (workspace or Workspace(q.device)).get(nb)
+    st = lib.slimkv_prefill_attn(ctypes.byref(sh), _ptr(q), _ptr(C_K), _ptr(C_V), _ptr(K_chunk),
+                                 _ptr(V_chunk), _ptr(U_K), _ptr(U_V), _ptr(p0), _ptr(out),
+                                 _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "slimkv_prefill_attn")
     return out
 
 

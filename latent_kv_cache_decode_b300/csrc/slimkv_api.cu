@@ -31,7 +31,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 slimkv_status check_shape(const slimkv_shape* s, int which) {
     if (s == nullptr) return SLIMKV_ERR_NULL;
     if (s->dtype != SLIMKV_F32 && s->dtype != SLIMKV_BF16) return SLIMKV_ERR_DTYPE;
-    if (which < SLIMKV_LATENT || which > SLIMKV_FULL_KV) return SLIMKV_ERR_SHAPE;
+    if (which < SLIMKV_LATENT || which > SLIMKV_PREFILL) return SLIMKV_ERR_SHAPE;
     if (s->B < 1 || s->B > kMaxB) return SLIMKV_ERR_SHAPE;
     if (s->Hq < 1 || s->Hq > kMaxHq || s->Hkv < 1 || s->Hq % s->Hkv != 0) return SLIMKV_ERR_SHAPE;
     if (s->d != 64 && s->d != 128) return SLIMKV_ERR_SHAPE;
@@ -47,6 +47,12 @@ slimkv_status check_shape(const slimkv_shape* s, int which) {
     if (!(s->rope_base > 0.0) || !isfinite(s->rope_base)) return SLIMKV_ERR_SHAPE;
     if (which == SLIMKV_FULL_KV && (s->N_b != 0 || s->W < 1)) return SLIMKV_ERR_SHAPE;
     if (which == SLIMKV_RECONSTRUCT && s->N_b < 1) return SLIMKV_ERR_SHAPE;
+    if (which == SLIMKV_PREFILL) {
+        // the chunk (W tokens) is always present; the tensor-core prefill kernel covers
+        // bf16, d = 128 and ranks that are multiples of 64 up to 256
+        if (s->W < 1 || s->dtype != SLIMKV_BF16) return SLIMKV_ERR_SHAPE;
+        if (!prefill_supported(s->d, s->N_b, s->r_k, s->r_v)) return SLIMKV_ERR_SHAPE;
+    }
     return SLIMKV_OK;
 }
 
@@ -64,6 +70,10 @@ int n_segments(const slimkv_shape* s, int which) {
 
 WsLayout layout(const slimkv_shape* s, int which) {
     WsLayout L;
+    if (which == SLIMKV_PREFILL) {
+        L.total = align_up(prefill_stage_bytes(s->B, s->W, s->Hq, s->Hkv));
+        return L;
+    }
     const bool lat = which == SLIMKV_LATENT && s->N_b > 0;
     L.Dmax = std::max(lat ? s->r_v : 0, s->d);
     L.slots = kSlotCap + n_segments(s, which);
@@ -103,6 +113,7 @@ int device_cc_major() {
 
 int select_path(const slimkv_shape* s, int which) {
     if (check_shape(s, which) != SLIMKV_OK) return -1;
+    if (which == SLIMKV_PREFILL) return 1;   // tensor-core kernel only
     if (g_force_simt) return 0;
     if (s->dtype != SLIMKV_BF16 || s->d != 128) return 0;
     if (!tc_supported(s->Hq, s->Hkv, s->d, which == SLIMKV_LATENT ? s->N_b : 0, s->r_k, s->r_v))
@@ -344,6 +355,37 @@ slimkv_status slimkv_decode_attn_full_kv(const slimkv_shape* shape, const void* 
                                          void* workspace, size_t ws_bytes, void* stream) {
     Ptrs p{q, nullptr, nullptr, K, V, nullptr, nullptr, q_pos, out, workspace, ws_bytes, 0};
     return run(shape, SLIMKV_FULL_KV, p, stream);
+}
+
+slimkv_status slimkv_prefill_attn(const slimkv_shape* shape, const void* q, const void* C_K, const void* C_V,
+                                  const void* K_chunk, const void* V_chunk, const void* U_K, const void* U_V,
+                                  const int32_t* p0, float* out, void* workspace, size_t ws_bytes, void* stream) {
+    slimkv_status st = check_shape(shape, SLIMKV_PREFILL);
+    if (st != SLIMKV_OK) return st;
+    Ptrs p{q, C_K, C_V, K_chunk, V_chunk, U_K, U_V, p0, out, workspace, ws_bytes, 0};
+    st = check_ptrs(shape, SLIMKV_PREFILL, p);
+    if (st != SLIMKV_OK) return st;
+    PrefillCall c;
+    c.B = shape->B;
+    c.T = shape->W;
+    c.Hq = shape->Hq;
+    c.Hkv = shape->Hkv;
+    c.N_b = shape->N_b;
+    c.r_k = shape->r_k;
+    c.r_v = shape->r_v;
+    c.scale = shape->scale;
+    c.rope_base = shape->rope_base;
+    c.q = q;
+    c.C_K = C_K;
+    c.C_V = C_V;
+    c.K_chunk = K_chunk;
+    c.V_chunk = V_chunk;
+    c.U_K = U_K;
+    c.U_V = U_V;
+    c.p0 = p0;
+    c.out = out;
+    c.stage = workspace;
+    return launch_prefill(c, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SLIMKV_OK : SLIMKV_ERR_CUDA;
 }
 
 const char* slimkv_status_str(slimkv_status status) {

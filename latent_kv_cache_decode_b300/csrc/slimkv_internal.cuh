@@ -146,6 +146,26 @@ template <typename T>
 cudaError_t launch_append_kv(const T* k_new, const T* v_new, T* K, T* V, const int32_t* pos, int B, int Hkv,
                              int d, int W, double base, cudaStream_t st);
 
+// Prefill over the beacon memory and a causal chunk (tensor-core path).
+struct PrefillCall {
+    int B, T, Hq, Hkv, N_b, r_k, r_v;
+    float scale;
+    double rope_base;
+    const void* q;         // [B, T, Hq, d] bf16
+    const void* C_K;       // [B, N_b, r_k]
+    const void* C_V;       // [B, N_b, r_v]
+    const void* K_chunk;   // [B, T, Hkv, d] (stored after RoPE)
+    const void* V_chunk;
+    const void* U_K;       // [Hkv d, r_k]
+    const void* U_V;
+    const int32_t* p0;     // [B] position of chunk token 0
+    float* out;            // [B, T, Hq, d]
+    void* stage;           // prefill_stage_bytes of scratch
+};
+bool prefill_supported(int d, int N_b, int r_k, int r_v);
+size_t prefill_stage_bytes(int B, int T, int Hq, int Hkv);
+cudaError_t launch_prefill(const PrefillCall& c, cudaStream_t st);
+
 // Events requested by slimkv_time_next_decode for the next call of this thread.
 struct DecodeTimer {
     cudaEvent_t start = nullptr, stop = nullptr;

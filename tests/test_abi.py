@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.slimkv_abi_version() == 3
+    assert lib.slimkv_abi_version() == 4
     for code, name in bd.STATUS.items():
         s = lib.slimkv_status_str(code)
         assert isinstance(s, bytes) and len(s) > 0
