@@ -208,7 +208,6 @@ struct SoftCtx {
     int tid, wq, lane, myrow, nMB;
     int aw;               // TMEM columns per 128 value rows of the accumulator
     const float* slope_s; // [NS] ALiBi slopes of the piece's score columns (log2 units)
-    int alibi;
 };
 
 // ALiBi offsets of this thread's rows in a tile (key position - query position, one per
@@ -277,11 +276,11 @@ __device__ __forceinline__ float warp_reduce16(float* v, int lane) {
 // the rescale factors alpha = exp2(m_old - m_new), and, when the accumulator already
 // holds earlier tiles of the piece (nMB > 0), the rescale of its columns once the
 // previous value MMAs are done. All 128 softmax threads call it together.
-template <int NS, int NP, int RB, bool LO>
+template <int NS, int NP, int RB, bool LO, bool AL>
 __device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* alpha_s, uint64_t* vfree,
                                              volatile int* abort, uint32_t tS0, uint32_t t_acc_lane, int row0,
                                              int rows, int j, int nMB, int aw, int tid, int lane, int wq,
-                                             const float* slope_s, int alibi, float dk0, float dk1) {
+                                             const float* slope_s, float dk0, float dk1) {
     // per-head maximum over this warp's valid rows, then over the four warps
     float x[NS];
 #pragma unroll
@@ -295,7 +294,7 @@ __device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* 
         for (int hc = 0; hc < NS / 16; ++hc) {
             float sc[16];
             load_scores<LO, NS>(tS + hc * 16, sc);
-            if (alibi) add_bias(sc, slope_s + hc * 16, rb == 0 ? dk0 : dk1);
+            if (AL) add_bias(sc, slope_s + hc * 16, rb == 0 ? dk0 : dk1);
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[hc * 16 + i] = valid ? fmaxf(x[hc * 16 + i], sc[i]) : x[hc * 16 + i];
         }
@@ -342,7 +341,7 @@ __device__ __noinline__ void softmax_new_ref(float* red, float* m_ref_s, float* 
 // 32 bytes, 32-byte swizzle), then signals vready[j]. Every head column is processed
 // alike: the query rows of absent heads are zero, so their scores are finite and
 // their columns, which are never written out, cost no branches.
-template <int NS, int NP, int RB, bool LO>
+template <int NS, int NP, int RB, bool LO, bool AL>
 __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, int rows, bool has_prev,
                                              float (&l_part)[NP], float (&mref)[NP], const RowBias& rbias) {
     constexpr int SW = SBuf<NP>::W;
@@ -365,7 +364,7 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
             for (int hc = 0; hc < NS / 16; ++hc) {
                 float sc[16];
                 load_scores<LO, NS>(tS + hc * 16, sc);
-                if (c.alibi) add_bias(sc, c.slope_s + hc * 16, rbias.d[rb]);
+                if (AL) add_bias(sc, c.slope_s + hc * 16, rbias.d[rb]);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) dm = fmaxf(dm, sc[i] - mref[hc * 16 + i]);
             }
@@ -378,9 +377,9 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
         slow = (fl[0] | fl[1] | fl[2] | fl[3]) != 0;
     }
     if (slow) {
-        softmax_new_ref<NS, NP, RB, LO>(c.red, c.m_ref_s, c.alpha_s, c.bar.vfree, c.abort, tS0, c.t_accp + c.lane_off,
-                                        row0, rows, j, has_prev ? c.nMB : 0, c.aw, c.tid, c.lane, c.wq, c.slope_s,
-                                        c.alibi, rbias.d[0], rbias.d[RB - 1]);
+        softmax_new_ref<NS, NP, RB, LO, AL>(c.red, c.m_ref_s, c.alpha_s, c.bar.vfree, c.abort, tS0,
+                                            c.t_accp + c.lane_off, row0, rows, j, has_prev ? c.nMB : 0, c.aw, c.tid,
+                                            c.lane, c.wq, c.slope_s, rbias.d[0], rbias.d[RB - 1]);
 #pragma unroll
         for (int h = 0; h < NS; ++h) {
             mref[h] = c.m_ref_s[h];
@@ -403,7 +402,7 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
         for (int hc = 0; hc < NS / 16; ++hc) {
             float sc[16];
             load_scores<LO, NS>(tS + hc * 16, sc);
-            if (c.alibi) add_bias(sc, c.slope_s + hc * 16, rbias.d[rb]);
+            if (AL) add_bias(sc, c.slope_s + hc * 16, rbias.d[rb]);
             uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -480,7 +479,7 @@ __device__ __forceinline__ void write_partial(const TcParams& p, const SoftCtx& 
 // NP: query heads rounded up to 16 (a template parameter, so the MMA issue sequences
 // are straight-line code: a conditional branch between two tcgen05.mma instructions
 // costs the issuing thread tens of cycles per MMA).
-template <int NP>
+template <int NP, bool AL>
 __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -835,7 +834,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         c.alpha_s = alpha_s;
         c.flags = flag + 1;
         c.slope_s = slope_s;
-        c.alibi = p.alibi;
         c.abort = abort_flag;
         c.tid = threadIdx.x - 64;            // 0..127
         c.wq = c.tid >> 5;                   // softmax warp 0..3
@@ -864,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 m_ref_s[c.tid] = -INFINITY;
                 // ALiBi slopes of the piece's score columns: every head (latent), or the
                 // heads of the piece's KV group (raw; padded columns get 0)
-                if (p.alibi)
+                if (AL)
                     slope_s[c.tid] = lat ? (c.tid < p.Hq ? p.slope_l2[c.tid] : 0.f)
                                          : (c.tid < G ? p.slope_l2[pc.g * G + c.tid] : 0.f);
             }
@@ -873,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 l_part[h] = 0.f;
                 mref[h] = -INFINITY;
             }
-            const long long qp = p.alibi ? (long long)p.q_pos[pc.b] : 0;
+            const long long qp = AL ? (long long)p.q_pos[pc.b] : 0;
             ptx::named_bar(1, 128);
             int jl = it.j;
             #pragma unroll 1
@@ -883,7 +881,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 // key position - query position of this thread's rows (beacon j at
                 // j * ratio + ratio - 1; window slot s at qp - ((qp - s) mod W))
                 RowBias rbias = {{0.f, 0.f}};
-                if (p.alibi) {
+                if (AL) {
 #pragma unroll
                     for (int rb = 0; rb < 2; ++rb) {
                         const long long row = row0 + rb * 128;
@@ -893,8 +891,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                     }
                 }
                 jl = it.j;
-                if (lat) softmax_tile<NP, NP, 1, false>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref, rbias);
-                else softmax_tile<kNG, NP, kRBRaw, true>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref, rbias);
+                if (lat) softmax_tile<NP, NP, 1, false, AL>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref, rbias);
+                else softmax_tile<kNG, NP, kRBRaw, true, AL>(c, it.j, row0, p.rows[k], t > pc.t0, l_part, mref, rbias);
                 it.next();
             }
             // ---- partial of (CTA, piece): reference max, row sum and accumulator
@@ -1138,10 +1136,10 @@ std::shared_ptr<const CtaPlan> cached_plan(int B, const SegList& sl, int lat_seg
     return r;
 }
 
-template <int NP>
-cudaError_t launch_decode(const TcParams& prm, int grid, uint32_t smem, cudaStream_t st) {
+template <int NP, bool AL>
+cudaError_t launch_decode_t(const TcParams& prm, int grid, uint32_t smem, cudaStream_t st) {
     static std::atomic<unsigned long long> attr_done{0};
-    const cudaError_t ea = set_max_smem_once((const void*)tc_decode_kernel<NP>, kSmemMax, attr_done);
+    const cudaError_t ea = set_max_smem_once((const void*)tc_decode_kernel<NP, AL>, kSmemMax, attr_done);
     if (ea != cudaSuccess) return ea;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -1153,7 +1151,13 @@ cudaError_t launch_decode(const TcParams& prm, int grid, uint32_t smem, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<NP>, prm);
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<NP, AL>, prm);
+}
+// The ALiBi bias is a separate instantiation: the plain decode keeps none of its code
+// (the kernel's speed depends on its instruction-cache footprint).
+template <int NP>
+cudaError_t launch_decode(const TcParams& prm, int grid, uint32_t smem, cudaStream_t st) {
+    return prm.alibi ? launch_decode_t<NP, true>(prm, grid, smem, st) : launch_decode_t<NP, false>(prm, grid, smem, st);
 }
 
 // Kinds of key rows of one call: rows / widths per segment and operands.
