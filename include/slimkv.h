@@ -266,6 +266,22 @@ slimkv_status slimkv_append_kv(const slimkv_shape* shape, const void* k_new, con
 /* Human-readable name of a status. Never NULL. */
 const char* slimkv_status_str(slimkv_status status);
 
+/* Failure detection. Every wait inside the tensor-core kernels is bounded (about 2 s);
+ * a thread block whose wait runs out stops waiting, lets its copies in flight land,
+ * frees its tensor memory, writes NaN into its part of the result and adds one to a
+ * per-device counter, instead of hanging the GPU. slimkv_abort_count synchronises the
+ * current device and returns that counter (thread blocks that gave up since the library
+ * was loaded or last reset; with reset != 0 it is set back to 0), or -1 on a CUDA error.
+ * A status of SLIMKV_OK from a call only means that its launches were accepted. */
+long long slimkv_abort_count(int reset);
+
+/* Test hook for the failure path above: in the next tensor-core decode launch made by
+ * this host thread, thread block `cta` of the split-decode kernel does not load its
+ * first key tile, so that its wait for it runs out (about 2 s later) and the abort path
+ * runs. Nothing faults: the block returns, its result is NaN and the counter rises.
+ * A negative `cta` clears a pending request. Not for production use. */
+void slimkv_test_withhold_first_load(int cta);
+
 /* SLIMKV_ABI_VERSION of the loaded library. */
 int slimkv_abi_version(void);
 

@@ -28,7 +28,8 @@ NOALLOC_SCRATCH_BYTES = 64 << 20   # SLIMKV_NOALLOC_SCRATCH_BYTES
 EXPORTS = ("slimkv_workspace_bytes", "slimkv_decode_attn", "slimkv_decode_attn_alibi", "slimkv_decode_attn_reconstruct",
            "slimkv_decode_attn_reconstruct_rope", "slimkv_decode_attn_full_kv", "slimkv_status_str", "slimkv_abi_version",
            "slimkv_kernel_path", "slimkv_force_simt", "slimkv_time_next_decode",
-           "slimkv_decode_attn_noalloc", "slimkv_append_kv", "slimkv_prefill_attn")
+           "slimkv_decode_attn_noalloc", "slimkv_append_kv", "slimkv_prefill_attn",
+           "slimkv_abort_count", "slimkv_test_withhold_first_load")
 
 
 class SlimkvError(RuntimeError):
@@ -73,6 +74,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.slimkv_decode_attn_noalloc.argtypes = [sp] + [vp] * 7 + [i32p, vp, vp]
     lib.slimkv_decode_attn_noalloc.restype = ctypes.c_int
     lib.slimkv_append_kv.argtypes = [sp, vp, vp, vp, vp, i32p, vp]
+    lib.slimkv_abort_count.restype = ctypes.c_longlong
+    lib.slimkv_abort_count.argtypes = [ctypes.c_int]
+    lib.slimkv_test_withhold_first_load.restype = None
+    lib.slimkv_test_withhold_first_load.argtypes = [ctypes.c_int]
     lib.slimkv_prefill_attn.restype = ctypes.c_int
     lib.slimkv_prefill_attn.argtypes = [sp] + [vp] * 7 + [i32p, vp, vp, sz, vp]
     lib.slimkv_append_kv.restype = ctypes.c_int
@@ -336,6 +341,21 @@ def decode_attn_noalloc(q, C_K, C_V, K_raw, V_raw, U_K, U_V, q_pos, *, scale=Non
                                         _ptr(q_pos), _ptr(out), _stream(stream))
     _check(st, "slimkv_decode_attn_noalloc")
     return out
+
+
+def abort_count(reset: bool = False) -> int:
+    """Thread blocks of the tensor-core kernels on the current device that gave up on a
+    bounded wait (their results are NaN) since load or the last reset; synchronises."""
+    n = int(load().slimkv_abort_count(1 if reset else 0))
+    if n < 0:
+        raise SlimkvError(6, "slimkv_abort_count")
+    return n
+
+
+def withhold_first_load_for_test(cta: int):
+    """Test hook: the next tensor-core decode launch of this thread skips CTA `cta`'s
+    first key load, so that a bounded wait runs out and the abort path runs."""
+    load().slimkv_test_withhold_first_load(int(cta))
 
 
 def status_str(status: int) -> str:

@@ -10,10 +10,33 @@
 
 using namespace slimkv;
 
+// CTAs of the tensor-core kernels that gave up on a bounded wait (one counter per
+// device: every device that loads the library has its own copy of this variable).
+__device__ unsigned long long g_slimkv_aborts;
+
 namespace slimkv {
 DecodeTimer& decode_timer() {
     static thread_local DecodeTimer t;
     return t;
+}
+
+unsigned long long* abort_counter() {
+    static unsigned long long* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_slimkv_aborts) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<unsigned long long*>(p);
+    }
+    return addr[dev];
+}
+
+static thread_local int g_withhold_cta = -1;
+int take_withheld_cta() {
+    const int c = g_withhold_cta;
+    g_withhold_cta = -1;
+    return c;
 }
 }  // namespace slimkv
 
@@ -436,6 +459,17 @@ void slimkv_time_next_decode(void* start_event, void* stop_event) {
     t.stop = static_cast<cudaEvent_t>(stop_event);
     if (!t.start || !t.stop) t.start = t.stop = nullptr;
 }
+
+long long slimkv_abort_count(int reset) {
+    unsigned long long* p = abort_counter();
+    if (p == nullptr || cudaDeviceSynchronize() != cudaSuccess) return -1;
+    unsigned long long n = 0;
+    if (cudaMemcpy(&n, p, sizeof(n), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+    if (reset && cudaMemset(p, 0, sizeof(n)) != cudaSuccess) return -1;
+    return (long long)n;
+}
+
+void slimkv_test_withhold_first_load(int cta) { g_withhold_cta = cta < 0 ? -1 : cta; }
 
 int slimkv_force_simt(int on) {
     const int prev = g_force_simt;

@@ -166,6 +166,13 @@ bool prefill_supported(int d, int N_b, int r_k, int r_v);
 size_t prefill_stage_bytes(int B, int T, int Hq, int Hkv);
 cudaError_t launch_prefill(const PrefillCall& c, cudaStream_t st);
 
+// Device address of the current device's abort counter (CTAs of the tensor-core
+// kernels that gave up on a bounded wait), or NULL if it cannot be had.
+unsigned long long* abort_counter();
+// The CTA that the next tensor-core decode launch of this host thread withholds its
+// first key load from (slimkv_test_withhold_first_load), then -1 again.
+int take_withheld_cta();
+
 // Events requested by slimkv_time_next_decode for the next call of this thread.
 struct DecodeTimer {
     cudaEvent_t start = nullptr, stop = nullptr;

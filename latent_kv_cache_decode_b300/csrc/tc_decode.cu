@@ -104,6 +104,8 @@ struct TcParams {
     int alibi, ratio;
     const int32_t* q_pos;
     float slope_l2[64];
+    unsigned long long* aborts;       // device counter of CTAs that gave up on a wait
+    int withhold_cta;                 // test hook: this CTA skips its first key load (-1: none)
     int u_begin[kMaxCtas + 1];        // CTA i owns units (tiles) [u_begin[i], u_begin[i+1])
     int slot_base[kMaxCtas];          // first partial slot of CTA i
 };
@@ -614,6 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
 #pragma unroll 1
                 for (int c = 0; c < nc; ++c) slot_free(ring_wrap(pos + c, p.nslot));
                 const int jr = ti.j % kR;
+                // test hook: the first key tile of this CTA is never loaded, so the wait
+                // for it runs out and the CTA takes the abort path
+                const bool withheld = p.withhold_cta == cta && ti.j == 0 && part == 0;
                 if (part == 0) {
                     if (ti.first() && ti.j > 0) {
                         if (q_pend) try_q(true);   // the previous piece's image goes first
@@ -623,13 +628,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                         q_tile = ti.j;
                         q_after = ti.j - 1;
                     }
-                    ptx::mbar_expect_tx(&bar.kready[jr], nc * kSlot);
+                    if (!withheld) ptx::mbar_expect_tx(&bar.kready[jr], nc * kSlot);
                 } else {
                     ptx::mbar_expect_tx(&bar.vready[jr], nc * kSlot);
                 }
                 uint64_t* rb = part ? &bar.vready[jr] : &bar.kready[jr];
 #pragma unroll 1
-                for (int c = 0; c < nc; ++c) {
+                for (int c = 0; c < nc && !withheld; ++c) {
                     const int s = ring_wrap(pos + c, p.nslot);
                     uint8_t* dst = ring + (size_t)s * kSlot;
                     const int col = (c % ncols) * 128;
@@ -643,6 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                     }
                     owner[s] = (ti.j << 1) | part;
                 }
+                if (withheld)
+                    for (int c = 0; c < nc; ++c) owner[ring_wrap(pos + c, p.nslot)] = (ti.j << 1) | part;
                 pos = ring_wrap(pos + nc, p.nslot);
                 try_q(false);
                 if (isK) kiss = ti.j + 1;
@@ -922,8 +929,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         ptx::tmem_dealloc(tmem, p.tmem_cols);
     }
     if (*abort_flag && warp >= 2 && warp <= 5) {
-        // a wait ran out: poison this CTA's partials so the result is NaN, not stale
+        // a wait ran out: poison this CTA's partials so the result is NaN, not stale, and
+        // count the CTA where the host can read it
         const int tid = threadIdx.x - 64;
+        if (tid == 0 && p.aborts != nullptr) atomicAdd(p.aborts, 1ull);
         int npieces = 0;
         #pragma unroll 1
         for (int u = u0; u < u1;) {
@@ -1288,6 +1297,8 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
         prm.q_pos = c.q_pos;
         for (int h = 0; h < c.Hq; ++h) prm.slope_l2[h] = c.alibi_slopes[h] * kLog2e;
     }
+    prm.aborts = abort_counter();
+    prm.withhold_cta = take_withheld_cta();
     for (int i = 0; i <= w.n_ctas; ++i) prm.u_begin[i] = w.u_begin[i];
     for (int i = 0; i < w.n_ctas; ++i) prm.slot_base[i] = w.slot_base[i];
 

@@ -56,6 +56,7 @@ struct GemmParams {
     // j * ratio + ratio - 1; turn[i] = theta_i / (2 pi) as a 64-bit fraction of a turn
     int ratio, rows_per_b;
     unsigned long long turn[64];
+    unsigned long long* aborts;   // device counter of CTAs that gave up on a wait
 };
 
 __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -251,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) recon_gemm_kernel(const __grid_co
     // ----------------------------------------------------------------- teardown
     ptx::tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag && p.aborts != nullptr) atomicAdd(p.aborts, 1ull);
     if (warp == 1) {
         ptx::tc_fence_after();
         if (lane == 0) {
@@ -305,6 +307,7 @@ cudaError_t launch_reconstruct_gemm(const __nv_bfloat16* C, const __nv_bfloat16*
     memset(&p, 0, sizeof(p));
     if (!make_map_2d(&p.tmC, C, r, rows) || !make_map_2d(&p.tmU, U, r, n)) return cudaErrorInvalidValue;
     p.out = out;
+    p.aborts = abort_counter();
     p.rows = rows;
     p.n = n;
     p.r = r;

@@ -70,6 +70,7 @@ struct PrefillParams {
     CUtensorMap tmUK;   // U_K [Hkv d, r_k], boxes 64 x 128
     CUtensorMap tmUV;   // U_V [Hkv d, r_v]
     float* out;         // [B, T, Hq, d]
+    unsigned long long* aborts;   // device counter of CTAs that gave up on a wait
     int T, Hq, Hkv, G, N_b, r_k, r_v, rows_pad;
 };
 
@@ -540,6 +541,7 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_prefill_kernel(const __grid_c
     // ----------------------------------------------------------------- teardown
     ptx::tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag && p.aborts != nullptr) atomicAdd(p.aborts, 1ull);
     if (warp == 1) {
         ptx::tc_fence_after();
         if (lane == 0) {
@@ -654,6 +656,7 @@ cudaError_t launch_prefill(const PrefillCall& c, cudaStream_t st) {
         }
     }
     p.out = c.out;
+    p.aborts = abort_counter();
     p.T = c.T;
     p.Hq = c.Hq;
     p.Hkv = c.Hkv;
