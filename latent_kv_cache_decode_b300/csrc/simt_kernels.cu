@@ -64,8 +64,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 // may read anything the preceding kernels wrote (the caches) without a wait of its own.
 // ---------------------------------------------------------------------------
 constexpr int kQpRows = 32;
-constexpr int kQpCols = 16;
+constexpr int kQpCols = 32;
 constexpr int kQpThreads = 256;
+// Dynamic shared memory of the query projection when it is launched early behind a
+// combine (it holds the U_K block; the rest is reserved, unused). Its CTAs are placed
+// while the combine's CTAs still occupy the SMs, and by registers alone three of them
+// would fit beside one combine CTA, so the block scheduler would stack them on a few
+// SMs and the grid would end with those (measured: 1.6 us alone, up to 8 us stacked).
+// With this reservation (plus the static rows) no SM takes two of them.
+constexpr int kQpSpreadSmem = 112 * 1024;
+constexpr int kQpUBytes = 128 * kQpCols * 4;   // the U_K column block (dynamic shared memory)
 
 // 16-byte vector of storage elements: 8 bf16 or 4 float32.
 template <typename T> struct Vec16;
@@ -96,7 +104,8 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
     // query rows, rotated and scaled (row stride padded by 4 floats: the projection
     // reads two rows per warp, which then fall in different banks)
     __shared__ __align__(16) float qr_s[kQpRows][128 + 4];
-    __shared__ __align__(16) float u_s[128][kQpCols];   // U_K^(g) column block
+    extern __shared__ __align__(16) float u_dyn[];
+    float (*u_s)[kQpCols] = reinterpret_cast<float (*)[kQpCols]>(u_dyn);   // U_K^(g) column block [d][kQpCols]
     constexpr int VN = Vec16<T>::N;
     const int g = blockIdx.x, cb = blockIdx.y, rb = blockIdx.z;
     const int tid = threadIdx.x;
@@ -121,8 +130,11 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
         constexpr int upr = kQpCols / VN;   // vectors per row of the block
         for (int idx = tid; idx < d * upr; idx += kQpThreads) {
             const int i = idx / upr, e = (idx - i * upr) * VN;
-            const uint4 v = *reinterpret_cast<const uint4*>((const T*)a.U_K + ((size_t)g * d + i) * a.r_k +
-                                                            cb * kQpCols + e);
+            // columns past r_k (a last, partial block) read as zero
+            const uint4 v = cb * kQpCols + e < a.r_k
+                                ? *reinterpret_cast<const uint4*>((const T*)a.U_K + ((size_t)g * d + i) * a.r_k +
+                                                                  cb * kQpCols + e)
+                                : make_uint4(0u, 0u, 0u, 0u);
             float f[VN];
             Vec16<T>::to_f(v, f);
 #pragma unroll
@@ -197,29 +209,34 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
         for (int idx = tid; idx < nb * npad * kQpCols; idx += kQpThreads) {
             const int bl = idx / (npad * kQpCols), rem = idx - bl * npad * kQpCols;
             const int h = a.Hq + rem / kQpCols, col = cb * kQpCols + rem % kQpCols;
+            if (col >= a.r_k) continue;
             uint8_t* img = a.lat_img + (size_t)(b0 + bl) * lat_img_bytes(a.NP, a.r_k);
             *reinterpret_cast<__nv_bfloat16*>(img + ptx::sw128_offset(h, col, a.NP)) = __float2bfloat16_rn(0.f);
         }
     }
     if (a.U_K == nullptr) return;
-    // q_lat block: 32 rows x 16 columns; thread = (column c, row pair rp)
-    const int c = tid & (kQpCols - 1), rp = tid / kQpCols;
-    const int r0 = 2 * rp, r1 = 2 * rp + 1;
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 4
+    // q_lat block: 32 rows x kQpCols columns; thread = (column c, rows rg, rg + RG, ...)
+    constexpr int RG = kQpThreads / kQpCols;     // row groups
+    constexpr int RPT = kQpRows / RG;            // rows per thread
+    const int c = tid & (kQpCols - 1), rg = tid / kQpCols;
+    float acc[RPT];
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) acc[k] = 0.f;
+#pragma unroll 2
     for (int i = 0; i < d; i += 4) {
-        const float4 qa = *reinterpret_cast<const float4*>(&qr_s[r0][i]);
-        const float4 qb = *reinterpret_cast<const float4*>(&qr_s[r1][i]);
         const float u0 = u_s[i][c], u1 = u_s[i + 1][c], u2 = u_s[i + 2][c], u3 = u_s[i + 3][c];
-        acc0 = fmaf(qa.x, u0, fmaf(qa.y, u1, fmaf(qa.z, u2, fmaf(qa.w, u3, acc0))));
-        acc1 = fmaf(qb.x, u0, fmaf(qb.y, u1, fmaf(qb.z, u2, fmaf(qb.w, u3, acc1))));
+#pragma unroll
+        for (int k = 0; k < RPT; ++k) {
+            const float4 q4 = *reinterpret_cast<const float4*>(&qr_s[rg + k * RG][i]);
+            acc[k] = fmaf(q4.x, u0, fmaf(q4.y, u1, fmaf(q4.z, u2, fmaf(q4.w, u3, acc[k]))));
+        }
     }
     const int col = cb * kQpCols + c;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int r = k ? r1 : r0;
-        const float v = k ? acc1 : acc0;
-        if (r < rows) {
+    for (int k = 0; k < RPT; ++k) {
+        const int r = rg + k * RG;
+        const float v = acc[k];
+        if (r < rows && col < a.r_k) {
             const int bl = r / ni, h = g * G + i0 + (r - bl * ni);
             if (a.q_lat != nullptr) a.q_lat[((size_t)(b0 + bl) * a.Hq + h) * a.r_k + col] = v;
             if (a.lat_img != nullptr) {
@@ -612,11 +629,13 @@ cudaError_t launch_qproj(const T* q, const T* U_K, const int32_t* q_pos, float* 
     }
     rope_turns(base, d, a.turn);
     const int row_blocks = (G <= kQpRows) ? (B + a.nbb - 1) / a.nbb : B * a.hcn;
-    const int col_blocks = U_K ? r_k / kQpCols : 1;
+    const int col_blocks = U_K ? (r_k + kQpCols - 1) / kQpCols : 1;
     static std::atomic<unsigned long long> attr_done{0};
-    const cudaError_t e = set_max_smem_once((const void*)qproj_kernel<T>, 0, attr_done);
+    const cudaError_t e =
+        set_max_smem_once((const void*)qproj_kernel<T>, std::max(kQpSpreadSmem, kQpUBytes), attr_done);
     if (e != cudaSuccess) return e;
-    return launch_ex(qproj_kernel<T>, dim3(Hkv, col_blocks, row_blocks), dim3(kQpThreads), 0, st, pdl, a);
+    return launch_ex(qproj_kernel<T>, dim3(Hkv, col_blocks, row_blocks), dim3(kQpThreads),
+                     (size_t)(pdl ? std::max(kQpSpreadSmem, kQpUBytes) : kQpUBytes), st, pdl, a);
 }
 
 template <typename T>

@@ -135,20 +135,25 @@ __global__ void __maxnreg__(96) tc_combine_kernel(const __grid_constant__ Combin
         for (int base = 0; base < ns; base += 32) {
             const int s = base + lane;
             if (s >= ns) continue;
+            // kind, m and l in one memory round (the (m, l) of a slot that does not cover
+            // this CTA's heads are read and dropped)
             const int kd = a.kind[s0 + s];
+            float mm[kHeads], ll[kHeads];
+#pragma unroll
+            for (int k = 0; k < kHeads; ++k) {
+                const int hk = h0 + min(k, nh - 1);
+                mm[k] = a.ml[((size_t)(s0 + s) * 2) * a.Hq + hk];
+                ll[k] = a.ml[((size_t)(s0 + s) * 2 + 1) * a.Hq + hk];
+            }
             const bool cover = s0 + s < sm ? (latent && kd == kSlotLatent) : (kd == kSlotRawAll || kd == kSlotRawGroup + g);
             float m[kHeads], l[kHeads];
 #pragma unroll
             for (int k = 0; k < kHeads; ++k) {
                 m[k] = -INFINITY;
                 l[k] = 0.f;
-                if (k < nh && cover) {
-                    const float mm = a.ml[((size_t)(s0 + s) * 2) * a.Hq + h0 + k];
-                    const float ll = a.ml[((size_t)(s0 + s) * 2 + 1) * a.Hq + h0 + k];
-                    if (ll != 0.f) {   // a NaN (poisoned) l is kept
-                        m[k] = mm;
-                        l[k] = ll;
-                    }
+                if (k < nh && cover && ll[k] != 0.f) {   // a NaN (poisoned) l is kept
+                    m[k] = mm[k];
+                    l[k] = ll[k];
                 }
                 mx[k] = fmaxf(mx[k], m[k]);
             }
