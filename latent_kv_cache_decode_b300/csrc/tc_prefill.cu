@@ -228,11 +228,13 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_prefill_kernel(const __grid_c
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
+            // beacon and chunk tiles keep the default L2 policy: every CTA of a batch element
+            // (all its KV groups and row blocks) reads the same beacon tiles, so they
+            // should stay in L2 rather than be streamed
             const int qrow = (b * p.Hkv + g) * p.rows_pad + R0;
             ptx::mbar_expect_tx(q_full, kQRegion);
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) ptx::tma_load_2d(qreg + i * kBox16, &p.tmQ, 64 * i, qrow, q_full);
-            const uint64_t pol = ptx::policy_evict_first();
             auto acquire = [&](int f) -> uint8_t* {
                 if (f >= kRing) ptx::mbar_wait(&empty[fslot(f)], fphase(f) ^ 1u, abort_flag);
                 return ring + fslot(f) * kSlotB;
@@ -261,12 +263,12 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_prefill_kernel(const __grid_c
                         const CUtensorMap* tm = part ? &p.tmCV : &p.tmCK;
                         ptx::mbar_expect_tx(fb, (uint32_t)(n * kBox8));
                         for (int k = 0; k < n; ++k)
-                            ptx::tma_load_3d_hint(dst + k * kBox8, tm, 64 * k, jl * kPKeys, b, fb, pol);
+                            ptx::tma_load_3d(dst + k * kBox8, tm, 64 * k, jl * kPKeys, b, fb);
                     } else {
                         const CUtensorMap* tm = part ? &p.tmV : &p.tmK;
                         ptx::mbar_expect_tx(fb, 2 * kBox8);
                         for (int k = 0; k < 2; ++k)
-                            ptx::tma_load_4d_hint(dst + k * kBox8, tm, 64 * k, g, j * kPKeys, b, fb, pol);
+                            ptx::tma_load_4d(dst + k * kBox8, tm, 64 * k, g, j * kPKeys, b, fb);
                     }
                 }
             }
