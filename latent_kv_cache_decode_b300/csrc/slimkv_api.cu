@@ -20,16 +20,15 @@ DecodeTimer& decode_timer() {
     return t;
 }
 
+// Looked up on every call (not cached): after a device reset the module is loaded
+// again and the variable may live at another address.
 unsigned long long* abort_counter() {
-    static unsigned long long* addr[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_slimkv_aborts) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<unsigned long long*>(p);
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_slimkv_aborts) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
     }
-    return addr[dev];
+    return static_cast<unsigned long long*>(p);
 }
 
 static thread_local int g_withhold_cta = -1;
