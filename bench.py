@@ -517,18 +517,25 @@ def run_slimkv(args):
     # appends overwrite the windows
     loop = None
     if args.loop > 0 and mode == "latent":
-        steps = wl.decode_steps(w, 0, 1, batch=batch_shard(w.B, world, rank))
-        k_new = [steps["k_new"][0].to(dev) for _ in layers]
-        v_new = [steps["v_new"][0].to(dev) for _ in layers]
+        # every (token, layer) gets its own query, key and value: seeded device draws for
+        # all tokens, copied into the graph's input buffers before each token's replay
+        # (inside the timed region, like the position)
+        Bl = layers[0]["q"].shape[0]
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(w.seed * 1000 + 17 + rank)
+        q_all = torch.randn((args.loop, w.layers, Bl, w.Hq, w.d), generator=gen, device=dev).to(w.torch_dtype())
+        kv_all = torch.randn((args.loop, 2, w.layers, Bl, w.Hkv, w.d), generator=gen, device=dev).to(w.torch_dtype())
+        q_cur = q_all[0].clone()
+        kv_cur = kv_all[0].clone()
         pos_all = (layers[0]["q_pos"].to(torch.int64)[None, :] +
                    torch.arange(args.loop + 1, device=dev)[:, None]).to(torch.int32)
         pos_cur = pos_all[0].clone()
 
         def token_step():
             for l, t in enumerate(layers):
-                bd.append_kv(k_new[l], v_new[l], t["K_raw"], t["V_raw"], pos_cur, rope_base=w.rope_base,
+                bd.append_kv(kv_cur[0, l], kv_cur[1, l], t["K_raw"], t["V_raw"], pos_cur, rope_base=w.rope_base,
                              stream=stream)
-                bd.decode_attn(t["q"], t["C_K"], t["C_V"], t["K_raw"], t["V_raw"], t["U_K"], t["U_V"], pos_cur,
+                bd.decode_attn(q_cur[l], t["C_K"], t["C_V"], t["K_raw"], t["V_raw"], t["U_K"], t["U_V"], pos_cur,
                                scale=w.scale, rope_base=w.rope_base, out=outs[l], workspace=ws, stream=stream)
 
         with torch.cuda.stream(stream):
@@ -543,12 +550,16 @@ def run_slimkv(args):
             la.record(stream)
             for i in range(args.loop):
                 pos_cur.copy_(pos_all[i + 1], non_blocking=True)
+                q_cur.copy_(q_all[i], non_blocking=True)
+                kv_cur.copy_(kv_all[i], non_blocking=True)
                 g_tok.replay()
             lb.record(stream)
         torch.cuda.synchronize()
         us_tok = la.elapsed_time(lb) * 1e3 / args.loop
         loop = {"tokens": args.loop, "us_per_token": us_tok, "tokens_per_s": world * w.B / (us_tok * 1e-6),
-                "per_token": f"{w.layers} layers x (window append + decode), CUDA graph per token",
+                "per_token": f"{w.layers} layers x (window append + decode), CUDA graph per token; each token's "
+                             "queries, keys and values (distinct per token and layer) copied into the graph's "
+                             "inputs before its replay",
                 "gpu_launches_per_token": w.layers * 4}
 
     if rank != 0:
