@@ -180,14 +180,15 @@ __global__ void __launch_bounds__(kQpThreads) qproj_kernel(const __grid_constant
     if (cb == 0 && a.raw_img != nullptr) {
         // raw image of (b, g): 32 rows x d, rows [0,16) high, [16,32) low parts of the
         // group's G (<= 16) heads; rows of absent heads are zero
-        const size_t ib = raw_img_bytes(d);
-        const int units = d / 8;
+        // rows of 128 columns: with d = 64 the columns past d are zero
+        const size_t ib = raw_img_bytes(128);
+        const int units = 128 / 8;
         for (int idx = tid; idx < nb * 16 * units; idx += kQpThreads) {
             const int bl = idx / (16 * units), rem = idx - bl * 16 * units;
             const int i = rem / units, u = rem - i * units;
             uint8_t* img = a.raw_img + ((size_t)(b0 + bl) * a.Hkv + g) * ib;
             uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
-            if (i < G) {
+            if (i < G && u * 8 < d) {
                 const float* src = &qr_s[bl * ni + i][u * 8];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {

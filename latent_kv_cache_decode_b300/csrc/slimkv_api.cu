@@ -108,7 +108,7 @@ WsLayout layout(const slimkv_shape* s, int which) {
     L.lat_img = off;
     if (lat) off = align_up(off + (size_t)s->B * lat_img_bytes(NP, s->r_k));
     L.raw_img = off;
-    off = align_up(off + (size_t)s->B * s->Hkv * raw_img_bytes(s->d));
+    off = align_up(off + (size_t)s->B * s->Hkv * raw_img_bytes(128));   // 128 columns (d = 64 zero-padded)
     L.acc = off;
     off = align_up(off + sizeof(float) * (size_t)L.slots * s->Hq * L.Dmax);
     L.ml = off;
@@ -137,7 +137,10 @@ int select_path(const slimkv_shape* s, int which) {
     if (check_shape(s, which) != SLIMKV_OK) return -1;
     if (which == SLIMKV_PREFILL) return 1;   // tensor-core kernel only
     if (g_force_simt) return 0;
-    if (s->dtype != SLIMKV_BF16 || s->d != 128) return 0;
+    if (s->dtype != SLIMKV_BF16) return 0;
+    // d = 64 runs on the tensor cores with zero-padded raw tiles, except the
+    // reconstruction baselines (their GEMM writes 128-column blocks per KV head)
+    if (s->d != 128 && (s->d != 64 || which == SLIMKV_RECONSTRUCT)) return 0;
     if (!tc_supported(s->Hq, s->Hkv, s->d, which == SLIMKV_LATENT ? s->N_b : 0, s->r_k, s->r_v))
         return 0;
     return device_cc_major() == 10 ? 1 : 0;

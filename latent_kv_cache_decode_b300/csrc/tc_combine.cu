@@ -48,7 +48,7 @@ __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v &
 __global__ void __maxnreg__(96) tc_combine_kernel(const __grid_constant__ CombineArgs a) {
     extern __shared__ __align__(16) float dyn[];
     __shared__ float L_s[kHeads];
-    constexpr int d = 128;
+    const int d = a.d;
     const int G = a.Hq / a.Hkv, nhc = (G + kHeads - 1) / kHeads;
     const int g = blockIdx.x / nhc, hc = blockIdx.x - g * nhc, b = blockIdx.y, i0 = blockIdx.z * kRows;
     const int h0 = g * G + hc * kHeads, nh = min(kHeads, G - hc * kHeads);
@@ -265,7 +265,7 @@ __global__ void __maxnreg__(96) tc_combine_kernel(const __grid_constant__ Combin
 cudaError_t launch_tc_combine(const CombineArgs& a, cudaStream_t st) {
     int ns_max = 0;
     for (int b = 0; b < a.B; ++b) ns_max = std::max(ns_max, a.slot_begin[b + 1] - a.slot_begin[b]);
-    if (ns_max > kMaxSlotsPerB || a.d != 128) return cudaErrorInvalidValue;
+    if (ns_max > kMaxSlotsPerB || a.d % kRows != 0 || a.d > 128) return cudaErrorInvalidValue;
     CombineArgs c = a;
     c.ns_max = (ns_max + 3) & ~3;
     const int r_v = a.U_V != nullptr ? a.r_v : 0;
@@ -281,7 +281,7 @@ cudaError_t launch_tc_combine(const CombineArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const int G = a.Hq / a.Hkv, nhc = (G + kHeads - 1) / kHeads;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.Hkv * nhc, a.B, 128 / kRows);
+    cfg.gridDim = dim3(a.Hkv * nhc, a.B, a.d / kRows);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;

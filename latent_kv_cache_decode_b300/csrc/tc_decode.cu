@@ -73,6 +73,7 @@ constexpr int kNG = 16;               // heads of a raw tile's query operand (th
 // for the previous value MMAs) off the common path even for peaked score distributions.
 constexpr float kLazy = 20.f;
 constexpr int kPAtom = 128 * 32;      // bytes of one 16-head column block of P per 128 rows (x 32 B)
+constexpr int kRawCols = 128;         // columns of a raw tile row (d = 64 rows are zero-padded)
 constexpr int kRBRaw = 2;             // 128-row blocks per raw tile: a raw tile is 256 tokens of one KV head
 constexpr int kR = 16;                // depth of the per-tile barrier rings
 constexpr int kMaxSlots = 16;
@@ -105,6 +106,7 @@ struct TcParams {
     const int32_t* q_pos;
     float slope_l2[64];
     unsigned long long* aborts;       // device counter of CTAs that gave up on a wait
+    int d_raw;                        // head dimension of the raw rows (64 or 128; tiles are 128 wide)
     int withhold_cta;                 // test hook: this CTA skips its first key load (-1: none)
     int u_begin[kMaxCtas + 1];        // CTA i owns units (tiles) [u_begin[i], u_begin[i+1])
     int slot_base[kMaxCtas];          // first partial slot of CTA i
@@ -907,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
             ptx::tc_fence_after();
             const int slot = p.slot_base[cta] + piece;
             if (lat) write_partial<NP, NP>(p, c, slot, kSlotLatent, 0, nvalid, p.dv[k], l_part);
-            else write_partial<kNG, NP>(p, c, slot, kSlotRawGroup + pc.g, pc.g * G, nvalid, p.dv[k], l_part);
+            else write_partial<kNG, NP>(p, c, slot, kSlotRawGroup + pc.g, pc.g * G, nvalid, p.d_raw, l_part);
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bar.accfree[p.accbuf == 2 ? (piece & 1) : 0]);
             ptx::named_bar(1, 128);
@@ -1185,7 +1187,10 @@ Kinds kinds_of(const TcCall& c) {
         if (T <= 0) return;
         s.rows[k] = T;
         s.ngroups[k] = c.Hkv;
-        s.dk[k] = s.dv[k] = c.d;
+        // raw tiles are 128 columns wide; with d = 64 the second 64-column box of every
+        // row lies past the tensor and is filled with zeros by the copy (no memory
+        // traffic), so scores and value rows are those of d = 64
+        s.dk[k] = s.dv[k] = kRawCols;
         s.K[k] = K;
         s.V[k] = V;
     };
@@ -1211,8 +1216,9 @@ Kinds kinds_of(const TcCall& c) {
 }  // namespace
 
 bool tc_supported(int Hq, int Hkv, int d, int N_b, int r_k, int r_v) {
-    if (d != 128 || Hq > 64 || Hkv > 128 || Hq / Hkv > kNG) return false;
-    int rows[kNumKinds] = {N_b, 1, 1}, dk[kNumKinds] = {r_k, d, d}, dv[kNumKinds] = {r_v, d, d};
+    if ((d != 128 && d != 64) || Hq > 64 || Hkv > 128 || Hq / Hkv > kNG) return false;
+    int rows[kNumKinds] = {N_b, 1, 1}, dk[kNumKinds] = {r_k, kRawCols, kRawCols},
+        dv[kNumKinds] = {r_v, kRawCols, kRawCols};
     if (N_b <= 0) rows[0] = 0;
     return plan_smem(Hq, dk, dv, rows).ok;
 }
@@ -1277,7 +1283,8 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     prm.lat_img = c.lat_img;
     prm.raw_img = c.raw_img;
     prm.lat_img_bytes = (uint32_t)lat_img_bytes(sp.NP, c.r_k);
-    prm.raw_img_bytes = (uint32_t)raw_img_bytes(c.d);
+    prm.raw_img_bytes = (uint32_t)raw_img_bytes(kRawCols);
+    prm.d_raw = c.d;
     prm.acc = c.acc;
     prm.ml = c.ml;
     prm.kind = c.kind;

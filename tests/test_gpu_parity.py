@@ -122,6 +122,26 @@ def test_large_ranks_take_the_tensor_core_path(Hq, rank):
     assert bd.kernel_path(sh, bd.SLIMKV_LATENT) == 1
 
 
+@pytest.mark.parametrize("which,path", [("latent", 1), ("full", 1), ("reconstruct", 0)])
+def test_d64_paths(which, path):
+    # bf16 with d = 64: the decode and full-KV attention run on the tensor cores with
+    # zero-padded 128-column raw tiles; the reconstruction baselines stay on the SIMT path
+    sh = bd.make_shape(2, 8, 2, 64, 0 if which == "full" else 128, 64, 64, 96, torch.bfloat16)
+    code = {"latent": bd.SLIMKV_LATENT, "full": bd.SLIMKV_FULL_KV, "reconstruct": bd.SLIMKV_RECONSTRUCT}[which]
+    assert bd.kernel_path(sh, code) == path
+
+
+@pytest.mark.parametrize("case", [
+    dict(B=3, Hq=8, Hkv=2, N_b=300, W=200, rank=128),        # several tiles and ragged ends
+    dict(B=1, Hq=40, Hkv=8, N_b=256, W=129, rank=256),       # G = 5, rank 256
+    dict(B=2, Hq=16, Hkv=2, N_b=0, W=600, rank=64),          # window only (3 raw tiles per head)
+])
+def test_d64_tensor_core_decode_matches_oracle(case):
+    w = wl.custom(d=64, **case)
+    t = wl.layer_tensors(w, 0)
+    assert_close(run_gpu("latent", w, t), run_oracle("latent", w, t), w.dtype, f"d64 {case}")
+
+
 @pytest.mark.parametrize("case", EDGE, ids=[c["name"] for c in EDGE])
 @pytest.mark.parametrize("which", ["latent", "reconstruct", "full"])
 def test_edge_cases(case, which):
@@ -192,15 +212,16 @@ def test_config1_reconstruct_rope_one_layer():
                  "config1 reconstruct-rope")
 
 
-# ALiBi on the reconstruction-free decode (tensor-core path for bf16 / d = 128, SIMT path
-# for float32 storage or d = 64), with the slopes of bd.alibi_slopes.
+# ALiBi on the reconstruction-free decode (tensor-core path for bf16, d = 128 or 64; SIMT
+# path for float32 storage), with the slopes of bd.alibi_slopes.
 @pytest.mark.parametrize("case", [
     ("config0-f32", None),
     ("bf16-tc", dict(B=2, Hq=8, Hkv=2, d=128, N_b=256, W=64, rank=64, ratio=4)),
     ("bf16-headline-shape", dict(B=2, Hq=32, Hkv=8, d=128, N_b=512, W=256, rank=256, ratio=16)),
     ("bf16-window-only", dict(B=1, Hq=8, Hkv=2, d=128, N_b=0, W=300, rank=64, ratio=4)),
     ("bf16-beacons-only", dict(B=1, Hq=8, Hkv=2, d=128, N_b=300, W=0, rank=64, ratio=8)),
-    ("bf16-simt-d64", dict(B=2, Hq=4, Hkv=1, d=64, N_b=96, W=32, rank=64, ratio=8)),
+    ("bf16-d64", dict(B=2, Hq=4, Hkv=1, d=64, N_b=96, W=32, rank=64, ratio=8)),
+    ("bf16-d64-window-only", dict(B=1, Hq=8, Hkv=2, d=64, N_b=0, W=300, rank=64, ratio=4)),
 ])
 def test_alibi_matches_oracle(case):
     name, kw = case
