@@ -209,3 +209,41 @@ def test_alibi_slopes_follow_the_geometric_rule():
     assert bd.alibi_slopes(8) == [2.0 ** (-i) for i in range(1, 9)]
     s12 = bd.alibi_slopes(12)
     assert s12[:8] == bd.alibi_slopes(8) and s12[8:] == bd.alibi_slopes(16)[0::2][:4]
+
+
+# ---------------------------------------------------------------- prefill (no launch)
+
+def test_prefill_workspace_is_the_staged_queries(lib):
+    # [B, Hkv, rows_pad, 2 d] bf16 with rows_pad = T * G rounded up to 128
+    s = _shape(W=1024)
+    assert bd.workspace_bytes(s, bd.SLIMKV_PREFILL) == 8 * 8 * 4096 * 256 * 2
+    s = _shape(B=1, Hq=10, Hkv=2, N_b=64, r_k=128, r_v=128, W=77)      # 385 rows -> 512
+    assert bd.workspace_bytes(s, bd.SLIMKV_PREFILL) == 1 * 2 * 512 * 256 * 2
+    assert bd.workspace_bytes(_shape(N_b=0, W=100), bd.SLIMKV_PREFILL) > 0     # no beacons
+
+
+@pytest.mark.parametrize("bad", [dict(dtype=bd.SLIMKV_F32), dict(d=64), dict(r_k=96), dict(r_v=320),
+                                 dict(W=0), dict(Hq=30)])
+def test_prefill_rejects_unsupported_shapes(lib, bad):
+    s = _shape(**bad)
+    assert bd.workspace_bytes(s, bd.SLIMKV_PREFILL) == 0
+    st = lib.slimkv_prefill_attn(ctypes.byref(s), *([256] * 7), 256, 256, 256, 1 << 40, None)
+    assert st == 2
+
+
+def test_prefill_rejects_null_and_misaligned_pointers(lib):
+    s = _shape(W=64)
+    ok = [256] * 7
+    assert lib.slimkv_prefill_attn(ctypes.byref(s), *ok, None, 256, 256, 1 << 40, None) == 1     # p0
+    assert lib.slimkv_prefill_attn(ctypes.byref(s), None, *ok[1:], 256, 256, 256, 1 << 40, None) == 1
+    bad = list(ok)
+    bad[3] = 264                                                                                 # K_chunk
+    assert lib.slimkv_prefill_attn(ctypes.byref(s), *bad, 256, 256, 256, 1 << 40, None) == 4
+    assert lib.slimkv_prefill_attn(ctypes.byref(s), *ok, 256, 256, 256, 16, None) == 5           # workspace
+
+
+def test_abort_count_without_a_device_reports_an_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a host without a GPU")
+    assert lib.slimkv_abort_count(0) == -1
