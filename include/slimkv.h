@@ -287,7 +287,8 @@ int slimkv_abi_version(void);
 
 /* Kernel path a call `which` with `shape` takes on the current device:
  * 1 = tcgen05/TMA path (bf16 storage, d == 128, sm_100-family device),
- * 0 = SIMT float32 path (float32 storage, d == 64, or forced), -1 = invalid shape. */
+ * 0 = SIMT float32 path (float32 storage, shapes the tensor-core kernels do not take,
+ * or forced), -1 = invalid shape. */
 int slimkv_kernel_path(const slimkv_shape* shape, int which);
 
 /* Process-wide switch: force the SIMT path for every later call (on != 0), or
@@ -300,7 +301,9 @@ int slimkv_force_simt(int on);
  * right after it (both cudaEvent_t passed as void*, created by the caller), so
  * cudaEventElapsedTime gives that kernel's duration. One-shot; NULL events
  * cancel a pending request. The events also stop the decode kernel from
- * overlapping the kernel before it, so the time measured is the kernel alone. */
+ * overlapping the kernel before it, so the time measured is the kernel alone.
+ * They are recorded as external events (cudaEventRecordExternal), so a call made
+ * under stream capture puts timeable event-record nodes into the graph. */
 void slimkv_time_next_decode(void* start_event, void* stop_event);
 
 #ifdef __cplusplus

@@ -179,13 +179,15 @@ struct DecodeTimer {
 };
 DecodeTimer& decode_timer();
 // Record the pending start event on `st` (before the decode launch).
+// (recorded as external events, so that under stream capture they become event-record
+// nodes of the graph that can be timed, rather than capture-internal dependencies)
 inline void timer_before(cudaStream_t st) {
-    if (decode_timer().start) cudaEventRecord(decode_timer().start, st);
+    if (decode_timer().start) cudaEventRecordWithFlags(decode_timer().start, st, cudaEventRecordExternal);
 }
 // Record the pending stop event on `st` (after the decode launch) and clear the request.
 inline void timer_after(cudaStream_t st) {
     DecodeTimer& t = decode_timer();
-    if (t.stop) cudaEventRecord(t.stop, st);
+    if (t.stop) cudaEventRecordWithFlags(t.stop, st, cudaEventRecordExternal);
     t.start = t.stop = nullptr;
 }
 
