@@ -204,7 +204,8 @@ slimkv_status slimkv_decode_attn_full_kv(const slimkv_shape* shape, const void* 
  *   out      [B, T, Hq, d] f32
  *   workspace >= slimkv_workspace_bytes(shape, SLIMKV_PREFILL) (the staged queries)
  * Runs on the tensor cores only: bf16 storage, d = 128 and, with beacons, r_k and r_v
- * multiples of 64 up to 256; other shapes return SLIMKV_ERR_SHAPE. Same pointer rules
+ * multiples of 64 up to 256, and T * (Hq / Hkv) <= 2^26; other shapes return
+ * SLIMKV_ERR_SHAPE. Same pointer rules
  * and errors as slimkv_decode_attn. */
 slimkv_status slimkv_prefill_attn(const slimkv_shape* shape, const void* q, const void* C_K,
                                   const void* C_V, const void* K_chunk, const void* V_chunk,
@@ -297,8 +298,8 @@ int slimkv_kernel_path(const slimkv_shape* shape, int which);
 int slimkv_force_simt(int on);
 
 /* Measurement hook: the next call made by this host thread records `start_event`
- * on its stream right before launching its split-decode kernel and `stop_event`
- * right after it (both cudaEvent_t passed as void*, created by the caller), so
+ * on its stream right before launching its split-decode kernel (for
+ * slimkv_prefill_attn: its prefill kernel) and `stop_event` right after it (both cudaEvent_t passed as void*, created by the caller), so
  * cudaEventElapsedTime gives that kernel's duration. One-shot; NULL events
  * cancel a pending request. The events also stop the decode kernel from
  * overlapping the kernel before it, so the time measured is the kernel alone.

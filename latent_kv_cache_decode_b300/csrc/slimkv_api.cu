@@ -73,6 +73,8 @@ slimkv_status check_shape(const slimkv_shape* s, int which) {
         // the chunk (W tokens) is always present; the tensor-core prefill kernel covers
         // bf16, d = 128 and ranks that are multiples of 64 up to 256
         if (s->W < 1 || s->dtype != SLIMKV_BF16) return SLIMKV_ERR_SHAPE;
+        // staged query rows per (batch element, KV group): T * G, indexed in int
+        if ((int64_t)s->W * (s->Hq / s->Hkv) > (int64_t(1) << 26)) return SLIMKV_ERR_SHAPE;
         if (!prefill_supported(s->d, s->N_b, s->r_k, s->r_v)) return SLIMKV_ERR_SHAPE;
     }
     return SLIMKV_OK;
