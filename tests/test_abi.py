@@ -223,7 +223,7 @@ def test_prefill_workspace_is_the_staged_queries(lib):
 
 
 @pytest.mark.parametrize("bad", [dict(dtype=bd.SLIMKV_F32), dict(d=64), dict(r_k=96), dict(r_v=320),
-                                 dict(W=0), dict(Hq=30), dict(W=1 << 24)])
+                                 dict(W=0), dict(Hq=30), dict(W=1 << 24, Hq=64)])
 def test_prefill_rejects_unsupported_shapes(lib, bad):
     s = _shape(**bad)
     assert bd.workspace_bytes(s, bd.SLIMKV_PREFILL) == 0
