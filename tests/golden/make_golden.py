@@ -30,7 +30,22 @@ def config0_arrays():
     return lat, rec
 
 
+def prefill_arrays():
+    """A 40-token chunk over the tiny workload's 64 beacons (ALiBi-free prefill rule)."""
+    w = wl.config(0)
+    t = wl.layer_tensors(w, 0)
+    t.update(wl.prefill_chunk(w, 0, 40))
+    f = {k: wl.as_f64(v) for k, v in t.items() if k not in ("q_pos", "p0")}
+    return oracle.prefill_attn(f["q"], f["C_K"], f["C_V"], f["K_chunk"], f["V_chunk"], f["U_K"], f["U_V"],
+                               t["p0"].numpy(), w.scale, w.rope_base)
+
+
 def main():
+    pre = prefill_arrays()
+    np.savetxt(os.path.join(HERE, "config0_prefill_out.txt"), pre.reshape(-1, pre.shape[-1]), fmt="%.17e",
+               header=("tiny fp32 workload (seed 0: B=1, Hq=4, Hkv=1, d=64, N_b=64, r=32), a 40-token chunk "
+                       "at positions 2048..2087 (keys after RoPE, seeded draws); oracle output out[b,t,h,:] "
+                       "one (token, head) per line; written by tests/golden/make_golden.py (prefill_attn)"))
     lat, rec = config0_arrays()
     hdr = ("tiny fp32 workload (seed 0: B=1, Hq=4, Hkv=1, d=64, N_b=64, r=32, W=32, "
            "q at position 2080, RoPE base 10000, scale 1/8); oracle output out[b,h,:] "

@@ -20,6 +20,13 @@ def test_golden_config0_matches_oracle():
     np.testing.assert_allclose(lat, rec, rtol=1e-11, atol=1e-12)
 
 
+def test_golden_prefill_matches_oracle():
+    from tests.golden.make_golden import prefill_arrays
+    pre = prefill_arrays()
+    g = np.loadtxt(os.path.join(HERE, "golden", "config0_prefill_out.txt"))
+    np.testing.assert_allclose(pre.reshape(g.shape), g, rtol=1e-14, atol=1e-15)
+
+
 def test_config_shapes_and_positions():
     c1, c2, c3 = wl.config(1), wl.config(2), wl.config(3)
     assert (c1.B, c1.Hq, c1.Hkv, c1.d, c1.N_b, c1.rank, c1.W, c1.layers) == (1, 32, 8, 128, 4096, 256, 1024, 32)
