@@ -1,6 +1,7 @@
 /*
  * slimkv.h - C ABI of libslimkv: SlimKV reconstruction-free decode attention
- * for one transformer layer and one decode step, on an NVIDIA B300 (sm_103a).
+ * for one transformer layer and one decode step (and its prefill-side and
+ * comparison variants), on an NVIDIA B300 (sm_103a).
  *
  * The method. "Can SlimKV compress KV cache jointly across tokens and features"
  * (wispaper.ai), section "Latent-space attention removes the rebuild step": the
@@ -54,7 +55,10 @@
 extern "C" {
 #endif
 
-/* 2: adds slimkv_append_kv (version 1 calls are unchanged) */
+/* 2: adds slimkv_append_kv; 3: adds slimkv_decode_attn_reconstruct_rope and
+ * slimkv_decode_attn_alibi; 4: adds slimkv_prefill_attn (SLIMKV_PREFILL),
+ * slimkv_abort_count and slimkv_test_withhold_first_load. Earlier calls are
+ * unchanged. */
 #define SLIMKV_ABI_VERSION 4
 
 typedef enum {
