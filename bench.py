@@ -472,11 +472,11 @@ def run_slimkv(args):
     del tgraph
     kern_avg_ms = statistics.mean(kern_ms)
 
-    # end to end through the public API with host buffers: every step copies all
-    # layers' q and q_pos from pinned host memory (one packed transfer), runs the 32
-    # layer calls, and reads all outputs back (one packed transfer), inside the timed
-    # region (the cache is device-resident state, like model weights); the calls run
-    # as a captured graph (`e2e`) and, separately, issued one by one (`eager_value`)
+    # end to end through the public API with host buffers: every step copies every
+    # layer's q and q_pos from pinned host memory, runs the layer calls, and reads every
+    # output back, inside the timed region (the cache is device-resident state, like
+    # model weights); the step runs as a captured graph (`e2e`) and, separately, issued
+    # call by call (`eager_value`)
     L = len(layers)
     q_dev = torch.stack([t["q"] for t in layers])            # [L, B, Hq, d]
     pos_dev = torch.stack([t["q_pos"] for t in layers])      # [L, B]
@@ -494,33 +494,54 @@ def run_slimkv(args):
         for l, t in enumerate(e2e_layers):
             call(l, t)
     torch.cuda.synchronize()
+    # the step's transfers are pipelined with its layers, as a serving loop would: the
+    # layers run in chunks of CH; each chunk's q / q_pos go up on a copy stream ahead of
+    # it (the first chunk before any layer), and its outputs come back on that stream
+    # while the later chunks compute; the step ends when the last outputs are on the host
+    CH = 4
+    chunks = [(c, min(c + CH, L)) for c in range(0, L, CH)]
+    cstream = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in chunks]
+    ev_out = [torch.cuda.Event() for _ in chunks]
+
+    def e2e_step():
+        cstream.wait_stream(stream)   # the previous step is done with q_dev / out_dev
+        with torch.cuda.stream(cstream):
+            for i, (a, z) in enumerate(chunks):
+                q_dev[a:z].copy_(q_host[a:z], non_blocking=True)
+                pos_dev[a:z].copy_(pos_host[a:z], non_blocking=True)
+                ev_in[i].record(cstream)
+        for i, (a, z) in enumerate(chunks):
+            stream.wait_event(ev_in[i])
+            for l in range(a, z):
+                call(l, e2e_layers[l])
+            ev_out[i].record(stream)
+            with torch.cuda.stream(cstream):
+                cstream.wait_event(ev_out[i])
+                out_host[a:z].copy_(out_dev[a:z], non_blocking=True)
+        stream.wait_stream(cstream)   # the step's outputs are on the host
+
     # eager: the 32 library calls issued from Python every step
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(e2e_steps):
-            q_dev.copy_(q_host, non_blocking=True)
-            pos_dev.copy_(pos_host, non_blocking=True)
-            for l, t in enumerate(e2e_layers):
-                call(l, t)
-            out_host.copy_(out_dev, non_blocking=True)
+            e2e_step()
         stream.synchronize()
     e2e_eager_us = (time.perf_counter() - t0) / e2e_steps * 1e6
-    # graph: the same 32 library calls captured once in a CUDA graph (as a serving loop
-    # would), replayed every step between the host copies
+    # graph: the same step (calls and transfers) captured once in a CUDA graph, replayed
     g_e2e = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_e2e, stream=stream):
-        for l, t in enumerate(e2e_layers):
-            call(l, t)
+        e2e_step()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(e2e_steps):
-            q_dev.copy_(q_host, non_blocking=True)
-            pos_dev.copy_(pos_host, non_blocking=True)
             g_e2e.replay()
-            out_host.copy_(out_dev, non_blocking=True)
         stream.synchronize()
     e2e_us = (time.perf_counter() - t0) / e2e_steps * 1e6
+    torch.cuda.synchronize()
+    if not torch.equal(out_host, out_dev.cpu()):
+        raise RuntimeError("end-to-end step: the outputs read back differ from the device outputs")
     del g_e2e
     outs[:] = outs_saved
 
@@ -610,12 +631,12 @@ def run_slimkv(args):
         "clocks": clk.summary(),
         "e2e": {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "how": "host clock around: pinned H2D of all layers' q and q_pos, the "
-                       f"{w.layers} library calls as one captured CUDA graph, D2H of all "
-                       "outputs, stream sync",
+                "how": "host clock around each step: pinned H2D of every layer's q and q_pos and "
+                       f"D2H of every output, pipelined in chunks of 4 layers on a copy stream with the "
+                       f"{w.layers} library calls, all captured in one CUDA graph; stream sync",
                 "eager_value": e2e_eager_us,
-                "eager_how": f"the same, with the {w.layers} library calls issued from Python "
-                             "every step"},
+                "eager_how": f"the same, with the {w.layers} library calls and the transfers issued "
+                             "from Python every step"},
         "gpu_launches": args.steps * w.layers * launches_per_call,
     }
     if loop is not None:
