@@ -430,8 +430,8 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
 }
 
 // Partial write-out of a piece, out of line (once per piece): (m, l) of the piece's
-// real heads from the per-warp row-sum reductions in `red`, and the accumulator
-// columns read from TMEM.
+// real heads from the per-warp row sums in `red` (reduce_row_sums), and the
+// accumulator columns read from TMEM, up to 32 columns per load and its wait.
 template <int NS, int NP>
 __device__ __noinline__ void write_partial_acc(float* ml, float* acc, int* kindp, const float* red,
                                                const float* m_ref_s, int Hq, int Dmax, int slot, int kind, int h0,
@@ -446,27 +446,38 @@ __device__ __noinline__ void write_partial_acc(float* ml, float* acc, int* kindp
 #pragma unroll 1
     for (int cc = 0; cc < nMB; ++cc) {
         const int r = cc * 128 + myrow;
-#pragma unroll 1
-        for (int hc = 0; hc < NS / 16; ++hc) {
-            float v[16];
-            const uint32_t ta = t_acc_lane + cc * aw + hc * 16;
-            ptx::tmem_ld16(ta, v);
-            if (r < dv) {
+        const uint32_t ta = t_acc_lane + cc * aw;
+        float v[NS];
+        if constexpr (NS % 32 == 0) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int h = hc * 16 + i;
-                    if (h < nvalid) acc[((size_t)slot * Hq + h0 + h) * Dmax + r] = v[i];
-                }
+            for (int hc = 0; hc < NS / 32; ++hc) {
+                float w[32];
+                ptx::tmem_ld32(ta + hc * 32, w);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[hc * 32 + i] = w[i];
             }
+        } else {
+#pragma unroll
+            for (int hc = 0; hc < NS / 16; ++hc) {
+                float w[16];
+                ptx::tmem_ld16(ta + hc * 16, w);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[hc * 16 + i] = w[i];
+            }
+        }
+        if (r < dv) {
+#pragma unroll
+            for (int h = 0; h < NS; ++h)
+                if (h < nvalid) acc[((size_t)slot * Hq + h0 + h) * Dmax + r] = v[h];
         }
     }
 }
 
-// End of a piece: reduce the row sums, write (m, l) and the accumulator columns of
-// the piece's real heads to partial slot `slot`.
+// End of a piece, first part: the per-warp row sums of every head into `red`. The
+// sums are final once the piece's last softmax tile is done, so this runs while its
+// last value MMAs are still in flight.
 template <int NS, int NP>
-__device__ __forceinline__ void write_partial(const TcParams& p, const SoftCtx& c, int slot, int kind,
-                                              int h0, int nvalid, int dv, float (&l_part)[NP]) {
+__device__ __forceinline__ void reduce_row_sums(const SoftCtx& c, float (&l_part)[NP]) {
     float v[NS];
 #pragma unroll
     for (int h = 0; h < NS; ++h) v[h] = l_part[h];
@@ -476,6 +487,13 @@ __device__ __forceinline__ void write_partial(const TcParams& p, const SoftCtx& 
         if (c.lane < 16) c.red[c.wq * NP + hc * 16 + c.lane] = wsum;
     }
     ptx::named_bar(1, 128);
+}
+
+// End of a piece, second part (after its last value MMAs): write (m, l) and the
+// accumulator columns of the piece's real heads to partial slot `slot`.
+template <int NS, int NP>
+__device__ __forceinline__ void write_partial(const TcParams& p, const SoftCtx& c, int slot, int kind,
+                                              int h0, int nvalid, int dv) {
     write_partial_acc<NS, NP>(p.ml, p.acc, p.kind, c.red, c.m_ref_s, p.Hq, p.Dmax, slot, kind, h0, nvalid, dv, c.nMB,
                               c.aw, c.t_accp + c.lane_off, c.tid, c.myrow);
 }
@@ -905,11 +923,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 it.next();
             }
             // ---- partial of (CTA, piece): reference max, row sum and accumulator
+            if (lat) reduce_row_sums<NP, NP>(c, l_part);
+            else reduce_row_sums<kNG, NP>(c, l_part);
             ptx::mbar_wait(&bar.vfree[jl % kR], ph_of(jl), abort_flag);   // V(jl) complete
             ptx::tc_fence_after();
             const int slot = p.slot_base[cta] + piece;
-            if (lat) write_partial<NP, NP>(p, c, slot, kSlotLatent, 0, nvalid, p.dv[k], l_part);
-            else write_partial<kNG, NP>(p, c, slot, kSlotRawGroup + pc.g, pc.g * G, nvalid, p.d_raw, l_part);
+            if (lat) write_partial<NP, NP>(p, c, slot, kSlotLatent, 0, nvalid, p.dv[k]);
+            else write_partial<kNG, NP>(p, c, slot, kSlotRawGroup + pc.g, pc.g * G, nvalid, p.d_raw);
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bar.accfree[p.accbuf == 2 ? (piece & 1) : 0]);
             ptx::named_bar(1, 128);
