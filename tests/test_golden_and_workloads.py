@@ -103,3 +103,38 @@ def test_bench_traffic_guard(tmp_path, monkeypatch):
     assert bench._measured_traffic(wl.config(1), "latent") is None
     (tmp_path / rels[0]).write_bytes(open(tmp_path / rels[0], "rb").read() + b"// changed\n")
     assert bench._measured_traffic(w, "latent") is None
+
+
+def _bench_reference(env_extra):
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(HERE)
+    env = dict(os.environ, **env_extra)
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--config", "0",
+                        "--steps", "1", "--warmup", "3"], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    return [json.loads(l) for l in lines]
+
+
+def test_bench_reference_arm_line():
+    # the reference arm times the float64 oracle on the host and prints one JSON line
+    # with the contract's keys, its own metric and an end-to-end record without copies
+    (line,) = _bench_reference({})
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["higher_is_better"] is False
+    assert line["value"] > 0 and line["warmup"] >= 3 and line["dtype"] == "f64"
+    assert line["config"]["workload"] == wl.config(0).name
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_bench_reference_arm_other_ranks_print_nothing():
+    assert _bench_reference({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
