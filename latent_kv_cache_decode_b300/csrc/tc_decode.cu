@@ -95,6 +95,7 @@ struct TcParams {
     int* kind;                        // [slots]
     int Dmax;
     int nslot;                        // ring slots of 32 KB
+    int npbuf;                        // P buffers: 2, or 1 when the ring needs their room
     int accbuf;                       // TMEM accumulator buffers (1 or 2)
     int accstride;                    // TMEM columns of one accumulator buffer
     uint32_t off_q, off_p, off_bar, off_red;
@@ -211,6 +212,7 @@ struct SoftCtx {
     uint32_t t_S, t_accp, lane_off;   // t_accp: accumulator of the current piece
     int tid, wq, lane, myrow, nMB;
     int aw;               // TMEM columns per 128 value rows of the accumulator
+    int npbuf;            // P buffers (1 or 2)
     const float* slope_s; // [NS] ALiBi slopes of the piece's score columns (log2 units)
 };
 
@@ -392,9 +394,9 @@ __device__ __forceinline__ void softmax_tile(const SoftCtx& c, int j, int row0, 
     }
 
     // pass 2: probabilities against the reference, rounded to bf16; the P buffer
-    // (j & 1) is free once the value MMAs of tile j - 2 are done
-    if (j >= 2) ptx::mbar_wait(&c.bar.vfree[(j - 2) % kR], ph_of(j - 2), c.abort);
-    uint8_t* phi = c.pbuf + (j & 1) * SBuf<NP>::PB;
+    // (j mod npbuf) is free once the value MMAs of tile j - npbuf are done
+    if (j >= c.npbuf) ptx::mbar_wait(&c.bar.vfree[(j - c.npbuf) % kR], ph_of(j - c.npbuf), c.abort);
+    uint8_t* phi = c.pbuf + (j & (c.npbuf - 1)) * SBuf<NP>::PB;
 #pragma unroll
     for (int rb = 0; rb < RB; ++rb) {
         const uint32_t tS = tS0 + rb * (LO ? 2 : 1) * NS;
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
     uint8_t* qbuf = smem + p.off_q;          // query operand of the current piece (image copy)
-    uint8_t* pbuf = smem + p.off_p;          // [2][NP/16 blocks][128 * RB rows x 32 B] bf16
+    uint8_t* pbuf = smem + p.off_p;          // [npbuf][NP/16 blocks][128 * RB rows x 32 B] bf16
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     float* red = reinterpret_cast<float*>(smem + p.off_red);   // [4][NP]
     float* m_ref_s = red + 4 * NP;                             // [NP]
@@ -783,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
                 ptx::tc_fence_after();
                 const uint32_t abase = t_acc + (uint32_t)((p.accbuf == 2 ? (pc & 1) : 0) * p.accstride);
                 const uint32_t acc0 = ti.first() ? 0u : 1u;
-                const uint32_t pboff = (uint32_t)(((ti.j & 1) * SBuf<NP>::PB) >> 4);
+                const uint32_t pboff = (uint32_t)(((ti.j & (p.npbuf - 1)) * SBuf<NP>::PB) >> 4);
                 if (ti.pc.k == 0) {
                     const uint64_t pd = dB_P + (uint64_t)pboff;
                     const int nV = (p.dv[0] + 127) >> 7;
@@ -856,6 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
         SoftCtx c;
         c.bar = bar;
         c.pbuf = pbuf;
+        c.npbuf = p.npbuf;
         c.red = red;
         c.m_ref_s = m_ref_s;
         c.alpha_s = alpha_s;
@@ -974,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_decode_kernel(const __grid_con
 
 // Shared-memory plan of one launch.
 struct SmemPlan {
-    int NP, nslot, q_cols, accbuf, accstride;
+    int NP, nslot, q_cols, accbuf, accstride, npbuf;
     uint32_t off_q, off_p, off_bar, off_red, total, tmem_cols;
     bool ok;
 };
@@ -1013,16 +1016,23 @@ SmemPlan plan_smem(int Hq, const int dk[kNumKinds], const int dv[kNumKinds], con
     while ((int)s.tmem_cols < tmem) s.tmem_cols *= 2;
     // query buffer: the latent image (NP rows, bf16) or a raw image (hi and lo parts of kNG heads)
     const int q_bytes = std::max(rows[0] > 0 ? s.NP * round_up(dk[0], 64) * 2 : 0, 2 * kNG * 128 * 2);
-    const int p_bytes = 2 * std::max(s.NP, kNG * kRBRaw) * 256;   // two P buffers (bf16)
     const int nbars = 4 * kR + 5;
     const int misc_bytes = (7 * s.NP + 32) * 4;
-    const int avail = budget - q_bytes - p_bytes - round_up(nbars * 8, 16) - misc_bytes - 1024;
-    s.nslot = std::min(kMaxSlots, avail / kSlot);
     // One tile part (keys or values) must fit the ring. The loads run in consumption
     // order and each waits only for earlier parts to be consumed, so a ring smaller
     // than a key plus a value tile (latent ranks above 256) still drains: it only
-    // serialises those tiles' loads behind their consumers.
-    if (s.nslot < std::max(maxK, maxV)) return s;
+    // serialises those tiles' loads behind their consumers. Two P buffers let the
+    // softmax of a tile run while the value MMAs of the previous one read theirs; when
+    // the ring would not hold a tile part otherwise (64 heads at rank 512), one buffer
+    // serialises the two instead.
+    int p_bytes = 0;
+    for (s.npbuf = 2; s.npbuf >= 1; --s.npbuf) {
+        p_bytes = s.npbuf * std::max(s.NP, kNG * kRBRaw) * 256;   // bf16
+        const int avail = budget - q_bytes - p_bytes - round_up(nbars * 8, 16) - misc_bytes - 1024;
+        s.nslot = std::min(kMaxSlots, avail / kSlot);
+        if (s.nslot >= std::max(maxK, maxV)) break;
+    }
+    if (s.npbuf < 1) return s;
     s.off_q = s.nslot * kSlot;
     s.off_p = s.off_q + q_bytes;
     s.off_bar = s.off_p + p_bytes;
@@ -1310,6 +1320,7 @@ cudaError_t tc_run(const TcCall& c, cudaStream_t st) {
     prm.kind = c.kind;
     prm.Dmax = c.Dmax;
     prm.nslot = sp.nslot;
+    prm.npbuf = sp.npbuf;
     prm.accbuf = sp.accbuf;
     prm.accstride = sp.accstride;
     prm.off_q = sp.off_q;

@@ -114,9 +114,10 @@ EDGE = [
 ]
 
 
-@pytest.mark.parametrize("Hq,rank", [(32, 320), (40, 384), (40, 512), (48, 512)])
+@pytest.mark.parametrize("Hq,rank", [(32, 320), (40, 384), (40, 512), (48, 512), (64, 512)])
 def test_large_ranks_take_the_tensor_core_path(Hq, rank):
-    # (64 heads with rank 512 needs a 64 KB query image and stays on the SIMT path)
+    # (64 heads at rank 512: a 64 KB query image, so the kernel runs with one P buffer
+    # to keep four ring slots)
     w = wl.custom(Hq=Hq, Hkv=8, N_b=256, W=128, rank=rank)
     sh = bd.make_shape(w.B, w.Hq, w.Hkv, w.d, w.N_b, rank, rank, w.W, torch.bfloat16)
     assert bd.kernel_path(sh, bd.SLIMKV_LATENT) == 1
